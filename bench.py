@@ -1,0 +1,420 @@
+"""Benchmark of the multi-scale deformable attention hot path on B300.
+
+One step = one forward and one backward pass (every kernel of the path) over
+the Deformable DETR encoder workload (bs=2, 4-level 100x167 pyramid, 22223
+queries, 8 heads, head_dim 32, 4 points, fp32), inputs resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl native|reference] [--no-cpu-baseline] [--no-e2e]
+
+Prints ONE JSON line (rank 0).  Timing: CUDA events on the launching stream
+around each kernel call of every timed step; L2 is flushed (a write of twice
+the L2 size) before every step, outside the events.  Under torchrun each rank
+runs its own batch (weak scaling, no data-path collective); the step time is
+the max over ranks.  ``--impl reference`` times the fp64 CPU oracle on the
+host cores instead (bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from scale_deformable_attention_05_b300 import inputs as gen  # noqa: E402
+
+METRIC = "MSDeformAttn fwd/bwd sampled points/s (1×B300); achieved GB/s vs HBM roofline"
+FALLBACK_HBM_GBS = 6400.0
+KERNEL_SOURCES = ["msda_device.cuh", "msda_forward.cuh", "msda_backward.cuh", "msda_kernels.cu"]
+
+
+# --------------------------------------------------------------------- utils
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    return FALLBACK_HBM_GBS, "fallback 6.4 TB/s"
+
+
+def _kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "scale_deformable_attention_05_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the sources."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if ":" in line:
+            k, v = line.split(":", 1)
+            rec[k.strip()] = v.strip()
+    if rec.get("source_hash") != _kernel_source_hash():
+        return None
+    v = rec.get(f"{kernel}_dram_bytes_per_launch")
+    return float(v) if v else None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------- reference arm
+def _oracle_step(inp, wl, threads=0):
+    import oracle
+    args = (inp["value"], inp["spatial_shapes"], inp["level_start_index"],
+            inp["sampling_locations"], inp["attention_weights"])
+    oracle.forward(*args, threads=threads)
+    oracle.backward(*args, inp["grad_output"], threads=threads)
+
+
+def _sample_inputs(inp, wl, q_count):
+    """The first q_count queries of the workload (all batches, heads, levels, points)."""
+    s = dict(inp)
+    for k in ("sampling_locations", "attention_weights", "grad_output"):
+        s[k] = np.ascontiguousarray(inp[k][:, :q_count])
+    return s
+
+
+def cpu_baseline(wl, inp, budget_s=12.0, min_reps=1):
+    """Time the oracle (forward + backward) on the host cores; bounded sample."""
+    import oracle
+    threads = oracle.max_threads()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(inp, wl)
+        reps += 1
+        el = time.perf_counter() - t0
+        if reps >= min_reps and (el >= budget_s or el / reps * (reps + 1) > 2.5 * budget_s):
+            break
+    return {"value": wl.points * reps / el, "unit": "points/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{reps} full forward+backward pass(es) of the '{wl.name}' workload "
+                      f"({wl.points} samples each), fp64 C oracle, {el:.1f} s"}
+
+
+def run_reference(args, wl):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    inp = gen.make_inputs(wl)
+    threads = oracle.max_threads()
+    # per step: the first q queries, sized so one step takes about a second
+    t0 = time.perf_counter()
+    probe_q = max(1, wl.num_queries // 16)
+    _oracle_step(_sample_inputs(inp, wl, probe_q), wl)
+    per_q = (time.perf_counter() - t0) / probe_q
+    q = int(max(1, min(wl.num_queries, 1.0 / max(per_q, 1e-9))))
+    sample = _sample_inputs(inp, wl, q)
+    pts = wl.bs * q * wl.num_heads * wl.num_levels * wl.num_points
+    for _ in range(args.warmup):
+        _oracle_step(sample, wl)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(sample, wl)
+    el = time.perf_counter() - t0
+    value = pts * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "points/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(wl, args),
+        "cpu_baseline": {"value": value, "unit": "points/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first {q} of {wl.num_queries} queries per step "
+                                   f"({pts} samples), forward + backward"},
+        "e2e": {"value": value, "unit": "points/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(wl, args):
+    return {"workload": wl.name, "bs": wl.bs, "num_queries": wl.num_queries,
+            "spatial_shapes": [list(s) for s in wl.spatial_shapes], "num_keys": wl.num_keys,
+            "num_heads": wl.num_heads, "head_dim": wl.head_dim, "num_levels": wl.num_levels,
+            "num_points": wl.num_points, "io_dtype": wl.dtype,
+            "passes": "forward+backward",
+            "l2": "flushed before every step (write of 2x L2 size, outside the timed events)",
+            "parallelism": f"replicas x{args.gpus} (each rank its own batch)"}
+
+
+# -------------------------------------------------------------- native arm
+def run_native(args, wl):
+    import torch
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    from scale_deformable_attention_05_b300 import binding as B
+
+    dev = torch.device("cuda", local)
+    # each rank draws its own batch (weak scaling)
+    wl_r = wl.with_(seed=wl.seed + 7919 * rank)
+    inp = gen.make_inputs(wl_r)
+
+    def t(name):
+        if wl.dtype == "bf16":
+            return torch.from_numpy(inp[name + "_bf16"].view(np.int16).copy()).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(inp[name]))
+
+    host = {k: t(k).pin_memory() for k in ("value", "sampling_locations", "attention_weights",
+                                          "grad_output")}
+    d = {k: v.to(dev) for k, v in host.items()}
+    shapes = torch.from_numpy(inp["spatial_shapes"]).to(dev)
+    lsi = torch.from_numpy(inp["level_start_index"]).to(dev)
+    out = torch.empty((wl.bs, wl.num_queries, wl.num_heads * wl.head_dim), dtype=d["value"].dtype,
+                      device=dev)
+    gv = torch.empty_like(d["value"])
+    gl = torch.empty_like(d["sampling_locations"])
+    gw = torch.empty_like(d["attention_weights"])
+    code = B.MSDA_BF16 if wl.dtype == "bf16" else B.MSDA_F32
+    ws_bytes = B.msda_backward_workspace_bytes(wl.bs, wl.num_keys, wl.num_heads, wl.head_dim, code)
+    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    args_fwd = (d["value"], shapes, lsi, d["sampling_locations"], d["attention_weights"])
+
+    # kernels per step (ours): forward 1; backward: zero-fill 1 + main 1 (+ finalize 1 for bf16)
+    launches_per_step = 3 + (1 if wl.dtype == "bf16" else 0)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        B.msda_forward(*args_fwd, output=out, stream=stream)
+        if evs:
+            evs[1].record(stream)
+        if wl.dtype == "f32":
+            B.msda_zero_fill(gv, stream=stream)
+        if evs:
+            evs[2].record(stream)
+        B.msda_backward(*args_fwd, d["grad_output"], gv, gl, gw, workspace=workspace,
+                        accumulate=(wl.dtype == "f32"), stream=stream)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(ev[i])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    zero_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    bwd_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    mean = lambda xs: sum(xs) / len(xs)
+    ms_step = mean(step_ms)
+    if dist:
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+
+    assert B.msda_last_device_error() == 0
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_gv = torch.empty(gv.shape, dtype=gv.dtype).pin_memory()
+        h_gl = torch.empty(gl.shape, dtype=gl.dtype).pin_memory()
+        h_gw = torch.empty(gw.shape, dtype=gw.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = sum(x.numel() * x.element_size() for x in (h_out, h_gv, h_gl, h_gw))
+
+        def e2e_step():
+            for k in host:
+                d[k].copy_(host[k], non_blocking=True)
+            B.msda_forward(*args_fwd, output=out, stream=stream)
+            B.msda_backward(*args_fwd, d["grad_output"], gv, gl, gw, workspace=workspace,
+                            stream=stream)
+            h_out.copy_(out, non_blocking=True)
+            h_gv.copy_(gv, non_blocking=True)
+            h_gl.copy_(gl, non_blocking=True)
+            h_gw.copy_(gw, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, min(args.steps, 10))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        if dist:
+            tt = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        e2e = {"value": wl.points * ws / (e2e_ms / 1e3), "unit": "points/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "path": "pinned host -> device copies, msda_forward, msda_backward, "
+                       "device -> pinned host copies of output and the three gradients"}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    hbm_gbs, peak_src = _peaks()
+    fb = wl.compulsory_bytes(backward=False)
+    bb = wl.compulsory_bytes(backward=True)
+    passes = {
+        "forward": {"kernel": "forward_kernel", "ms": mean(fwd_ms), "min_ms": min(fwd_ms),
+                    "points_per_s": wl.points / (mean(fwd_ms) / 1e3),
+                    "compulsory_bytes": fb, "gbs": fb / (mean(fwd_ms) / 1e3) / 1e9},
+        "zero_fill": {"kernel": "zero_fill_kernel", "ms": mean(zero_ms)},
+        "backward": {"kernel": "backward_kernel" + ("" if wl.dtype == "f32" else
+                                                    " (+zero/finalize)"),
+                     "ms": mean(bwd_ms), "min_ms": min(bwd_ms),
+                     "points_per_s": wl.points / (mean(bwd_ms) / 1e3),
+                     "compulsory_bytes": bb, "gbs": bb / (mean(bwd_ms) / 1e3) / 1e9},
+    }
+    for p in ("forward", "backward"):
+        passes[p]["frac_of_measured_hbm"] = passes[p]["gbs"] / hbm_gbs
+        passes[p]["frac_of_8tbs"] = passes[p]["gbs"] / 8000.0
+    dom = max(("forward", "backward"), key=lambda p: passes[p]["ms"])
+    kname = "forward_kernel" if dom == "forward" else "backward_kernel"
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": passes[dom]["gbs"],
+                "peak": hbm_gbs, "unit": "GB/s", "frac": passes[dom]["gbs"] / hbm_gbs,
+                "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": passes[dom]["compulsory_bytes"],
+                "traffic": _profiled_traffic(wl.name, kname)}
+
+    line = {
+        "metric": METRIC, "value": wl.points * ws / (ms_step / 1e3), "unit": "points/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": _config(wl, args),
+        "roofline": roofline, "passes": passes, "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed_region_incl_flush": wall, "clocks": clocks, "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, gen.make_inputs(wl))
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="encoder", choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    wl = gen.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_native(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,183 @@
+/*
+ * msda.h -- C ABI of the B300 (sm_103a) multi-scale deformable attention library.
+ *
+ * The operator (Deformable DETR walk-through, zhangshiyu.com/post/59697.html,
+ * section "2.2.4 源码分析", ms_deform_attn_core_pytorch and
+ * MSDeformAttn.forward; argument shapes and dtypes from the Ascend
+ * DrivingSDK page "multi_scale_deformable_attn", section "参数说明"):
+ *
+ *   output[b, q, m*D + d] = sum_{l<L} sum_{p<P} attention_weights[b,q,m,l,p] *
+ *                           bilinear_zero(value[b, lsi[l] + y*W_l + x, m, d], x_im, y_im)
+ *   x_im = sampling_locations[b,q,m,l,p,0] * W_l - 0.5
+ *   y_im = sampling_locations[b,q,m,l,p,1] * H_l - 0.5
+ *
+ * i.e. torch grid_sample(mode=bilinear, padding_mode=zeros,
+ * align_corners=False) at grid = 2*loc - 1, per level and head, weighted and
+ * summed over levels and points.  The backward returns the gradients with
+ * respect to value, sampling_locations and attention_weights (the three
+ * gradients of MSDeformAttnFunction.backward on the DQ-DETR ops page,
+ * blog.csdn.net/qq_43298381/article/details/145882935, section "关键代码").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Layouts  All tensors are dense, C-contiguous, innermost index last:
+ *             value               [bs, num_keys, num_heads, head_dim]      (dtype)
+ *             spatial_shapes      [num_levels, 2] int64, rows (H, W)
+ *             level_start_index   [num_levels]    int64
+ *             sampling_loc        [bs, num_queries, num_heads, num_levels, num_points, 2] (dtype), (x, y)
+ *             attn_weight         [bs, num_queries, num_heads, num_levels, num_points]    (dtype)
+ *             output, grad_output [bs, num_queries, num_heads * head_dim]  (dtype)
+ *           Gradients have the shape and dtype of their input.
+ *  Memory   Every tensor pointer is a DEVICE pointer (cudaMalloc or equivalent)
+ *           on the current device, 16-byte aligned.  The caller owns and
+ *           allocates every buffer, including the backward workspace; the
+ *           library allocates nothing and keeps no per-call state.
+ *  Streams  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *           default stream).  Every call only enqueues work on it and returns
+ *           without synchronising, except the two calls marked BLOCKING.
+ *  Numerics fp32 and bf16 inputs both accumulate in fp32.  Pixel coordinates
+ *           are one fp32 fused multiply-add, loc*W - 0.5 rounded once.  A
+ *           sample contributes only when -1 < x_im < W and -1 < y_im < H;
+ *           pixels outside the map count as zero.  bf16 results are rounded
+ *           to nearest even.
+ *  Errors   Arguments are validated on the host before anything is enqueued;
+ *           a failed check returns a non-zero msda_status and enqueues
+ *           nothing.  MSDA_ERR_CUDA reports a launch error from the CUDA
+ *           runtime.  Device-side contents (shapes and start indices
+ *           consistent with num_keys) are preconditions: kernels never read
+ *           outside value for inconsistent levels -- such a level contributes
+ *           nothing and raises the device error word that
+ *           msda_last_device_error() returns.
+ *  Empty    bs, num_queries, num_levels or num_points may be 0; the call then
+ *           writes zeros to its outputs.  num_keys may be 0 only with no
+ *           level holding pixels.
+ *  Threads  Calls are re-entrant; concurrent calls on different streams with
+ *           disjoint outputs are safe.
+ */
+#ifndef MSDA_H_
+#define MSDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSDA_VERSION 1
+
+#if defined(__GNUC__)
+#define MSDA_API __attribute__((visibility("default")))
+#else
+#define MSDA_API
+#endif
+
+/* Element type of value, sampling_loc, attn_weight, output and all gradients.
+ * The Ascend page ("参数说明") lists float32 and float16; bf16 with fp32
+ * accumulation is this library's half-width type. */
+typedef enum { MSDA_F32 = 0, MSDA_BF16 = 1 } msda_dtype;
+
+typedef enum {
+    MSDA_OK = 0,
+    MSDA_ERR_NULL = 1,          /* a required pointer is NULL */
+    MSDA_ERR_DIM = 2,           /* a dimension is negative, or a size overflows the index range */
+    MSDA_ERR_UNSUPPORTED = 3,   /* head_dim % 8 != 0 or > MSDA_MAX_HEAD_DIM, num_levels >
+                                   MSDA_MAX_LEVELS, num_levels*num_points > MSDA_MAX_LEVEL_POINTS,
+                                   unknown dtype or flag */
+    MSDA_ERR_ALIGN = 4,         /* a tensor pointer is not 16-byte aligned */
+    MSDA_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than msda_backward_workspace_bytes() */
+    MSDA_ERR_CUDA = 6,          /* the CUDA runtime reported an error */
+    MSDA_ERR_SHAPES = 7,        /* spatial_shapes / level_start_index inconsistent with num_keys */
+    MSDA_ERR_DEVICE_BOUNDS = 8  /* a kernel met an inconsistent level and skipped it */
+} msda_status;
+
+/* Limits of this implementation.  The Ascend page's envelope ("约束说明":
+ * num_levels*num_points <= 64, num_heads <= 8, embed_dims <= 256,
+ * embed_dims % 8 == 0) lies inside them; num_heads is not limited. */
+#define MSDA_MAX_LEVELS 16
+#define MSDA_MAX_LEVEL_POINTS 256
+#define MSDA_MAX_HEAD_DIM 512
+
+/* Flags of msda_backward. */
+#define MSDA_GRAD_VALUE_ACCUMULATE 1u /* add into grad_value instead of overwriting it */
+
+/*
+ * Forward: writes output [bs, num_queries, num_heads*head_dim].
+ * Defined by ms_deform_attn_core_pytorch (walk-through, "2.2.4 源码分析")
+ * with the interface of mx_driving.multi_scale_deformable_attn (Ascend page,
+ * "接口原型").  output is fully overwritten.  One kernel launch.
+ */
+MSDA_API int msda_forward(const void* value, const int64_t* spatial_shapes,
+                 const int64_t* level_start_index, const void* sampling_loc,
+                 const void* attn_weight, void* output, int bs, int num_keys, int num_heads,
+                 int head_dim, int num_levels, int num_points, int num_queries, int dtype,
+                 void* stream);
+
+/*
+ * Bytes of device workspace msda_backward needs: 0 for MSDA_F32; for
+ * MSDA_BF16 an fp32 accumulator of bs*num_keys*num_heads*head_dim floats.
+ * Returns 0 for invalid arguments as well.
+ */
+MSDA_API size_t msda_backward_workspace_bytes(int bs, int num_keys, int num_heads, int head_dim,
+                                     int dtype);
+
+/*
+ * Backward: gradients of sum(output * grad_output) with respect to value,
+ * sampling_loc and attn_weight (the three tensors MSDeformAttnFunction.backward
+ * returns, DQ-DETR ops page "关键代码").
+ *   grad_sampling_loc and grad_attn_weight are fully overwritten.
+ *   grad_value is overwritten (zero-filled, then accumulated), or added to
+ *   when flags has MSDA_GRAD_VALUE_ACCUMULATE.
+ *   workspace: device buffer of at least msda_backward_workspace_bytes()
+ *   (may be NULL when that is 0); its contents on entry do not matter.
+ * Samples outside the map get zero location and weight gradients.  The
+ * gradient at an integer pixel coordinate is the one of the cell to its
+ * right.  grad_value is summed with fp32 atomics: its last bits may differ
+ * between runs.  Launches: zero-fill (unless accumulating), the gather /
+ * scatter kernel, and for bf16 one fp32->bf16 finalize kernel.
+ */
+MSDA_API int msda_backward(const void* value, const int64_t* spatial_shapes,
+                  const int64_t* level_start_index, const void* sampling_loc,
+                  const void* attn_weight, const void* grad_output, void* grad_value,
+                  void* grad_sampling_loc, void* grad_attn_weight, void* workspace,
+                  size_t workspace_bytes, int bs, int num_keys, int num_heads, int head_dim,
+                  int num_levels, int num_points, int num_queries, int dtype, unsigned flags,
+                  void* stream);
+
+/*
+ * Zero `bytes` bytes of device memory at `ptr` on `stream` with the
+ * library's vectorised fill kernel (ptr 16-byte aligned, bytes a multiple
+ * of 16).  For callers that accumulate gradients across calls with
+ * MSDA_GRAD_VALUE_ACCUMULATE.
+ */
+MSDA_API int msda_zero_fill(void* ptr, size_t bytes, void* stream);
+
+/*
+ * BLOCKING.  Checks on the device that level_start_index is the exclusive
+ * prefix sum of H*W (Ascend page call example; walk-through "2.3.1") and
+ * that the levels add up to num_keys (the assertion at the top of
+ * MSDeformAttn.forward).  Returns MSDA_OK or MSDA_ERR_SHAPES.  Synchronises
+ * `stream`.  A debugging aid: the hot path does not call it.
+ */
+MSDA_API int msda_check_shapes(const int64_t* spatial_shapes, const int64_t* level_start_index,
+                      int num_levels, int num_keys, void* stream);
+
+/*
+ * BLOCKING.  Synchronises `stream`, then returns MSDA_ERR_DEVICE_BOUNDS if
+ * any kernel of this library on the current device met a level whose pixels
+ * fall outside [0, num_keys) since the previous call, else MSDA_OK; clears
+ * the word.
+ */
+MSDA_API int msda_last_device_error(void* stream);
+
+/* Static, human-readable text of a status code. */
+MSDA_API const char* msda_status_string(int status);
+
+/* MSDA_VERSION of the built library. */
+MSDA_API int msda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSDA_H_ */

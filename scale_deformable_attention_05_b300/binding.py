@@ -1,0 +1,227 @@
+"""Thin Python binding of the C ABI in ``include/msda.h`` (``libmsda.so``).
+
+Argument marshalling only: every step of the operator runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors (torch is used for device
+memory and streams); their data pointers, the dims and the current CUDA
+stream are handed to the C functions of the same names.  There is no CPU
+path: if the library is missing this module raises on import, and tensors
+that are not on a CUDA device are rejected.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+__all__ = [
+    "MSDA_F32", "MSDA_BF16", "MSDA_GRAD_VALUE_ACCUMULATE", "MsdaError", "LIB_PATH",
+    "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
+    "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
+    "MSDeformAttnFunction", "ms_deform_attn", "EXPORTED_SYMBOLS", "load_library",
+]
+
+MSDA_F32 = 0
+MSDA_BF16 = 1
+MSDA_GRAD_VALUE_ACCUMULATE = 1
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsda.so")
+EXPORTED_SYMBOLS = (
+    "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
+    "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
+)
+
+_vp = ctypes.c_void_p
+_int = ctypes.c_int
+_DIMS = [_int] * 7
+
+
+class MsdaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {msda_status_string(status)} (status {status})")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with `python -m scale_deformable_attention_05_b300.build`"
+            " (nvcc, sm_103a); there is no fallback implementation")
+    lib = ctypes.CDLL(path)
+    lib.msda_forward.argtypes = [_vp] * 6 + _DIMS + [_int, _vp]
+    lib.msda_forward.restype = _int
+    lib.msda_backward_workspace_bytes.argtypes = [_int] * 5
+    lib.msda_backward_workspace_bytes.restype = ctypes.c_size_t
+    lib.msda_backward.argtypes = [_vp] * 10 + [ctypes.c_size_t] + _DIMS + [_int, ctypes.c_uint, _vp]
+    lib.msda_backward.restype = _int
+    lib.msda_zero_fill.argtypes = [_vp, ctypes.c_size_t, _vp]
+    lib.msda_zero_fill.restype = _int
+    lib.msda_check_shapes.argtypes = [_vp, _vp, _int, _int, _vp]
+    lib.msda_check_shapes.restype = _int
+    lib.msda_last_device_error.argtypes = [_vp]
+    lib.msda_last_device_error.restype = _int
+    lib.msda_status_string.argtypes = [_int]
+    lib.msda_status_string.restype = ctypes.c_char_p
+    lib.msda_version.argtypes = []
+    lib.msda_version.restype = _int
+    return lib
+
+
+_LIB = load_library()
+
+
+def msda_status_string(status: int) -> str:
+    return _LIB.msda_status_string(int(status)).decode()
+
+
+def msda_version() -> int:
+    return int(_LIB.msda_version())
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise MsdaError(fn, status)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MSDA_F32
+    if t.dtype == torch.bfloat16:
+        return MSDA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if t.device.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device (no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _dims(value: torch.Tensor, spatial_shapes: torch.Tensor, sampling_loc: torch.Tensor
+          ) -> Tuple[int, ...]:
+    if value.dim() != 4 or sampling_loc.dim() != 6:
+        raise ValueError("value must be [bs,K,M,D] and sampling_loc [bs,Q,M,L,P,2]")
+    bs, K, M, D = value.shape
+    bs2, Q, M2, L, P, two = sampling_loc.shape
+    if bs2 != bs or M2 != M or two != 2 or spatial_shapes.shape != (L, 2):
+        raise ValueError("inconsistent shapes between value, sampling_loc and spatial_shapes")
+    return int(bs), int(K), int(M), int(D), int(L), int(P), int(Q)
+
+
+def _index(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype != torch.int64:
+        raise TypeError("spatial_shapes and level_start_index must be int64")
+    return t
+
+
+def msda_forward(value: torch.Tensor, spatial_shapes: torch.Tensor,
+                 level_start_index: torch.Tensor, sampling_loc: torch.Tensor,
+                 attn_weight: torch.Tensor, output: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """output [bs, Q, M*D] = MSDeformAttn forward (see include/msda.h)."""
+    bs, K, M, D, L, P, Q = _dims(value, spatial_shapes, sampling_loc)
+    code = _dtype_code(value)
+    if output is None:
+        output = torch.empty((bs, Q, M * D), dtype=value.dtype, device=value.device)
+    _check("msda_forward", _LIB.msda_forward(
+        _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index)),
+        _ptr(sampling_loc), _ptr(attn_weight), _ptr(output), bs, K, M, D, L, P, Q, code,
+        _stream(stream)))
+    return output
+
+
+def msda_backward_workspace_bytes(bs: int, num_keys: int, num_heads: int, head_dim: int,
+                                  dtype: int) -> int:
+    return int(_LIB.msda_backward_workspace_bytes(bs, num_keys, num_heads, head_dim, dtype))
+
+
+def msda_backward(value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
+                  grad_output, grad_value=None, grad_sampling_loc=None, grad_attn_weight=None,
+                  workspace: Optional[torch.Tensor] = None, accumulate: bool = False,
+                  stream=None):
+    """(grad_value, grad_sampling_loc, grad_attn_weight) of MSDeformAttn (see include/msda.h)."""
+    bs, K, M, D, L, P, Q = _dims(value, spatial_shapes, sampling_loc)
+    code = _dtype_code(value)
+    dev, dt = value.device, value.dtype
+    if grad_value is None:
+        grad_value = torch.empty_like(value)
+    if grad_sampling_loc is None:
+        grad_sampling_loc = torch.empty_like(sampling_loc)
+    if grad_attn_weight is None:
+        grad_attn_weight = torch.empty_like(attn_weight)
+    need = msda_backward_workspace_bytes(bs, K, M, D, code)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("msda_backward", _LIB.msda_backward(
+        _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index)),
+        _ptr(sampling_loc), _ptr(attn_weight), _ptr(grad_output), _ptr(grad_value),
+        _ptr(grad_sampling_loc), _ptr(grad_attn_weight),
+        _ptr(workspace) if workspace is not None else None, ws_bytes,
+        bs, K, M, D, L, P, Q, code, MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0,
+        _stream(stream)))
+    return grad_value, grad_sampling_loc, grad_attn_weight
+
+
+def msda_zero_fill(t: torch.Tensor, stream=None) -> torch.Tensor:
+    _check("msda_zero_fill", _LIB.msda_zero_fill(_ptr(t), t.numel() * t.element_size(),
+                                                 _stream(stream)))
+    return t
+
+
+def msda_check_shapes(spatial_shapes: torch.Tensor, level_start_index: torch.Tensor,
+                      num_keys: int, stream=None) -> int:
+    """BLOCKING. 0 (MSDA_OK) or 7 (MSDA_ERR_SHAPES); raises on other errors."""
+    st = _LIB.msda_check_shapes(_ptr(_index(spatial_shapes)), _ptr(_index(level_start_index)),
+                                int(spatial_shapes.shape[0]), int(num_keys), _stream(stream))
+    if st not in (0, 7):
+        _check("msda_check_shapes", st)
+    return st
+
+
+def msda_last_device_error(stream=None) -> int:
+    """BLOCKING. 0, or 8 (MSDA_ERR_DEVICE_BOUNDS) when a kernel skipped an inconsistent level."""
+    st = _LIB.msda_last_device_error(_stream(stream))
+    if st not in (0, 8):
+        _check("msda_last_device_error", st)
+    return st
+
+
+class MSDeformAttnFunction(torch.autograd.Function):
+    """Autograd wrapper with the argument order of the DQ-DETR ops page's
+    ``MSDeformAttnFunction``: (value, spatial_shapes, level_start_index,
+    sampling_loc, attn_weight, im2col_step).  ``im2col_step`` is accepted and
+    ignored (the kernels keep no column buffer).  backward returns
+    (grad_value, None, None, grad_sampling_loc, grad_attn_weight, None)."""
+
+    @staticmethod
+    def forward(ctx, value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
+                im2col_step=64):
+        value, sampling_loc, attn_weight = (value.contiguous(), sampling_loc.contiguous(),
+                                            attn_weight.contiguous())
+        out = msda_forward(value, spatial_shapes, level_start_index, sampling_loc, attn_weight)
+        ctx.save_for_backward(value, spatial_shapes, level_start_index, sampling_loc, attn_weight)
+        return out
+
+    @staticmethod
+    def backward(ctx, grad_output):
+        value, spatial_shapes, level_start_index, sampling_loc, attn_weight = ctx.saved_tensors
+        gv, gl, ga = msda_backward(value, spatial_shapes, level_start_index, sampling_loc,
+                                   attn_weight, grad_output.contiguous())
+        return gv, None, None, gl, ga, None
+
+
+def ms_deform_attn(value, spatial_shapes, level_start_index, sampling_loc, attn_weight):
+    return MSDeformAttnFunction.apply(value, spatial_shapes, level_start_index, sampling_loc,
+                                      attn_weight, 64)

@@ -1,0 +1,243 @@
+// All device code of the library, in one translation unit: the forward and
+// backward kernels (instantiated per element type and lane layout), the
+// fill / finalize / shape-check kernels, and the host-side launchers the
+// C ABI calls.
+#include <algorithm>
+
+#include "msda_backward.cuh"
+#include "msda_device.cuh"
+#include "msda_forward.cuh"
+#include "msda_launch.h"
+
+namespace msda {
+
+__device__ int g_shape_check = 0;
+
+// ------------------------------------------------------------ small kernels
+// Grid-stride 16-byte zero fill; n16 = number of 16-byte words.
+__global__ void zero_fill_kernel(uint4* __restrict__ p, size_t n16) {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+         i += (size_t)gridDim.x * blockDim.x)
+        p[i] = z;
+}
+
+// bf16 grad_value from the fp32 workspace: overwrite, or add when accumulating.
+// n8 = number of 8-element groups (head_dim % 8 == 0 makes the total a multiple of 8).
+__global__ void finalize_bf16_kernel(const float4* __restrict__ ws, uint4* __restrict__ gv,
+                                     size_t n8, int accumulate) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const float4 a = __ldcs(ws + 2 * i), b = __ldcs(ws + 2 * i + 1);
+        float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        if (accumulate) {
+            const uint4 old = gv[i];
+            v[0] += bf16_lo(old.x); v[1] += bf16_hi(old.x);
+            v[2] += bf16_lo(old.y); v[3] += bf16_hi(old.y);
+            v[4] += bf16_lo(old.z); v[5] += bf16_hi(old.z);
+            v[6] += bf16_lo(old.w); v[7] += bf16_hi(old.w);
+        }
+        uint4 o;
+        o.x = pack_bf16x2(v[0], v[1]); o.y = pack_bf16x2(v[2], v[3]);
+        o.z = pack_bf16x2(v[4], v[5]); o.w = pack_bf16x2(v[6], v[7]);
+        __stcs(gv + i, o);
+    }
+}
+
+// One thread: level_start_index must be the exclusive prefix sum of H*W and
+// the levels must add up to num_keys.
+__global__ void check_shapes_kernel(const int64_t* __restrict__ shapes,
+                                    const int64_t* __restrict__ lsi, int num_levels,
+                                    int num_keys) {
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    int64_t acc = 0;
+    int ok = 1;
+    for (int l = 0; l < num_levels; ++l) {
+        const int64_t H = shapes[2 * l], W = shapes[2 * l + 1];
+        if (H < 0 || W < 0 || lsi[l] != acc) ok = 0;
+        acc += H * W;
+    }
+    if (acc != (int64_t)num_keys) ok = 0;
+    g_shape_check = ok;
+}
+
+// ---------------------------------------------------------------- dispatch
+namespace {
+
+constexpr int kRowItersFwd = 2;  // lane-group rows per warp in one CTA, forward
+constexpr int kRowItersBwd = 2;
+constexpr int kMaxPtsPerWarpFwd = 512;
+constexpr int kMaxPtsPerWarpBwd = 256;
+
+int next_pow2(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+struct Layout {
+    int lanes, vpl;
+};
+
+// Lanes per row group and 16-byte vectors per lane for a head of `nvec`
+// vectors and L*P samples per row.
+Layout choose_layout(int nvec, int LP, int max_pts_per_warp) {
+    Layout ly;
+    if (nvec <= 32) {
+        ly.lanes = next_pow2(nvec);
+        ly.vpl = 1;
+        while (ly.lanes < 32 && (32 / ly.lanes) * LP > max_pts_per_warp) ly.lanes <<= 1;
+    } else {
+        ly.lanes = 32;
+        ly.vpl = (nvec + 31) / 32 <= 2 ? 2 : 4;
+    }
+    return ly;
+}
+
+template <typename K>
+void allow_big_smem(K kernel, size_t smem) {
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+template <typename T, int kLanes, int kVPL>
+cudaError_t launch_forward_t(const Problem& pb, void* out, cudaStream_t st) {
+    constexpr int kGroups = 32 / kLanes;
+    const int LP = pb.L * pb.P;
+    const int rows = pb.bs * pb.Q * pb.M;
+    const int rows_per_warp = kGroups * kRowItersFwd;
+    const int rows_per_cta = rows_per_warp * kWarpsPerCta;
+    const size_t smem = sizeof(LevelInfo) * kMaxLevels +
+                        (size_t)kWarpsPerCta * kGroups * LP * (sizeof(float4) + sizeof(int2));
+    auto kernel = forward_kernel<T, kLanes, kVPL>;
+    allow_big_smem(kernel, smem);
+    const int grid = (rows + rows_per_cta - 1) / rows_per_cta;
+    kernel<<<grid, kThreadsPerCta, smem, st>>>(
+        static_cast<const T*>(pb.value), pb.shapes, pb.lsi, static_cast<const T*>(pb.loc),
+        static_cast<const T*>(pb.attn), static_cast<T*>(out), pb.K, pb.M, pb.D, pb.L, pb.P, pb.Q,
+        rows, rows_per_warp);
+    return cudaGetLastError();
+}
+
+template <typename T, int kLanes, int kVPL>
+cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv32,
+                              void* grad_loc, void* grad_attn, cudaStream_t st) {
+    constexpr int kGroups = 32 / kLanes;
+    const int LP = pb.L * pb.P;
+    const int rows = pb.bs * pb.Q * pb.M;
+    const int rows_per_warp = kGroups * kRowItersBwd;
+    const int rows_per_cta = rows_per_warp * kWarpsPerCta;
+    const size_t smem = sizeof(LevelInfo) * kMaxLevels +
+                        (size_t)kWarpsPerCta * kGroups * LP * (3 * sizeof(float4) + sizeof(int2));
+    auto kernel = backward_kernel<T, kLanes, kVPL>;
+    allow_big_smem(kernel, smem);
+    const int grid = (rows + rows_per_cta - 1) / rows_per_cta;
+    kernel<<<grid, kThreadsPerCta, smem, st>>>(
+        static_cast<const T*>(pb.value), pb.shapes, pb.lsi, static_cast<const T*>(pb.loc),
+        static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
+        static_cast<T*>(grad_loc), static_cast<T*>(grad_attn), pb.K, pb.M, pb.D, pb.L, pb.P,
+        pb.Q, rows, rows_per_warp);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_forward(const Problem& pb, void* out, cudaStream_t st) {
+    const Layout ly = choose_layout(pb.D / IO<T>::kVec, pb.L * pb.P, kMaxPtsPerWarpFwd);
+    if (ly.vpl == 1) {
+        switch (ly.lanes) {
+            case 1: return launch_forward_t<T, 1, 1>(pb, out, st);
+            case 2: return launch_forward_t<T, 2, 1>(pb, out, st);
+            case 4: return launch_forward_t<T, 4, 1>(pb, out, st);
+            case 8: return launch_forward_t<T, 8, 1>(pb, out, st);
+            case 16: return launch_forward_t<T, 16, 1>(pb, out, st);
+            default: return launch_forward_t<T, 32, 1>(pb, out, st);
+        }
+    }
+    if (ly.vpl == 2) return launch_forward_t<T, 32, 2>(pb, out, st);
+    return launch_forward_t<T, 32, 4>(pb, out, st);
+}
+
+template <typename T>
+cudaError_t dispatch_backward(const Problem& pb, const void* g, float* gv32, void* gl, void* ga,
+                              cudaStream_t st) {
+    const Layout ly = choose_layout(pb.D / IO<T>::kVec, pb.L * pb.P, kMaxPtsPerWarpBwd);
+    if (ly.vpl == 1) {
+        switch (ly.lanes) {
+            case 1: return launch_backward_t<T, 1, 1>(pb, g, gv32, gl, ga, st);
+            case 2: return launch_backward_t<T, 2, 1>(pb, g, gv32, gl, ga, st);
+            case 4: return launch_backward_t<T, 4, 1>(pb, g, gv32, gl, ga, st);
+            case 8: return launch_backward_t<T, 8, 1>(pb, g, gv32, gl, ga, st);
+            case 16: return launch_backward_t<T, 16, 1>(pb, g, gv32, gl, ga, st);
+            default: return launch_backward_t<T, 32, 1>(pb, g, gv32, gl, ga, st);
+        }
+    }
+    if (ly.vpl == 2) return launch_backward_t<T, 32, 2>(pb, g, gv32, gl, ga, st);
+    return launch_backward_t<T, 32, 4>(pb, g, gv32, gl, ga, st);
+}
+
+int grid_for(size_t n, int threads) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t want = (n + threads - 1) / threads;
+    return (int)std::max<size_t>(1, std::min<size_t>(want, (size_t)sms * 8));
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const Problem& pb, void* out, int dtype, cudaStream_t st) {
+    if (dtype == 0) return dispatch_forward<float>(pb, out, st);
+    return dispatch_forward<__nv_bfloat16>(pb, out, st);
+}
+
+cudaError_t launch_backward(const Problem& pb, const void* grad_out, float* gv32, void* grad_loc,
+                            void* grad_attn, int dtype, cudaStream_t st) {
+    if (dtype == 0) return dispatch_backward<float>(pb, grad_out, gv32, grad_loc, grad_attn, st);
+    return dispatch_backward<__nv_bfloat16>(pb, grad_out, gv32, grad_loc, grad_attn, st);
+}
+
+cudaError_t launch_zero_fill(void* p, size_t bytes, cudaStream_t st) {
+    const size_t n16 = bytes / 16;
+    if (n16 == 0) return cudaSuccess;
+    zero_fill_kernel<<<grid_for(n16, 256), 256, 0, st>>>(static_cast<uint4*>(p), n16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_bf16(const float* ws, void* grad_value, size_t elems, bool accumulate,
+                                 cudaStream_t st) {
+    const size_t n8 = elems / 8;
+    if (n8 == 0) return cudaSuccess;
+    finalize_bf16_kernel<<<grid_for(n8, 256), 256, 0, st>>>(
+        reinterpret_cast<const float4*>(ws), static_cast<uint4*>(grad_value), n8,
+        accumulate ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t check_shapes_blocking(const int64_t* shapes, const int64_t* lsi, int num_levels,
+                                  int num_keys, cudaStream_t st, bool* ok) {
+    check_shapes_kernel<<<1, 32, 0, st>>>(shapes, lsi, num_levels, num_keys);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    int h = 0;
+    e = cudaMemcpyFromSymbolAsync(&h, g_shape_check, sizeof(int), 0, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(st);
+    *ok = (h != 0);
+    return e;
+}
+
+cudaError_t read_and_clear_error(cudaStream_t st, unsigned* word) {
+    unsigned h = 0;
+    const unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&h, g_error_word, sizeof(unsigned), 0,
+                                              cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbolAsync(g_error_word, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice,
+                                st);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(st);
+    *word = h;
+    return e;
+}
+
+}  // namespace msda

@@ -1,0 +1,32 @@
+// Host-side launchers between the C ABI (msda_api.cpp) and the device code
+// (msda_kernels.cu).  Arguments are already validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace msda {
+
+struct Problem {
+    const void* value;
+    const int64_t* shapes;
+    const int64_t* lsi;
+    const void* loc;
+    const void* attn;
+    int bs, K, M, D, L, P, Q;
+};
+
+cudaError_t launch_forward(const Problem& pb, void* out, int dtype, cudaStream_t st);
+// gv32: fp32 grad_value accumulator (the caller's fp32 grad_value, or the
+// bf16 path's workspace), already zeroed or holding the sum to add to.
+cudaError_t launch_backward(const Problem& pb, const void* grad_out, float* gv32, void* grad_loc,
+                            void* grad_attn, int dtype, cudaStream_t st);
+cudaError_t launch_zero_fill(void* p, size_t bytes, cudaStream_t st);
+cudaError_t launch_finalize_bf16(const float* ws, void* grad_value, size_t elems, bool accumulate,
+                                 cudaStream_t st);
+cudaError_t check_shapes_blocking(const int64_t* shapes, const int64_t* lsi, int num_levels,
+                                  int num_keys, cudaStream_t st, bool* ok);
+cudaError_t read_and_clear_error(cudaStream_t st, unsigned* word);
+
+}  // namespace msda

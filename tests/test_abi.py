@@ -1,0 +1,152 @@
+"""The C ABI library loads, exports every symbol include/msda.h declares, and
+rejects bad arguments on the host before touching the device.
+
+No test here launches device work: every call made below fails a host-side
+check and returns before the first CUDA runtime call, so these run on a
+machine without a GPU.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from scale_deformable_attention_05_b300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msda.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MSDA_API\s+[\w\s\*]+?\b(msda_\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared_functions()
+    assert set(B.EXPORTED_SYMBOLS) <= set(names)
+    assert len(names) >= 8
+
+
+def test_library_exports_every_declared_symbol():
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [n for n in _declared_functions() if n not in exported]
+    assert not missing, missing
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for n in _declared_functions():
+        assert getattr(lib, n) is not None
+
+
+def test_library_exports_nothing_else():
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == set(_declared_functions())
+
+
+def test_version_and_status_strings():
+    assert B.msda_version() == 1
+    for code in range(9):
+        s = B.msda_status_string(code)
+        assert s and s != "unknown status"
+    assert B.msda_status_string(99) == "unknown status"
+
+
+def test_workspace_bytes():
+    assert B.msda_backward_workspace_bytes(2, 22223, 8, 32, B.MSDA_F32) == 0
+    assert B.msda_backward_workspace_bytes(4, 22223, 8, 32, B.MSDA_BF16) == 4 * 22223 * 8 * 32 * 4
+    assert B.msda_backward_workspace_bytes(-1, 10, 8, 32, B.MSDA_BF16) == 0
+
+
+# ----------------------------------------------------- host-side rejections
+L = B._LIB
+A = 0x10000  # an aligned, never-dereferenced stand-in address
+DIMS = dict(bs=1, K=10000, M=4, D=32, L=1, P=8, Q=16)
+
+
+def _fwd(value=A, shapes=A, lsi=A, loc=A, w=A, out=A, dtype=0, **kw):
+    d = dict(DIMS, **kw)
+    return L.msda_forward(value, shapes, lsi, loc, w, out, d["bs"], d["K"], d["M"], d["D"],
+                          d["L"], d["P"], d["Q"], dtype, None)
+
+
+def _bwd(value=A, shapes=A, lsi=A, loc=A, w=A, g=A, gv=A, gl=A, gw=A, ws=None, ws_bytes=0,
+         dtype=0, flags=0, **kw):
+    d = dict(DIMS, **kw)
+    return L.msda_backward(value, shapes, lsi, loc, w, g, gv, gl, gw, ws, ws_bytes, d["bs"],
+                           d["K"], d["M"], d["D"], d["L"], d["P"], d["Q"], dtype, flags, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(out=None), 1),
+    (dict(value=None), 1),
+    (dict(loc=None), 1),
+    (dict(w=None), 1),
+    (dict(shapes=None), 1),
+    (dict(lsi=None), 1),
+    (dict(bs=-1), 2),
+    (dict(Q=-3), 2),
+    (dict(D=12), 3),
+    (dict(D=520), 3),
+    (dict(L=17, P=1), 3),
+    (dict(L=4, P=65), 3),
+    (dict(dtype=2), 3),
+    (dict(value=A + 8), 4),
+    (dict(loc=A + 4), 4),
+    (dict(out=A + 2), 4),
+    (dict(bs=70000, Q=70000), 2),
+])
+def test_forward_rejects_on_host(kw, status):
+    assert _fwd(**kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(gv=None), 1),
+    (dict(gl=None), 1),
+    (dict(gw=None), 1),
+    (dict(g=None), 1),
+    (dict(flags=2), 3),
+    (dict(D=4), 3),
+    (dict(gl=A + 8), 4),
+    (dict(dtype=1), 5),                       # bf16 needs a workspace
+    (dict(dtype=1, ws=A, ws_bytes=16), 5),    # too small
+    (dict(dtype=1, ws=A + 4, ws_bytes=1 << 30), 4),
+])
+def test_backward_rejects_on_host(kw, status):
+    assert _bwd(**kw) == status
+
+
+def test_zero_fill_and_check_shapes_reject_on_host():
+    assert L.msda_zero_fill(None, 16, None) == 1
+    assert L.msda_zero_fill(A + 4, 16, None) == 4
+    assert L.msda_zero_fill(A, 15, None) == 4
+    assert L.msda_zero_fill(None, 0, None) == 0
+    assert L.msda_check_shapes(None, None, 1, 10, None) == 1
+    assert L.msda_check_shapes(A, A, 17, 10, None) == 3
+    assert L.msda_check_shapes(A, A, -1, 10, None) == 2
+    assert L.msda_check_shapes(None, None, 0, 0, None) == 0
+    assert L.msda_check_shapes(None, None, 0, 5, None) == 7
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    v = torch.zeros(1, 4, 1, 8)
+    loc = torch.zeros(1, 2, 1, 1, 1, 2)
+    w = torch.zeros(1, 2, 1, 1, 1)
+    shapes = torch.tensor([[2, 2]])
+    lsi = torch.tensor([0])
+    with pytest.raises(ValueError, match="CUDA"):
+        B.msda_forward(v, shapes, lsi, loc, w)
+
+
+def test_product_path_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "scale_deformable_attention_05_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "msda_oracle" not in text and "liboracle" not in text, f

@@ -14,12 +14,14 @@ namespace msda {
 __device__ int g_shape_check = 0;
 
 // ------------------------------------------------------------ small kernels
-// Grid-stride 16-byte zero fill; n16 = number of 16-byte words.
-__global__ void zero_fill_kernel(uint4* __restrict__ p, size_t n16) {
+// Grid-stride zero fill: n16 16-byte words, then tail_bytes (< 16) single bytes.
+__global__ void zero_fill_kernel(uint4* __restrict__ p, size_t n16, int tail_bytes) {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
          i += (size_t)gridDim.x * blockDim.x)
         p[i] = z;
+    if (blockIdx.x == 0 && threadIdx.x < tail_bytes)
+        reinterpret_cast<unsigned char*>(p + n16)[threadIdx.x] = 0;
 }
 
 // bf16 grad_value from the fp32 workspace: overwrite, or add when accumulating.
@@ -197,9 +199,10 @@ cudaError_t launch_backward(const Problem& pb, const void* grad_out, float* gv32
 }
 
 cudaError_t launch_zero_fill(void* p, size_t bytes, cudaStream_t st) {
+    if (bytes == 0) return cudaSuccess;
     const size_t n16 = bytes / 16;
-    if (n16 == 0) return cudaSuccess;
-    zero_fill_kernel<<<grid_for(n16, 256), 256, 0, st>>>(static_cast<uint4*>(p), n16);
+    zero_fill_kernel<<<grid_for(n16 + 1, 256), 256, 0, st>>>(static_cast<uint4*>(p), n16,
+                                                              (int)(bytes % 16));
     return cudaGetLastError();
 }
 

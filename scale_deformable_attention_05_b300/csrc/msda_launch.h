@@ -22,6 +22,7 @@ cudaError_t launch_forward(const Problem& pb, void* out, int dtype, cudaStream_t
 // bf16 path's workspace), already zeroed or holding the sum to add to.
 cudaError_t launch_backward(const Problem& pb, const void* grad_out, float* gv32, void* grad_loc,
                             void* grad_attn, int dtype, cudaStream_t st);
+// Zeroes `bytes` bytes at p (16-byte aligned; any byte count).
 cudaError_t launch_zero_fill(void* p, size_t bytes, cudaStream_t st);
 cudaError_t launch_finalize_bf16(const float* ws, void* grad_value, size_t elems, bool accumulate,
                                  cudaStream_t st);

@@ -158,6 +158,24 @@ def test_out_of_range_and_empty_inputs(B):
         assert torch.all(gl == 0) and torch.all(gw == 0)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_no_value_rows_zero_fills_odd_sized_gradients(B, dtype):
+    """head_dim 0 leaves nothing to read: every gradient, of any element count, is zeroed."""
+    shapes = ((3, 3),)
+    v = torch.ones(1, 9, 1, 0, device="cuda", dtype=dtype)
+    loc = torch.rand(1, 3, 1, 1, 3, 2, device="cuda").to(dtype)   # 9 samples: odd sizes
+    w = torch.rand(1, 3, 1, 1, 3, device="cuda").to(dtype)
+    g = torch.ones(1, 3, 0, device="cuda", dtype=dtype)
+    sh = torch.tensor(shapes, device="cuda")
+    lsi = torch.tensor([0], device="cuda")
+    gv = torch.empty_like(v)
+    gl = torch.full_like(loc, 5.0)
+    gw = torch.full_like(w, 5.0)
+    B.msda_backward(v, sh, lsi, loc, w, g, gv, gl, gw)
+    torch.cuda.synchronize()
+    assert torch.all(gl == 0) and torch.all(gw == 0)
+
+
 def test_inconsistent_level_is_skipped_and_reported(B):
     """A level whose pixels fall past num_keys contributes nothing and raises the
     device error word; the kernels read nothing outside value."""

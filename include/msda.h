@@ -173,6 +173,35 @@ MSDA_API int msda_last_device_error(void* stream);
 /* Static, human-readable text of a status code. */
 MSDA_API const char* msda_status_string(int status);
 
+/*
+ * Allocation-free bf16 backward.  No counterpart in the paper: an addition for
+ * callers that cannot allocate device memory (a host framework that owns every
+ * allocation, a plug-in without access to the allocator, code that must not
+ * call cudaMalloc while work is captured or timed).  Same arguments, results
+ * and launches as msda_backward with dtype MSDA_BF16, except that there is no
+ * workspace argument: the fp32 accumulator is a fixed array of
+ * MSDA_NOALLOC_MAX_WORKSPACE_BYTES in the library's own device memory, which
+ * every GPU that loads the library holds until the process exits.
+ *   - Returns MSDA_ERR_WORKSPACE when bs*num_keys*num_heads*head_dim*4 exceeds
+ *     MSDA_NOALLOC_MAX_WORKSPACE_BYTES, and MSDA_ERR_UNSUPPORTED for any dtype
+ *     but MSDA_BF16 (the fp32 backward needs no workspace: use msda_backward).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and zero-fills the part it
+ *     uses before accumulating; calls whose work overlaps on the GPU (other
+ *     streams, other host threads) race on it and must be serialised.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define MSDA_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)64 << 20)
+MSDA_API int msda_backward_noalloc(const void* value, const int64_t* spatial_shapes,
+                                   const int64_t* level_start_index, const void* sampling_loc,
+                                   const void* attn_weight, const void* grad_output,
+                                   void* grad_value, void* grad_sampling_loc,
+                                   void* grad_attn_weight, int bs, int num_keys, int num_heads,
+                                   int head_dim, int num_levels, int num_points, int num_queries,
+                                   int dtype, unsigned flags, void* stream);
+
 /* MSDA_VERSION of the built library. */
 MSDA_API int msda_version(void);
 

@@ -19,7 +19,7 @@ __all__ = [
     "MSDA_F32", "MSDA_BF16", "MSDA_GRAD_VALUE_ACCUMULATE", "MsdaError", "LIB_PATH",
     "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
-    "MSDeformAttnFunction", "ms_deform_attn", "EXPORTED_SYMBOLS", "load_library",
+    "msda_backward_noalloc", "MSDeformAttnFunction", "ms_deform_attn", "EXPORTED_SYMBOLS", "load_library",
 ]
 
 MSDA_F32 = 0
@@ -30,6 +30,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsda.so"
 EXPORTED_SYMBOLS = (
     "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
+    "msda_backward_noalloc",
 )
 
 _vp = ctypes.c_void_p
@@ -65,6 +66,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msda_status_string.restype = ctypes.c_char_p
     lib.msda_version.argtypes = []
     lib.msda_version.restype = _int
+    lib.msda_backward_noalloc.argtypes = [_vp] * 9 + _DIMS + [_int, ctypes.c_uint, _vp]
+    lib.msda_backward_noalloc.restype = _int
     return lib
 
 
@@ -171,6 +174,21 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_loc, attn_w
         _ptr(workspace) if workspace is not None else None, ws_bytes,
         bs, K, M, D, L, P, Q, code, MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0,
         _stream(stream)))
+    return grad_value, grad_sampling_loc, grad_attn_weight
+
+
+def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
+                          grad_output, grad_value, grad_sampling_loc, grad_attn_weight,
+                          accumulate: bool = False, stream=None):
+    """bf16 backward into caller-provided gradient tensors, with the library's own
+    fixed scratch array instead of a workspace (see msda_backward_noalloc in
+    include/msda.h); the library allocates nothing."""
+    bs, K, M, D, L, P, Q = _dims(value, spatial_shapes, sampling_loc)
+    _check("msda_backward_noalloc", _LIB.msda_backward_noalloc(
+        _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index)),
+        _ptr(sampling_loc), _ptr(attn_weight), _ptr(grad_output), _ptr(grad_value),
+        _ptr(grad_sampling_loc), _ptr(grad_attn_weight), bs, K, M, D, L, P, Q,
+        _dtype_code(value), MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0, _stream(stream)))
     return grad_value, grad_sampling_loc, grad_attn_weight
 
 

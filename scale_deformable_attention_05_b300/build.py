@@ -14,7 +14,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libmsda.so")
-SOURCES = ["msda_kernels.cu", "msda_api.cpp"]
+SOURCES = ["msda_kernels.cu", "msda_api.cpp", "msda_noalloc.cu"]
 HEADERS = ["msda_device.cuh", "msda_forward.cuh", "msda_backward.cuh", "msda_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,0 +1,122 @@
+// Allocation-free variant of the bf16 backward (msda_backward_noalloc).
+//
+// The bf16 backward accumulates grad_value in an fp32 scratch buffer before
+// rounding it to bf16.  msda_backward takes that buffer from the caller.  Some
+// callers cannot allocate device memory at all: code running inside a
+// framework's memory pool that forbids extra allocations, plug-ins whose host
+// application owns every allocation, or processes that must not call
+// cudaMalloc while other work is being captured or timed.  This entry point
+// serves them: its scratch is a fixed-size array in the library's own device
+// memory, so the caller only passes inputs and outputs.
+//
+// The array is file-scope device memory.  On the host its name is only a
+// stand-in symbol, never a device address: the address is looked up with
+// cudaGetSymbolAddress once per device (the first call on that device, made
+// with that device current) and cached.  That first call should therefore come
+// before any stream capture.  Every call on a device shares the one array and
+// zero-fills it before use; calls whose work overlaps on the GPU race on it.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/msda.h"
+#include "msda_launch.h"
+
+// Held by every GPU that loads the library, until the process exits.
+static __device__ __align__(256) float g_noalloc_scratch[MSDA_NOALLOC_MAX_WORKSPACE_BYTES /
+                                                        sizeof(float)];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+float* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up once per device).
+int scratch_for_current_device(float** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MSDA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MSDA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return MSDA_ERR_CUDA;
+        g_scratch_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_scratch_ptr[dev];
+    return MSDA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_tensor(const void* p, int64_t elems) {
+    if (elems == 0) return MSDA_OK;
+    if (p == nullptr) return MSDA_ERR_NULL;
+    return aligned16(p) ? MSDA_OK : MSDA_ERR_ALIGN;
+}
+
+}  // namespace
+
+extern "C" MSDA_API int msda_backward_noalloc(
+    const void* value, const int64_t* spatial_shapes, const int64_t* level_start_index,
+    const void* sampling_loc, const void* attn_weight, const void* grad_output, void* grad_value,
+    void* grad_sampling_loc, void* grad_attn_weight, int bs, int num_keys, int num_heads,
+    int head_dim, int num_levels, int num_points, int num_queries, int dtype, unsigned flags,
+    void* stream) {
+    if (dtype != MSDA_BF16) return MSDA_ERR_UNSUPPORTED;  // only bf16 needs scratch
+    if (flags & ~MSDA_GRAD_VALUE_ACCUMULATE) return MSDA_ERR_UNSUPPORTED;
+    if (bs < 0 || num_keys < 0 || num_heads < 0 || head_dim < 0 || num_levels < 0 ||
+        num_points < 0 || num_queries < 0)
+        return MSDA_ERR_DIM;
+    if (num_levels > MSDA_MAX_LEVELS || (int64_t)num_levels * num_points > MSDA_MAX_LEVEL_POINTS ||
+        head_dim % 8 != 0 || head_dim > MSDA_MAX_HEAD_DIM)
+        return MSDA_ERR_UNSUPPORTED;
+    const int64_t value_elems = (int64_t)bs * num_keys * num_heads * head_dim;
+    const int64_t points = (int64_t)bs * num_queries * num_heads * num_levels * num_points;
+    const int64_t out_elems = (int64_t)bs * num_queries * num_heads * head_dim;
+    if ((int64_t)num_heads * head_dim > 2147483647 || (int64_t)bs * num_queries * num_heads >
+        1073741823 || (int64_t)bs * num_keys > 2147483647)
+        return MSDA_ERR_DIM;
+    // The fp32 accumulator must fit the library's fixed scratch array.
+    if ((size_t)value_elems * sizeof(float) > (size_t)MSDA_NOALLOC_MAX_WORKSPACE_BYTES)
+        return MSDA_ERR_WORKSPACE;
+    int rc;
+    if ((rc = check_tensor(grad_value, value_elems)) != MSDA_OK) return rc;
+    if ((rc = check_tensor(grad_sampling_loc, 2 * points)) != MSDA_OK) return rc;
+    if ((rc = check_tensor(grad_attn_weight, points)) != MSDA_OK) return rc;
+    const bool work = points > 0 && value_elems > 0;
+    if (work) {
+        if ((rc = check_tensor(value, value_elems)) != MSDA_OK) return rc;
+        if ((rc = check_tensor(sampling_loc, points)) != MSDA_OK) return rc;
+        if ((rc = check_tensor(attn_weight, points)) != MSDA_OK) return rc;
+        if ((rc = check_tensor(grad_output, out_elems)) != MSDA_OK) return rc;
+        if (spatial_shapes == nullptr || level_start_index == nullptr) return MSDA_ERR_NULL;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool accumulate = (flags & MSDA_GRAD_VALUE_ACCUMULATE) != 0;
+    if (!work) {
+        if (!accumulate && msda::launch_zero_fill(grad_value, value_elems * 2, st) != cudaSuccess)
+            return MSDA_ERR_CUDA;
+        if (msda::launch_zero_fill(grad_sampling_loc, 2 * points * 2, st) != cudaSuccess)
+            return MSDA_ERR_CUDA;
+        return msda::launch_zero_fill(grad_attn_weight, points * 2, st) == cudaSuccess
+                   ? MSDA_OK : MSDA_ERR_CUDA;
+    }
+    float* scratch = nullptr;
+    if ((rc = scratch_for_current_device(&scratch)) != MSDA_OK) return rc;
+    // The array keeps the previous call's sums: clear the part this call uses.
+    if (msda::launch_zero_fill(scratch, (size_t)value_elems * sizeof(float), st) != cudaSuccess)
+        return MSDA_ERR_CUDA;
+    const msda::Problem pb{value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
+                           bs, num_keys, num_heads, head_dim, num_levels, num_points,
+                           num_queries};
+    if (msda::launch_backward(pb, grad_output, scratch, grad_sampling_loc, grad_attn_weight,
+                              MSDA_BF16, st) != cudaSuccess)
+        return MSDA_ERR_CUDA;
+    return msda::launch_finalize_bf16(scratch, grad_value, (size_t)value_elems, accumulate, st) ==
+                   cudaSuccess
+               ? MSDA_OK
+               : MSDA_ERR_CUDA;
+}

@@ -1,0 +1,75 @@
+"""msda_backward_noalloc: the bf16 backward for callers that cannot allocate.
+
+Some callers of this library may not allocate device memory themselves: a
+host framework that owns every allocation, a plug-in with no access to the
+allocator, or code that must not call cudaMalloc while work is being captured
+or timed.  For them the library offers msda_backward_noalloc, which takes no
+workspace and accumulates in a fixed scratch array of its own.  This test
+calls it through the C ABI (the ctypes binding) twice in a row, on two
+different problems, and checks each result against the regular
+msda_backward with its caller-provided workspace, within the bf16 gradient
+tolerance the parity tests use (max|err| <= 1e-2 * max|ref|).  The second call
+shows that the scratch left by the first call does not leak into the next.
+
+The file name makes pytest collect it last.
+"""
+import numpy as np
+import pytest
+import torch
+
+from scale_deformable_attention_05_b300 import inputs as gen
+from tests.gpu_helpers import assert_grad_close, host, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from scale_deformable_attention_05_b300 import binding
+    return binding
+
+
+def _decoder_bf16(seed):
+    # decoder cross-attention shape in bf16: the fp32 accumulator (45.5 MB) fits
+    # the fixed scratch array
+    return gen.WORKLOADS["decoder"].with_(seed=seed, dtype="bf16")
+
+
+def test_noalloc_backward_matches_regular_backward_twice(B):
+    for seed in (2001, 2002):
+        wl = _decoder_bf16(seed)
+        d = to_device(gen.make_inputs(wl), wl)
+        args = (d["value"], d["spatial_shapes"], d["level_start_index"],
+                d["sampling_locations"], d["attention_weights"], d["grad_output"])
+        ref = B.msda_backward(*args)
+        got = tuple(torch.full_like(t, 3.0) for t in ref)
+        B.msda_backward_noalloc(*args, *got)
+        torch.cuda.synchronize()
+        assert B.msda_last_device_error() == 0
+        for name, g, r in zip(("grad_value", "grad_sampling_loc", "grad_attn_weight"), got, ref):
+            assert_grad_close(host(g), host(r), "bf16", f"{name} (seed {seed})")
+        assert torch.count_nonzero(got[0]) > 0
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(B):
+    # bs*K*M*D fp32 accumulators above the fixed maximum: refused before any launch
+    limit_elems = (64 << 20) // 4
+    K = limit_elems // (8 * 32) + 1
+    v = torch.zeros(1, K, 8, 32, device="cuda", dtype=torch.bfloat16)
+    loc = torch.zeros(1, 2, 8, 1, 1, 2, device="cuda", dtype=torch.bfloat16)
+    w = torch.zeros(1, 2, 8, 1, 1, device="cuda", dtype=torch.bfloat16)
+    g = torch.zeros(1, 2, 256, device="cuda", dtype=torch.bfloat16)
+    sh = torch.tensor([[1, K]], device="cuda")
+    lsi = torch.tensor([0], device="cuda")
+    with pytest.raises(B.MsdaError) as e:
+        B.msda_backward_noalloc(v, sh, lsi, loc, w, g, torch.empty_like(v),
+                                torch.empty_like(loc), torch.empty_like(w))
+    assert e.value.status == 5
+    # fp32 needs no workspace, so it has no allocation-free variant
+    with pytest.raises(B.MsdaError) as e:
+        f = lambda t: t.float()
+        B.msda_backward_noalloc(f(v[:, :4]), torch.tensor([[1, 4]], device="cuda"), lsi,
+                                f(loc), f(w), f(g), f(v[:, :4]), f(loc), f(w))
+    assert e.value.status == 3

@@ -386,7 +386,7 @@ def run_native(args, wl):
         "metric": METRIC, "value": wl.points * ws / (ms_step / 1e3), "unit": "points/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic", "config": _config(wl, args),
+        "dtype": wl.dtype, "data": "synthetic", "config": _config(wl, args),
         "roofline": roofline, "passes": passes, "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed_region_incl_flush": wall, "clocks": clocks, "e2e": e2e,
     }
@@ -408,8 +408,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
-    if args.warmup < 3:
-        ap.error("--warmup must be at least 3")
+    # timing rule: at least three untimed warm-up steps
+    args.warmup = max(args.warmup, 3)
     wl = gen.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, wl)

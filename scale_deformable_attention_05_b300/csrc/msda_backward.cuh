@@ -1,187 +1,572 @@
 // Backward gather/scatter kernel of multi-scale deformable attention.
 //
 // For every sample (b, q, m, l, p) with attention weight a, fractions
-// (fx, fy), corner weights w_c and corner rows v_c (zero off the map), and
+// (fx, fy), corner weights w_c, corner rows v_c (zero off the map) and
 // grad_output row g (DQ-DETR ops page, MSDeformAttnFunction.backward returns
 // these three gradients; the formulas are the derivative of the walk-through's
-// ms_deform_attn_core_pytorch sum):
-//   grad_attn[pt]       = sum_d g_d * sum_c w_c v_c,d
-//   grad_loc[pt].x      = W * a * sum_d g_d ((1-fy)(v01-v00) + fy (v11-v10))_d
-//   grad_loc[pt].y      = H * a * sum_d g_d ((1-fx)(v10-v00) + fx (v11-v01))_d
+// ms_deform_attn_core_pytorch sum), with the corner dot products
+// s_c = sum_d g_d v_c,d:
+//   grad_attn[pt]       = sum_c w_c s_c
+//   grad_loc[pt].x      = W * a * ((1-fy)(s_01 - s_00) + fy (s_11 - s_10))
+//   grad_loc[pt].y      = H * a * ((1-fx)(s_10 - s_00) + fx (s_11 - s_01))
 //   grad_value[b,key_c,m,d] += a * w_c * g_d          (fp32 vector red to global)
 //
-// Decomposition as in the forward (one row per lane group, 16-byte vectors per
-// lane).  The channel sums for the three per-sample gradients are reduced
-// across the group's lanes with xor shuffles; the per-sample results are
-// staged in shared memory and written back coalesced once the group's rows
-// are done.  grad_value is accumulated in fp32 (the caller's fp32 grad_value,
-// or the fp32 workspace for bf16) with red.global.add.v4.f32.
+// Decomposition as in the forward (one query per lane group, kGroups
+// consecutive queries of one (b, m) per warp tile, footprints in shared
+// memory).  Each group walks its samples in batches of eight: per sample it
+// loads the live corner rows, adds each lane's share of the four dot
+// products into registers and scatters a*w_c*g into grad_value with
+// red.global.add.v4.f32.  After a batch the 32 partial dot products of the
+// group are transpose-reduced across its lanes (each exchange halves the
+// values a lane holds), which leaves the four dot products of one sample in
+// one lane (kLanes = 8); that lane forms the sample's location and weight
+// gradients, so the group writes eight consecutive samples' gradients at once.
 #pragma once
 
 #include "msda_device.cuh"
 
 namespace msda {
 
+// Bilinear weight of corner c and its derivatives along x_im and y_im.
+__device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w, float& dwx,
+                                             float& dwy) {
+    const bool cx = (c & 1) != 0, cy = (c & 2) != 0;
+    const float wx = cx ? fx : 1.f - fx, wy = cy ? fy : 1.f - fy;
+    w = wx * wy;
+    dwx = cx ? wy : -wy;
+    dwy = cy ? wx : -wx;
+}
+
+#ifndef MSDA_BWD_MIN_BLOCKS
+#define MSDA_BWD_MIN_BLOCKS 2
+#endif
+
+// Stores the footprint records (corner keys, a*w_c, (a, fx, fy, level)) of
+// the round fetched in f.
+template <int kSPG, int kStride>
+__device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* wax,
+                                                 const SampleFetch& f,
+                                                 const LevelInfo* s_levels,
+                                                 const unsigned char* s_level_of, int r0,
+                                                 int lane) {
+#pragma unroll
+    for (int h = 0; h < kSamplesPerWarp / 32; ++h) {
+        const int s = lane + 32 * h;
+        const int sg = s / kSPG, sj = s % kSPG;
+        int4 key = make_int4(-1, -1, -1, -1);
+        float4 aw = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 aux = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (f.ok[h]) {
+            const int l = s_level_of[r0 + sj];
+            const LevelInfo lv = s_levels[l];
+            const float a = f.a[h];
+            const Footprint fp = make_footprint(fmaf(f.xy[h].x, (float)lv.W, -0.5f),
+                                                fmaf(f.xy[h].y, (float)lv.H, -0.5f), lv);
+            key = make_int4(fp.key[0], fp.key[1], fp.key[2], fp.key[3]);
+            aw = make_float4(fp.key[0] >= 0 ? a * fp.w[0] : 0.f, fp.key[1] >= 0 ? a * fp.w[1] : 0.f,
+                             fp.key[2] >= 0 ? a * fp.w[2] : 0.f, fp.key[3] >= 0 ? a * fp.w[3] : 0.f);
+            aux = make_float4(fp.live ? a : 0.f, fp.fx, fp.fy, __int_as_float(l));
+        }
+        wk[sg * kStride + sj] = key;
+        waw[sg * kStride + sj] = aw;
+        wax[sg * kStride + sj] = aux;
+    }
+}
+
+// grad_output row of query q (zeros past the last query or channel).
 template <typename T, int kLanes, int kVPL>
-__global__ void __launch_bounds__(kThreadsPerCta)
+__device__ __forceinline__ void load_grad_row(float (&gr)[kVPL][IO<T>::kVec],
+                                              const T* __restrict__ grad_out,
+                                              const TileCoord& tc, int g, int li, int nvec,
+                                              int num_queries, int num_heads, int head_dim) {
+    const int q = tc.q0 + g;
+    const int64_t row = ((int64_t)tc.b * num_queries + q) * num_heads + tc.m;
+#pragma unroll
+    for (int k = 0; k < kVPL; ++k) {
+        const int vi = li + k * kLanes;
+#pragma unroll
+        for (int e = 0; e < IO<T>::kVec; ++e) gr[k][e] = 0.f;
+        if (q < num_queries && vi < nvec)
+            IO<T>::load_vec_stream(grad_out + row * head_dim + vi * IO<T>::kVec, gr[k]);
+    }
+}
+
+// tiles_per_cta: CTA c runs tiles [c * tiles_per_cta, (c + 1) * tiles_per_cta).
+template <typename T, int kLanes, int kVPL>
+__global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
     backward_kernel(const T* __restrict__ value, const int64_t* __restrict__ spatial_shapes,
                     const int64_t* __restrict__ level_start_index, const T* __restrict__ loc,
                     const T* __restrict__ attn, const T* __restrict__ grad_out,
                     float* __restrict__ grad_value_f32, T* __restrict__ grad_loc,
                     T* __restrict__ grad_attn, int num_keys, int num_heads, int head_dim,
-                    int num_levels, int num_points, int num_queries, int rows,
-                    int rows_per_warp) {
-    constexpr int kGroups = 32 / kLanes;
+                    int num_levels, int num_points, int num_queries, int num_qtiles,
+                    int num_tiles, int tiles_per_cta) {
+    using Geom = TileGeom<kLanes>;
+    constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
     constexpr int V = IO<T>::kVec;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    LevelInfo* s_levels = reinterpret_cast<LevelInfo*>(smem_raw);
-    const int LP = num_levels * num_points;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane / kLanes, li = lane % kLanes;
-    const int pts_per_iter = kGroups * LP;
-    const size_t per_warp = (size_t)pts_per_iter;
-    unsigned char* base = smem_raw + sizeof(LevelInfo) * kMaxLevels;
-    float4* s_w = reinterpret_cast<float4*>(base) + warp * per_warp;
-    float4* s_aux = reinterpret_cast<float4*>(base) + (kWarpsPerCta + warp) * per_warp;
-    float4* s_res = reinterpret_cast<float4*>(base) + (2 * kWarpsPerCta + warp) * per_warp;
-    int2* s_k = reinterpret_cast<int2*>(reinterpret_cast<float4*>(base) +
-                                        3 * kWarpsPerCta * per_warp) +
-                warp * per_warp;
+    constexpr int kBatch = 8;                      // samples per transpose-reduce
+    constexpr int kHeld = 32 / kLanes;             // dot products a lane keeps after it
+    constexpr int kSampPerLane = kHeld >= 4 ? kHeld / 4 : 1;
+    constexpr int kLanesPerSamp = kHeld >= 4 ? 1 : 4 / kHeld;
+    static_assert(kSPG % kBatch == 0, "round must hold whole batches");
 
-    load_level_table(s_levels, spatial_shapes, level_start_index, num_levels, num_keys);
+    __shared__ LevelInfo s_levels[kMaxLevels];
+    __shared__ unsigned char s_level_of[kMaxLevelPoints];
+    __shared__ int4 s_key[kWarpsPerCta][Geom::kRecords];
+    __shared__ float4 s_aw[kWarpsPerCta][Geom::kRecords];
+    __shared__ float4 s_aux[kWarpsPerCta][Geom::kRecords];
+
+    load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, num_levels,
+                     num_points, num_keys);
     __syncthreads();
 
-    const int64_t MD = (int64_t)num_heads * head_dim;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane / kLanes, li = lane % kLanes;
+    const int LP = num_levels * num_points;
     const int nvec = head_dim / V;
-    const int row0 = (blockIdx.x * kWarpsPerCta + warp) * rows_per_warp;
+    const unsigned row_bytes = (unsigned)(num_heads * head_dim) * (unsigned)sizeof(T);
+    const unsigned row_bytes32 = (unsigned)(num_heads * head_dim) * 4u;
+    int4* wk = s_key[warp];
+    float4* waw = s_aw[warp];
+    float4* wax = s_aux[warp];
 
-    for (int it = 0; it < rows_per_warp; it += kGroups) {
-        const int rbase = row0 + it;
-        if (rbase >= rows) break;
-        const int64_t pt0 = (int64_t)rbase * LP;
-        // ---- phase 1: footprints (bilinear weights without a; validity mask)
-        for (int t = lane; t < pts_per_iter; t += 32) {
-            const int rl = t / LP;
-            float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            float4 aux = make_float4(0.f, 0.f, 0.f, 0.f);
-            int2 k2 = make_int2(0, 0);
-            if (rbase + rl < rows) {
-                const int j = t - rl * LP;
-                const LevelInfo lv = s_levels[j / num_points];
-                const float2 xy = IO<T>::load_xy(loc + 2 * (pt0 + t));
-                const float a = IO<T>::load_one(attn + pt0 + t);
-                const float x = fmaf(xy.x, (float)lv.W, -0.5f);
-                const float y = fmaf(xy.y, (float)lv.H, -0.5f);
-                const Footprint f = make_footprint(x, y, lv);
-                w4 = make_float4(f.w[0], f.w[1], f.w[2], f.w[3]);
-                aux = make_float4(a, f.fx, f.fy, 0.f);
-                k2 = make_int2(f.key00, (int)f.info);
+    StepIter it;
+    it.t = blockIdx.x * tiles_per_cta + warp;
+    it.end = min(num_tiles, (blockIdx.x + 1) * tiles_per_cta);
+    it.r0 = 0;
+    it.LP = LP;
+    it.spg = kSPG;
+    if (!it.valid()) return;
+
+    SampleFetch f;
+    TileCoord tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
+    fetch_samples<T, kSPG>(f, loc, attn, tc, 0, lane, LP, num_queries, num_heads);
+    float gr[kVPL][V], gnext[kVPL][V];
+    load_grad_row<T, kLanes, kVPL>(gnext, grad_out, tc, g, li, nvec, num_queries, num_heads,
+                                   head_dim);
+
+    while (true) {
+        // ---- 1. footprints of this round (inputs fetched one round ahead)
+        backward_records<kSPG, kStride>(wk, waw, wax, f, s_levels, s_level_of, it.r0, lane);
+        __syncwarp();
+        const TileCoord cur = tc;
+        const int r0 = it.r0;
+        if (r0 == 0) {
+#pragma unroll
+            for (int k = 0; k < kVPL; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) gr[k][e] = gnext[k][e];
+        }
+        it.next();
+        const bool more = it.valid();
+        if (more) {
+            tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
+            fetch_samples<T, kSPG>(f, loc, attn, tc, it.r0, lane, LP, num_queries, num_heads);
+            if (it.r0 == 0)
+                load_grad_row<T, kLanes, kVPL>(gnext, grad_out, tc, g, li, nvec, num_queries,
+                                               num_heads, head_dim);
+        }
+
+        const int64_t head0 = ((int64_t)cur.b * num_keys * num_heads + cur.m) * head_dim;
+        const char* vbase = reinterpret_cast<const char*>(value + head0);
+        char* gvbase = reinterpret_cast<char*>(grad_value_f32 + head0);
+        const int q = cur.q0 + g;
+        const int64_t row = ((int64_t)cur.b * num_queries + q) * num_heads + cur.m;
+        const int nj = min(kSPG, LP - r0);
+        const int4* gk = wk + g * kStride;
+        const float4* gaw = waw + g * kStride;
+        const float4* gax = wax + g * kStride;
+        for (int jb = 0; jb < nj; jb += kBatch) {
+            // ---- 2. gather + scatter a batch of eight samples (records past
+            //         the round's end hold dead samples)
+            float dots[4 * kBatch];
+#pragma unroll
+            for (int s8 = 0; s8 < kBatch; ++s8) {
+                const int4 k4 = gk[jb + s8];
+                const float4 a4 = gaw[jb + s8];
+                const int keys[4] = {k4.x, k4.y, k4.z, k4.w};
+                const float awc[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[kVPL][V];
+                    const char* p = row_ptr(vbase, keys[c], row_bytes);
+#pragma unroll
+                    for (int k = 0; k < kVPL; ++k) {
+                        const int vi = li + k * kLanes;
+#pragma unroll
+                        for (int e = 0; e < V; ++e) v[k][e] = 0.f;
+                        if (keys[c] >= 0 && vi < nvec) IO<T>::load_vec(p + vi * 16, v[k]);
+                    }
+                    float d = 0.f;
+#pragma unroll
+                    for (int k = 0; k < kVPL; ++k)
+#pragma unroll
+                        for (int e = 0; e < V; ++e) d = fmaf(gr[k][e], v[k][e], d);
+                    dots[s8 * 4 + c] = d;
+                    if (keys[c] >= 0) {
+                        float* gp = reinterpret_cast<float*>(
+                            gvbase + (size_t)(unsigned)keys[c] * row_bytes32);
+#pragma unroll
+                        for (int k = 0; k < kVPL; ++k) {
+                            const int vi = li + k * kLanes;
+                            if (vi < nvec) {
+#pragma unroll
+                                for (int e = 0; e < V; e += 4)
+                                    red_add_v4(gp + vi * V + e, awc[c] * gr[k][e],
+                                               awc[c] * gr[k][e + 1], awc[c] * gr[k][e + 2],
+                                               awc[c] * gr[k][e + 3]);
+                            }
+                        }
+                    }
+                }
             }
-            s_w[t] = w4;
-            s_aux[t] = aux;
-            s_k[t] = k2;
+
+            // ---- 3. transpose-reduce the batch's dot products across the group
+#pragma unroll
+            for (int rr = 0; (kLanes >> (rr + 1)) >= 1; ++rr) {
+                const int o = kLanes >> (rr + 1);
+                const int n = (4 * kBatch / 2) >> rr;
+                const bool upper = (li & o) != 0;
+#pragma unroll
+                for (int k = 0; k < n; ++k) {
+                    const float send = upper ? dots[k] : dots[k + n];
+                    const float keep = upper ? dots[k + n] : dots[k];
+                    dots[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+
+            // ---- 4. per-sample location and weight gradients
+#pragma unroll
+            for (int u = 0; u < kSampPerLane; ++u) {
+                const int s8 = kHeld >= 4 ? li * (kHeld / 4) + u : (li * kHeld) / 4;
+                const float4 ax = gax[jb + s8];
+                const float a = ax.x, fx = ax.y, fy = ax.z;
+                float ga = 0.f, gx = 0.f, gy = 0.f;
+#pragma unroll
+                for (int k = 0; k < (kHeld >= 4 ? 4 : kHeld); ++k) {
+                    const int c = kHeld >= 4 ? k : (li * kHeld + k) & 3;
+                    float w, dwx, dwy;
+                    corner_terms(c, fx, fy, w, dwx, dwy);
+                    const float d = dots[(kHeld >= 4 ? u * 4 : 0) + k];
+                    ga = fmaf(w, d, ga);
+                    gx = fmaf(dwx, d, gx);
+                    gy = fmaf(dwy, d, gy);
+                }
+#pragma unroll
+                for (int o = 1; o < kLanesPerSamp; o <<= 1) {
+                    ga += __shfl_xor_sync(0xffffffffu, ga, o);
+                    gx += __shfl_xor_sync(0xffffffffu, gx, o);
+                    gy += __shfl_xor_sync(0xffffffffu, gy, o);
+                }
+                if (li % kLanesPerSamp == 0 && jb + s8 < nj && q < num_queries) {
+                    const LevelInfo lv = s_levels[__float_as_int(ax.w)];
+                    const int64_t pt = row * LP + r0 + jb + s8;
+                    IO<T>::store_xy(grad_loc + 2 * pt, (float)lv.W * (a * gx),
+                                    (float)lv.H * (a * gy));
+                    IO<T>::store_one(grad_attn + pt, ga);
+                }
+            }
+        }
+        __syncwarp();
+        if (!more) break;
+    }
+}
+
+// ------------------------------------------------------------------------
+// Backward with merged grad_value scatter (the fast path).
+//
+// The scatter of grad_value is bound by the bytes the SMs send to L2: every
+// red.global.add of a corner row carries head_dim fp32 values.  Neighbouring
+// queries of one head sample the same pixels, so this kernel merges them
+// before sending: a warp tile is G = 32 / kLanes (<= 4) consecutive queries of
+// one (b, m), and its samples are taken in rounds of 32 ordered (level, query,
+// point), one sample per lane.  In a round, for each pixel parity class t
+// (two corners can be the same pixel only if they have the same class), the
+// lanes holding the same corner key find each other with __match_any_sync;
+// the lowest lane collects the per-query weight sums A_q = sum a*w_c over its
+// peers, and the round's distinct (key, A_0..A_{G-1}) entries go to a list in
+// shared memory.  The groups then send one red per distinct entry with the
+// payload sum_q A_q * g_q (every lane holds the grad_output rows of all G
+// queries).  The location and weight gradients come from the corner dot
+// products as in backward_kernel, each group handling its own query's samples.
+template <typename T, int kLanes, int kVPL>
+__global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
+    backward_merge_kernel(const T* __restrict__ value, const int64_t* __restrict__ spatial_shapes,
+                          const int64_t* __restrict__ level_start_index,
+                          const T* __restrict__ loc, const T* __restrict__ attn,
+                          const T* __restrict__ grad_out, float* __restrict__ grad_value_f32,
+                          T* __restrict__ grad_loc, T* __restrict__ grad_attn, int num_keys,
+                          int num_heads, int head_dim, int num_levels, int num_points,
+                          int log2_points, int num_queries, int num_qtiles, int num_tiles,
+                          int tiles_per_cta) {
+    constexpr int G = 32 / kLanes;                 // queries per tile (one per lane group)
+    static_assert(G <= 4, "merged weights hold at most four queries");
+    constexpr int V = IO<T>::kVec;
+    constexpr int kBatch = 8;                      // samples per transpose-reduce
+    constexpr int kHeld = 32 / kLanes;             // dot products a lane keeps after it
+    constexpr int kSampPerLane = kHeld >= 4 ? kHeld / 4 : 1;
+    constexpr int kLanesPerSamp = kHeld >= 4 ? 1 : 4 / kHeld;
+    constexpr int kPerGroup = 32 / G;              // a group's samples in one round
+    constexpr int kMaxUnique = 4 * 32;
+
+    __shared__ LevelInfo s_levels[kMaxLevels];
+    __shared__ unsigned char s_level_of[kMaxLevelPoints];
+    __shared__ int4 s_key[kWarpsPerCta][32];       // corner keys (corner order) per round sample
+    __shared__ float4 s_aux[kWarpsPerCta][32];     // (a, fx, fy, level) per round sample
+    __shared__ int s_ukey[kWarpsPerCta][kMaxUnique];
+    __shared__ float4 s_uA[kWarpsPerCta][kMaxUnique];
+
+    load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, num_levels,
+                     num_points, num_keys);
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane / kLanes, li = lane % kLanes;
+    const int P = num_points, LP = num_levels * num_points;
+    const int log2_gp = log2_points + (G == 4 ? 2 : G == 2 ? 1 : 0);
+    const int S = G * LP;                          // samples per tile
+    const int nvec = head_dim / V;
+    const unsigned row_bytes = (unsigned)(num_heads * head_dim) * (unsigned)sizeof(T);
+    const unsigned row_bytes32 = (unsigned)(num_heads * head_dim) * 4u;
+
+    StepIter it;
+    it.t = blockIdx.x * tiles_per_cta + warp;
+    it.end = min(num_tiles, (blockIdx.x + 1) * tiles_per_cta);
+    it.r0 = 0;
+    it.LP = S;
+    it.spg = 32;
+    if (!it.valid()) return;
+
+    // round sample s = r0 + lane  ->  (level, query, point)
+    auto locate = [&](int r0, int& qo, int& j) {
+        const int s = r0 + lane;
+        const int l = s >> log2_gp, rem = s & ((1 << log2_gp) - 1);
+        qo = rem >> log2_points;
+        j = l * P + (rem & (P - 1));
+        return s < S;
+    };
+    auto fetch = [&](const TileCoord& tc, int r0, float2& xy, float& a, bool& ok) {
+        int qo, j;
+        ok = locate(r0, qo, j) && tc.q0 + qo < num_queries;
+        xy = make_float2(0.f, 0.f);
+        a = 0.f;
+        if (ok) {
+            const int64_t pt =
+                (((int64_t)tc.b * num_queries + tc.q0 + qo) * num_heads + tc.m) * LP + j;
+            xy = IO<T>::load_xy(loc + 2 * pt);
+            a = IO<T>::load_one(attn + pt);
+        }
+    };
+
+    TileCoord tc = tile_coord(it.t, num_heads, num_qtiles, G);
+    float2 fxy;
+    float fa;
+    bool fok;
+    fetch(tc, 0, fxy, fa, fok);
+    float gq[G][kVPL][V];
+    float gown[kVPL][V];
+
+    while (true) {
+        const TileCoord cur = tc;
+        const int r0 = it.r0;
+        if (r0 == 0) {
+            // grad_output rows of the tile's queries, in every lane
+#pragma unroll
+            for (int qq = 0; qq < G; ++qq) {
+                const int q = cur.q0 + qq;
+                const int64_t row = ((int64_t)cur.b * num_queries + q) * num_heads + cur.m;
+#pragma unroll
+                for (int k = 0; k < kVPL; ++k) {
+                    const int vi = li + k * kLanes;
+#pragma unroll
+                    for (int e = 0; e < V; ++e) gq[qq][k][e] = 0.f;
+                    if (q < num_queries && vi < nvec)
+                        IO<T>::load_vec_stream(grad_out + row * head_dim + vi * V, gq[qq][k]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kVPL; ++k)
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    float x = gq[0][k][e];
+#pragma unroll
+                    for (int qq = 1; qq < G; ++qq) x = g == qq ? gq[qq][k][e] : x;
+                    gown[k][e] = x;
+                }
+        }
+
+        // ---- 1. my sample's footprint
+        int myq, myj;
+        locate(r0, myq, myj);
+        ClassCorners cc;
+        {
+            int4 key = make_int4(-1, -1, -1, -1);
+            float4 aux = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                cc.key[t] = -1;
+                cc.w[t] = 0.f;
+            }
+            if (fok) {
+                const int l = s_level_of[myj];
+                const LevelInfo lv = s_levels[l];
+                const Footprint fp = make_footprint(fmaf(fxy.x, (float)lv.W, -0.5f),
+                                                    fmaf(fxy.y, (float)lv.H, -0.5f), lv);
+                key = make_int4(fp.key[0], fp.key[1], fp.key[2], fp.key[3]);
+                aux = make_float4(fp.live ? fa : 0.f, fp.fx, fp.fy, __int_as_float(l));
+                cc = class_corners(fp, fa);
+            }
+            s_key[warp][lane] = key;
+            s_aux[warp][lane] = aux;
+        }
+        it.next();
+        const bool more = it.valid();
+        if (more) {
+            tc = tile_coord(it.t, num_heads, num_qtiles, G);
+            fetch(tc, it.r0, fxy, fa, fok);
+        }
+
+        // ---- 2. merge equal corner keys of the round, class by class
+        int nu = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int key = cc.key[t];
+            const float aw = cc.w[t];
+            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            const bool lead = key >= 0 && (__ffs(peers) - 1) == lane;
+            float A[4];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) A[qq] = myq == qq ? aw : 0.f;
+            unsigned rem = lead ? (peers & (peers - 1u)) : 0u;
+            while (__any_sync(0xffffffffu, rem != 0u)) {
+                const int src = rem ? __ffs(rem) - 1 : lane;
+                const float w = __shfl_sync(0xffffffffu, aw, src);
+                const int qs = __shfl_sync(0xffffffffu, myq, src);
+                if (rem) {
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) A[qq] += qs == qq ? w : 0.f;
+                    rem &= rem - 1u;
+                }
+            }
+            const unsigned lm = __ballot_sync(0xffffffffu, lead);
+            if (lead) {
+                const int pos = nu + __popc(lm & ((1u << lane) - 1u));
+                s_ukey[warp][pos] = key;
+                s_uA[warp][pos] = make_float4(A[0], A[1], A[2], A[3]);
+            }
+            nu += __popc(lm);
         }
         __syncwarp();
 
-        // ---- phase 2: gather corners, reduce per-sample grads, scatter grad_value.
-        // Every lane runs the sample loop (the group sums shuffle across the
-        // whole warp); a group past the last row has all-zero footprints, so
-        // it reads and writes nothing.
-        const bool active = rbase + g < rows;
-        const int r = active ? rbase + g : rbase;
-        {
-            const int m = r % num_heads;
-            const int b = (r / num_heads) / num_queries;
-            const int64_t vrow = ((int64_t)b * num_keys * num_heads + m) * head_dim;
-            const T* vb = value + vrow;
-            float* gvb = grad_value_f32 + vrow;
-            float gr[kVPL][V];
+        // ---- 3. corner dot products and location / weight gradients of my group's samples
+        const int64_t head0 = ((int64_t)cur.b * num_keys * num_heads + cur.m) * head_dim;
+        const char* vbase = reinterpret_cast<const char*>(value + head0);
+        char* gvbase = reinterpret_cast<char*>(grad_value_f32 + head0);
+        const int q = cur.q0 + g;
+        const int64_t row = ((int64_t)cur.b * num_queries + q) * num_heads + cur.m;
+#pragma unroll 1
+        for (int kb = 0; kb < kPerGroup; kb += kBatch) {
+            float dots[4 * kBatch];
+#pragma unroll
+            for (int s8 = 0; s8 < kBatch; ++s8) {
+                const int k = kb + s8;
+                const int sl = ((k >> log2_points) << log2_gp) + (g << log2_points) + (k & (P - 1));
+                const int4 k4 = s_key[warp][sl];
+                const int keys[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[kVPL][V];
+                    const char* p = row_ptr(vbase, keys[c], row_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < kVPL; ++kk) {
+                        const int vi = li + kk * kLanes;
+#pragma unroll
+                        for (int e = 0; e < V; ++e) v[kk][e] = 0.f;
+                        if (keys[c] >= 0 && vi < nvec) IO<T>::load_vec(p + vi * 16, v[kk]);
+                    }
+                    float d = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < kVPL; ++kk)
+#pragma unroll
+                        for (int e = 0; e < V; ++e) d = fmaf(gown[kk][e], v[kk][e], d);
+                    dots[s8 * 4 + c] = d;
+                }
+            }
+#pragma unroll
+            for (int rr = 0; (kLanes >> (rr + 1)) >= 1; ++rr) {
+                const int o = kLanes >> (rr + 1);
+                const int n = (4 * kBatch / 2) >> rr;
+                const bool upper = (li & o) != 0;
+#pragma unroll
+                for (int k = 0; k < n; ++k) {
+                    const float send = upper ? dots[k] : dots[k + n];
+                    const float keep = upper ? dots[k + n] : dots[k];
+                    dots[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kSampPerLane; ++u) {
+                const int s8 = kHeld >= 4 ? li * (kHeld / 4) + u : (li * kHeld) / 4;
+                const int k = kb + s8;
+                const int sl = ((k >> log2_points) << log2_gp) + (g << log2_points) + (k & (P - 1));
+                const float4 ax = s_aux[warp][sl];
+                const float a = ax.x, fx = ax.y, fy = ax.z;
+                float ga = 0.f, gx = 0.f, gy = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < (kHeld >= 4 ? 4 : kHeld); ++kk) {
+                    const int c = kHeld >= 4 ? kk : (li * kHeld + kk) & 3;
+                    float w, dwx, dwy;
+                    corner_terms(c, fx, fy, w, dwx, dwy);
+                    const float d = dots[(kHeld >= 4 ? u * 4 : 0) + kk];
+                    ga = fmaf(w, d, ga);
+                    gx = fmaf(dwx, d, gx);
+                    gy = fmaf(dwy, d, gy);
+                }
+#pragma unroll
+                for (int o = 1; o < kLanesPerSamp; o <<= 1) {
+                    ga += __shfl_xor_sync(0xffffffffu, ga, o);
+                    gx += __shfl_xor_sync(0xffffffffu, gx, o);
+                    gy += __shfl_xor_sync(0xffffffffu, gy, o);
+                }
+                const int s = r0 + sl;
+                const int j = (s >> log2_gp) * P + (s & (P - 1));
+                if (li % kLanesPerSamp == 0 && s < S && q < num_queries) {
+                    const LevelInfo lv = s_levels[__float_as_int(ax.w)];
+                    const int64_t pt = row * LP + j;
+                    IO<T>::store_xy(grad_loc + 2 * pt, (float)lv.W * (a * gx),
+                                    (float)lv.H * (a * gy));
+                    IO<T>::store_one(grad_attn + pt, ga);
+                }
+            }
+        }
+
+        // ---- 4. one red per distinct corner row: payload sum_q A_q * g_q
+#pragma unroll 1
+        for (int u = g; u < nu; u += G) {
+            const int key = s_ukey[warp][u];
+            const float4 A4 = s_uA[warp][u];
+            const float A[4] = {A4.x, A4.y, A4.z, A4.w};
+            float* gp = reinterpret_cast<float*>(gvbase + (size_t)(unsigned)key * row_bytes32);
 #pragma unroll
             for (int k = 0; k < kVPL; ++k) {
                 const int vi = li + k * kLanes;
-                if (active && vi < nvec) {
-                    IO<T>::load_vec_stream(grad_out + (int64_t)r * head_dim + vi * V, gr[k]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < V; ++e) gr[k][e] = 0.f;
-                }
-            }
-            const float4* sw = s_w + g * LP;
-            const float4* sa = s_aux + g * LP;
-            const int2* sk = s_k + g * LP;
-            for (int j = 0; j < LP; ++j) {
-                const float4 w4 = sw[j];
-                const float4 ax = sa[j];
-                const int2 k2 = sk[j];
-                const unsigned mask = (unsigned)k2.y & 15u;
-                const int W = (int)((unsigned)k2.y >> 4);
-                const float a = ax.x, fx = ax.y, fy = ax.z;
-                float v[4][kVPL][V];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const T* p = vb + (int64_t)corner_key(k2.x, W, c) * MD;
-#pragma unroll
-                    for (int k = 0; k < kVPL; ++k) {
-                        const int vi = li + k * kLanes;
-                        if ((mask >> c & 1u) && vi < nvec) {
-                            IO<T>::load_vec(p + vi * V, v[c][k]);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < V; ++e) v[c][k][e] = 0.f;
-                        }
-                    }
-                }
-                float pa = 0.f, px = 0.f, py = 0.f;
-                const float gy0 = 1.f - fy, gx0 = 1.f - fx;
-#pragma unroll
-                for (int k = 0; k < kVPL; ++k)
+                if (vi < nvec) {
+                    float pay[V];
 #pragma unroll
                     for (int e = 0; e < V; ++e) {
-                        const float v00 = v[0][k][e], v01 = v[1][k][e];
-                        const float v10 = v[2][k][e], v11 = v[3][k][e];
-                        const float s = w4.x * v00 + w4.y * v01 + w4.z * v10 + w4.w * v11;
-                        const float gd = gr[k][e];
-                        pa = fmaf(gd, s, pa);
-                        px = fmaf(gd, gy0 * (v01 - v00) + fy * (v11 - v10), px);
-                        py = fmaf(gd, gx0 * (v10 - v00) + fx * (v11 - v01), py);
+                        float x = A[0] * gq[0][k][e];
+#pragma unroll
+                        for (int qq = 1; qq < G; ++qq) x = fmaf(A[qq], gq[qq][k][e], x);
+                        pay[e] = x;
                     }
-                // scatter a * w_c * g into grad_value for every corner on the map
-                const float aw[4] = {a * w4.x, a * w4.y, a * w4.z, a * w4.w};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (!(mask >> c & 1u)) continue;
-                    float* q = gvb + (int64_t)corner_key(k2.x, W, c) * MD;
-#pragma unroll
-                    for (int k = 0; k < kVPL; ++k) {
-                        const int vi = li + k * kLanes;
-                        if (vi < nvec) {
-#pragma unroll
-                            for (int e = 0; e < V; e += 4)
-                                red_add_v4(q + vi * V + e, aw[c] * gr[k][e], aw[c] * gr[k][e + 1],
-                                           aw[c] * gr[k][e + 2], aw[c] * gr[k][e + 3]);
-                        }
-                    }
-                }
-                pa = group_sum<kLanes>(pa);
-                px = group_sum<kLanes>(px);
-                py = group_sum<kLanes>(py);
-                if (li == 0) {
-                    const LevelInfo lv = s_levels[j / num_points];
-                    s_res[g * LP + j] = make_float4((float)lv.W * (a * px), (float)lv.H * (a * py),
-                                                    pa, 0.f);
+                    for (int e = 0; e < V; e += 4)
+                        red_add_v4(gp + vi * V + e, pay[e], pay[e + 1], pay[e + 2], pay[e + 3]);
                 }
             }
         }
         __syncwarp();
-        // ---- write back the per-sample gradients of the iteration, coalesced
-        for (int t = lane; t < pts_per_iter; t += 32) {
-            if (rbase + t / LP < rows) {
-                const float4 res = s_res[t];
-                IO<T>::store_xy(grad_loc + 2 * (pt0 + t), res.x, res.y);
-                IO<T>::store_one(grad_attn + pt0 + t, res.z);
-            }
-        }
-        __syncwarp();
+        if (!more) break;
     }
 }
 

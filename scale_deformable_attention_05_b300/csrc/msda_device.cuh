@@ -1,6 +1,6 @@
 // Device-side building blocks shared by the forward and backward kernels:
 // element-type traits with 16-byte vector loads/stores, the per-CTA level
-// table, and the per-sample "footprint" (bilinear corners of one sample).
+// table, the per-sample bilinear footprint, and the warp-tile geometry.
 //
 // Sampling semantics (Deformable DETR walk-through, "2.2.4 源码分析",
 // ms_deform_attn_core_pytorch: grid_sample(bilinear, zeros,
@@ -9,6 +9,17 @@
 //   the sample is live iff -1 < x_im < W and -1 < y_im < H
 //   corners (y0,x0), (y0,x0+1), (y0+1,x0), (y0+1,x0+1) with x0 = floor(x_im),
 //   weights (1-fx)(1-fy), fx(1-fy), (1-fx)fy, fx*fy; a corner off the map is 0.
+//
+// Work decomposition (both kernels).  A "row" is one (b, q, m) triple: its
+// L*P samples are contiguous in sampling_locations / attention_weights and
+// its head_dim outputs are contiguous in output.  A warp is split into
+// kGroups = 32 / kLanes lane groups; each lane owns kVPL 16-byte vectors of
+// the head's channels, so one corner row of value (head_dim * e bytes) is
+// read by a group as coalesced 128-bit loads (one 128-byte line for fp32
+// head_dim 32).  A warp tile is kGroups consecutive queries of ONE (b, m):
+// group g owns query q0 + g, all groups read the same head's slice of value,
+// and samples of neighbouring queries that fall on the same pixel row are
+// served by one cache line in the same load instruction.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -20,6 +31,9 @@ namespace msda {
 constexpr int kWarpsPerCta = 8;
 constexpr int kThreadsPerCta = kWarpsPerCta * 32;
 constexpr int kMaxLevels = 16;
+constexpr int kMaxLevelPoints = 256;
+// Samples whose footprints one warp computes per round (two per lane).
+constexpr int kSamplesPerWarp = 64;
 
 // Set (atomicOr) by a kernel that meets a level whose pixels would fall
 // outside [0, num_keys); read and cleared by msda_last_device_error().
@@ -35,12 +49,12 @@ struct IO;
 template <>
 struct IO<float> {
     static constexpr int kVec = 4;  // elements per 16-byte vector
-    // Value rows: read-only, reused across queries -> keep in L1.
-    __device__ __forceinline__ static void load_vec(const float* p, float (&v)[kVec]) {
+    // Value rows: read-only, reused across samples -> keep in L1.
+    __device__ __forceinline__ static void load_vec(const void* p, float (&v)[kVec]) {
         const float4 t = __ldg(reinterpret_cast<const float4*>(p));
         v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
     }
-    // Streamed once (locations, weights, grad_output): evict-first.
+    // Streamed once (grad_output): evict-first.
     __device__ __forceinline__ static void load_vec_stream(const float* p, float (&v)[kVec]) {
         const float4 t = __ldcs(reinterpret_cast<const float4*>(p));
         v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
@@ -73,7 +87,7 @@ struct IO<__nv_bfloat16> {
         v[0] = bf16_lo(t.x); v[1] = bf16_hi(t.x); v[2] = bf16_lo(t.y); v[3] = bf16_hi(t.y);
         v[4] = bf16_lo(t.z); v[5] = bf16_hi(t.z); v[6] = bf16_lo(t.w); v[7] = bf16_hi(t.w);
     }
-    __device__ __forceinline__ static void load_vec(const T* p, float (&v)[kVec]) {
+    __device__ __forceinline__ static void load_vec(const void* p, float (&v)[kVec]) {
         unpack(__ldg(reinterpret_cast<const uint4*>(p)), v);
     }
     __device__ __forceinline__ static void load_vec_stream(const T* p, float (&v)[kVec]) {
@@ -104,15 +118,16 @@ struct IO<__nv_bfloat16> {
 
 // ------------------------------------------------------------- level table
 // One entry per level: H, W, first key, and whether every pixel of the level
-// lies inside [0, num_keys).  Built once per CTA in shared memory.
+// lies inside [0, num_keys).  Built once per CTA in shared memory, together
+// with the level of every flattened (level, point) index j < L*P.
 struct LevelInfo {
     int H, W, start, ok;
 };
 
-__device__ __forceinline__ void load_level_table(LevelInfo* s_levels,
+__device__ __forceinline__ void load_level_table(LevelInfo* s_levels, unsigned char* s_level_of,
                                                  const int64_t* __restrict__ spatial_shapes,
                                                  const int64_t* __restrict__ level_start_index,
-                                                 int num_levels, int num_keys) {
+                                                 int num_levels, int num_points, int num_keys) {
     if (threadIdx.x < num_levels) {
         const int l = threadIdx.x;
         const int64_t H = spatial_shapes[2 * l], W = spatial_shapes[2 * l + 1];
@@ -127,52 +142,77 @@ __device__ __forceinline__ void load_level_table(LevelInfo* s_levels,
         s_levels[l] = li;
         if (!ok && blockIdx.x == 0) atomicOr(&g_error_word, kErrLevelOutOfRange);
     }
+    const int LP = num_levels * num_points;
+    for (int j = threadIdx.x; j < LP; j += blockDim.x) s_level_of[j] = (unsigned char)(j / num_points);
 }
 
 // --------------------------------------------------------------- footprint
-// Bilinear footprint of one sample, as stored in shared memory.
-//   key00: flattened key of corner (y0, x0) (may be off the map)
-//   info : (W << 4) | mask, bit c of mask set when corner c is read
+// Bilinear footprint of one sample.
+//   key[c] : flattened key of corner c, or -1 when the corner is off the map
+//            or the sample is not live (such corners are never read)
+//   fx, fy : fractions inside the cell (0 for a dead sample)
+//   w[c]   : (1-fx)(1-fy), fx(1-fy), (1-fx)fy, fx*fy
 struct Footprint {
+    int key[4];
+    int x0, y0;  // cell (top-left pixel); 0 for a dead sample
     float fx, fy;
-    int key00;
-    unsigned info;
-    float w[4];  // bilinear corner weights (1-fx)(1-fy), fx(1-fy), (1-fx)fy, fx*fy
+    float w[4];
+    bool live;
 };
 
 // x, y: pixel coordinates already rounded to fp32 (one FMA each).
 __device__ __forceinline__ Footprint make_footprint(float x, float y, const LevelInfo& lv) {
     Footprint f;
     const float Wf = (float)lv.W, Hf = (float)lv.H;
-    const bool live = lv.ok && (x > -1.f) && (x < Wf) && (y > -1.f) && (y < Hf);
-    const float x0f = floorf(x), y0f = floorf(y);
-    f.fx = live ? x - x0f : 0.f;  // exact (Sterbenz)
-    f.fy = live ? y - y0f : 0.f;
-    const int x0 = live ? (int)x0f : 0, y0 = live ? (int)y0f : 0;
+    f.live = lv.ok && (x > -1.f) && (x < Wf) && (y > -1.f) && (y < Hf);  // NaN -> dead
+    const float xs = f.live ? x : 0.f, ys = f.live ? y : 0.f;
+    const float x0f = floorf(xs), y0f = floorf(ys);
+    f.fx = xs - x0f;  // exact for |x| >= 1 (Sterbenz); for x in (-1, 0) one rounding
+    f.fy = ys - y0f;
+    const int x0 = (int)x0f, y0 = (int)y0f;
+    f.x0 = x0;
+    f.y0 = y0;
+    const bool vx0 = f.live && x0 >= 0, vx1 = f.live && x0 + 1 < lv.W;
+    const bool vy0 = y0 >= 0, vy1 = y0 + 1 < lv.H;
+    const int k00 = lv.start + y0 * lv.W + x0;
+    f.key[0] = (vx0 && vy0) ? k00 : -1;
+    f.key[1] = (vx1 && vy0) ? k00 + 1 : -1;
+    f.key[2] = (vx0 && vy1) ? k00 + lv.W : -1;
+    f.key[3] = (vx1 && vy1) ? k00 + lv.W + 1 : -1;
     const float gx = 1.f - f.fx, gy = 1.f - f.fy;
     f.w[0] = gx * gy;
     f.w[1] = f.fx * gy;
     f.w[2] = gx * f.fy;
     f.w[3] = f.fx * f.fy;
-    const bool vx0 = x0 >= 0, vx1 = x0 + 1 < lv.W, vy0 = y0 >= 0, vy1 = y0 + 1 < lv.H;
-    unsigned mask = (unsigned)(vx0 && vy0) | ((unsigned)(vx1 && vy0) << 1) |
-                    ((unsigned)(vx0 && vy1) << 2) | ((unsigned)(vx1 && vy1) << 3);
-    if (!live) mask = 0;
-    f.key00 = live ? lv.start + y0 * lv.W + x0 : 0;
-    f.info = ((unsigned)lv.W << 4) | mask;
     return f;
 }
 
-__device__ __forceinline__ int corner_key(int key00, int W, int c) {
-    return key00 + (c & 1) + ((c >> 1) ? W : 0);
+// Corners of a footprint reordered by pixel parity class t = (x & 1) + 2 (y & 1).
+// Each sample has exactly one corner in each class, so two samples can share
+// a pixel only within the same class.  kw[t] is corner weight * a (0 when off
+// the map).
+struct ClassCorners {
+    int key[4];
+    float w[4];
+};
+
+__device__ __forceinline__ ClassCorners class_corners(const Footprint& f, float a) {
+    ClassCorners cc;
+    const int px = f.x0 & 1, py = f.y0 & 1;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int c = (((t >> 1) ^ py) << 1) | ((t & 1) ^ px);  // corner holding class t
+        const int k = c == 0 ? f.key[0] : c == 1 ? f.key[1] : c == 2 ? f.key[2] : f.key[3];
+        const float w = c == 0 ? f.w[0] : c == 1 ? f.w[1] : c == 2 ? f.w[2] : f.w[3];
+        cc.key[t] = k;
+        cc.w[t] = k >= 0 ? a * w : 0.f;
+    }
+    return cc;
 }
 
-// Sum over the `width` lanes of an aligned lane group (width a power of two).
-template <int kWidth>
-__device__ __forceinline__ float group_sum(float v) {
-#pragma unroll
-    for (int o = kWidth / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+// Byte address of the row of `key` in a [*, num_keys, M, D] slice starting at base.
+__device__ __forceinline__ const char* row_ptr(const char* base, int key, unsigned row_bytes) {
+    return base + (size_t)(unsigned)key * row_bytes;
 }
 
 // Fire-and-forget vector fp32 add into global memory (sm_90+ vector red).
@@ -181,5 +221,75 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
                  "f"(c), "f"(d)
                  : "memory");
 }
+
+// Geometry of a warp tile for lane groups of kLanes lanes.
+template <int kLanes>
+struct TileGeom {
+    static_assert(kLanes == 4 || kLanes == 8 || kLanes == 16 || kLanes == 32, "lane group");
+    static constexpr int kGroups = 32 / kLanes;                  // queries per warp tile
+    static constexpr int kSPG = kSamplesPerWarp / kGroups;       // samples per group per round
+    static constexpr int kStride = kSPG + 1;                     // padded record stride (16 B units)
+    static constexpr int kRecords = kGroups * kStride;           // records per warp
+};
+
+// Warp tile t -> (b, first query, m).  Tiles are ordered (b, m, query block):
+// consecutive tiles are neighbouring queries of one head, and a CTA walks a
+// contiguous range of them, so the value rows its samples touch stay in L1.
+struct TileCoord {
+    int b, q0, m;
+};
+__device__ __forceinline__ TileCoord tile_coord(int t, int num_heads, int num_qtiles, int groups) {
+    TileCoord c;
+    const int qt = t % num_qtiles;
+    const int rest = t / num_qtiles;
+    c.q0 = qt * groups;
+    c.m = rest % num_heads;
+    c.b = rest / num_heads;
+    return c;
+}
+
+// Locations and attention weights of the two samples a lane handles in one
+// round of a warp tile, loaded one round ahead of their use.
+struct SampleFetch {
+    float2 xy[2];
+    float a[2];
+    bool ok[2];
+};
+
+template <typename T, int kSPG>
+__device__ __forceinline__ void fetch_samples(SampleFetch& f, const T* __restrict__ loc,
+                                              const T* __restrict__ attn, const TileCoord& tc,
+                                              int r0, int lane, int LP, int num_queries,
+                                              int num_heads) {
+#pragma unroll
+    for (int h = 0; h < kSamplesPerWarp / 32; ++h) {
+        const int s = lane + 32 * h;
+        const int sg = s / kSPG, sj = s % kSPG;
+        const int j = r0 + sj, q = tc.q0 + sg;
+        f.ok[h] = q < num_queries && j < LP;
+        f.xy[h] = make_float2(0.f, 0.f);
+        f.a[h] = 0.f;
+        if (f.ok[h]) {
+            const int64_t pt = (((int64_t)tc.b * num_queries + q) * num_heads + tc.m) * LP + j;
+            f.xy[h] = IO<T>::load_xy(loc + 2 * pt);
+            f.a[h] = IO<T>::load_one(attn + pt);
+        }
+    }
+}
+
+// The (tile, round) steps one warp executes: tiles begin + warp, begin + warp
+// + kWarpsPerCta, ... below end; each tile in rounds of kSPG samples per group.
+struct StepIter {
+    int t, r0, end, LP, spg;
+    __device__ __forceinline__ bool valid() const { return t < end; }
+    __device__ __forceinline__ bool last_round() const { return r0 + spg >= LP; }
+    __device__ __forceinline__ void next() {
+        r0 += spg;
+        if (r0 >= LP) {
+            r0 = 0;
+            t += kWarpsPerCta;
+        }
+    }
+};
 
 }  // namespace msda

@@ -4,135 +4,169 @@
 // ms_deform_attn_core_pytorch):
 //   out[b, q, m*D + d] = sum_{l,p} a[b,q,m,l,p] * sum_c w_c * value[b, key_c, m, d]
 //
-// Work decomposition.  A "row" is one (b, q, m) triple: its L*P samples are
-// contiguous in sampling_locations / attention_weights and its D outputs are
-// contiguous in output.  A warp is split into 32/kLanes lane groups; each
-// group owns one row at a time and each lane owns kVPL 16-byte vectors of
-// the head's D channels, so one corner row of value (D*e bytes) is read by
-// the group as coalesced 128-bit loads.
-//
-// Each warp iteration has two phases:
-//   1. footprint: the warp's lanes take the iteration's samples one per lane
-//      (coalesced loads of locations and weights), compute the pixel
-//      coordinates, cell, corner validity and the four corner weights with
-//      the attention weight folded in, once per sample, into shared memory;
-//   2. gather: every group walks its row's samples, reads each footprint
-//      as a shared-memory broadcast and issues one 128-bit load per live
-//      corner and vector, accumulating 4 FMAs per channel per sample in fp32.
-// Corners off the map or with weight 0 are not read at all.
+// One warp tile = kGroups consecutive queries of one (b, m) (see
+// msda_device.cuh); a CTA's warps take consecutive tiles of a contiguous
+// range.  The tile's samples are handled in rounds of kSamplesPerWarp, and
+// the locations and weights of the next round are loaded while the current
+// round gathers:
+//   1. footprint: each lane takes two samples (coalesced loads of locations
+//      and weights), computes the cell, the four corner keys (-1 when off
+//      the map) and the four corner weights with the attention weight folded
+//      in, and stores them as two 16-byte records in shared memory (per-group
+//      stride padded so the four groups' reads never share a bank);
+//   2. gather: each group walks its query's samples; per sample one 16-byte
+//      broadcast read of keys and of weights, one 128-bit load per lane and
+//      live corner, and 4 FMAs per channel, accumulated in fp32 registers.
+// The group writes its query's head_dim outputs once, as 128-bit stores.
 #pragma once
 
 #include "msda_device.cuh"
 
 namespace msda {
 
+#ifndef MSDA_FWD_UNROLL
+#define MSDA_FWD_UNROLL 2
+#endif
+#ifndef MSDA_FWD_MIN_BLOCKS
+#define MSDA_FWD_MIN_BLOCKS 4
+#endif
+#define MSDA_PRAGMA(x) _Pragma(#x)
+#define MSDA_UNROLL(n) MSDA_PRAGMA(unroll n)
+
+// Stores the footprint records of the round fetched in f.
+template <int kSPG, int kStride>
+__device__ __forceinline__ void forward_records(int4* wk, float4* ww, const SampleFetch& f,
+                                                const LevelInfo* s_levels,
+                                                const unsigned char* s_level_of, int r0,
+                                                int lane) {
+#pragma unroll
+    for (int h = 0; h < kSamplesPerWarp / 32; ++h) {
+        const int s = lane + 32 * h;
+        const int sg = s / kSPG, sj = s % kSPG;
+        int4 key = make_int4(-1, -1, -1, -1);
+        float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (f.ok[h]) {
+            const LevelInfo lv = s_levels[s_level_of[r0 + sj]];
+            const float a = f.a[h];
+            const Footprint fp = make_footprint(fmaf(f.xy[h].x, (float)lv.W, -0.5f),
+                                                fmaf(f.xy[h].y, (float)lv.H, -0.5f), lv);
+            key = make_int4(fp.key[0], fp.key[1], fp.key[2], fp.key[3]);
+            w = make_float4(fp.key[0] >= 0 ? a * fp.w[0] : 0.f, fp.key[1] >= 0 ? a * fp.w[1] : 0.f,
+                            fp.key[2] >= 0 ? a * fp.w[2] : 0.f, fp.key[3] >= 0 ? a * fp.w[3] : 0.f);
+        }
+        wk[sg * kStride + sj] = key;
+        ww[sg * kStride + sj] = w;
+    }
+}
+
+// tiles_per_cta: CTA c runs tiles [c * tiles_per_cta, (c + 1) * tiles_per_cta).
 template <typename T, int kLanes, int kVPL>
-__global__ void __launch_bounds__(kThreadsPerCta)
+__global__ void __launch_bounds__(kThreadsPerCta, MSDA_FWD_MIN_BLOCKS)
     forward_kernel(const T* __restrict__ value, const int64_t* __restrict__ spatial_shapes,
                    const int64_t* __restrict__ level_start_index, const T* __restrict__ loc,
                    const T* __restrict__ attn, T* __restrict__ out, int num_keys, int num_heads,
-                   int head_dim, int num_levels, int num_points, int num_queries, int rows,
-                   int rows_per_warp) {
-    constexpr int kGroups = 32 / kLanes;
+                   int head_dim, int num_levels, int num_points, int num_queries,
+                   int num_qtiles, int num_tiles, int tiles_per_cta) {
+    using Geom = TileGeom<kLanes>;
+    constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
     constexpr int V = IO<T>::kVec;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    LevelInfo* s_levels = reinterpret_cast<LevelInfo*>(smem_raw);
-    const int LP = num_levels * num_points;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane / kLanes, li = lane % kLanes;
-    const int pts_per_iter = kGroups * LP;
-    float4* s_w = reinterpret_cast<float4*>(smem_raw + sizeof(LevelInfo) * kMaxLevels) +
-                  (size_t)warp * pts_per_iter;
-    int2* s_k = reinterpret_cast<int2*>(
-                    smem_raw + sizeof(LevelInfo) * kMaxLevels +
-                    sizeof(float4) * (size_t)kWarpsPerCta * pts_per_iter) +
-                (size_t)warp * pts_per_iter;
+    __shared__ LevelInfo s_levels[kMaxLevels];
+    __shared__ unsigned char s_level_of[kMaxLevelPoints];
+    __shared__ int4 s_key[kWarpsPerCta][Geom::kRecords];
+    __shared__ float4 s_w[kWarpsPerCta][Geom::kRecords];
 
-    load_level_table(s_levels, spatial_shapes, level_start_index, num_levels, num_keys);
+    load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, num_levels,
+                     num_points, num_keys);
     __syncthreads();
 
-    const int64_t MD = (int64_t)num_heads * head_dim;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane / kLanes, li = lane % kLanes;
+    const int LP = num_levels * num_points;
     const int nvec = head_dim / V;
-    const int row0 = (blockIdx.x * kWarpsPerCta + warp) * rows_per_warp;
+    const unsigned row_bytes = (unsigned)(num_heads * head_dim) * (unsigned)sizeof(T);
+    int4* wk = s_key[warp];
+    float4* ww = s_w[warp];
 
-    for (int it = 0; it < rows_per_warp; it += kGroups) {
-        const int rbase = row0 + it;
-        if (rbase >= rows) break;
-        // ---- phase 1: one footprint per sample, one sample per lane
-        const int64_t pt0 = (int64_t)rbase * LP;
-        for (int t = lane; t < pts_per_iter; t += 32) {
-            const int rl = t / LP;
-            float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            int2 k2 = make_int2(0, 0);
-            if (rbase + rl < rows) {
-                const int j = t - rl * LP;
-                const LevelInfo lv = s_levels[j / num_points];
-                const float2 xy = IO<T>::load_xy(loc + 2 * (pt0 + t));
-                const float a = IO<T>::load_one(attn + pt0 + t);
-                const float x = fmaf(xy.x, (float)lv.W, -0.5f);
-                const float y = fmaf(xy.y, (float)lv.H, -0.5f);
-                Footprint f = make_footprint(x, y, lv);
-                w4 = make_float4(a * f.w[0], a * f.w[1], a * f.w[2], a * f.w[3]);
-                unsigned mask = f.info & 15u;
-                mask &= (w4.x != 0.f ? 1u : 0u) | (w4.y != 0.f ? 2u : 0u) |
-                        (w4.z != 0.f ? 4u : 0u) | (w4.w != 0.f ? 8u : 0u);
-                k2 = make_int2(f.key00, (int)((f.info & ~15u) | mask));
+    StepIter it;
+    it.t = blockIdx.x * tiles_per_cta + warp;
+    it.end = min(num_tiles, (blockIdx.x + 1) * tiles_per_cta);
+    it.r0 = 0;
+    it.LP = LP;
+    it.spg = kSPG;
+    if (!it.valid()) return;
+
+    SampleFetch f;
+    TileCoord tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
+    fetch_samples<T, kSPG>(f, loc, attn, tc, 0, lane, LP, num_queries, num_heads);
+    float acc[kVPL][V];
+#pragma unroll
+    for (int k = 0; k < kVPL; ++k)
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[k][e] = 0.f;
+
+    while (true) {
+        // ---- 1. footprints of this round (inputs fetched one round ahead)
+        forward_records<kSPG, kStride>(wk, ww, f, s_levels, s_level_of, it.r0, lane);
+        __syncwarp();
+        const TileCoord cur = tc;
+        const int r0 = it.r0;
+        const bool last = it.last_round();
+        it.next();
+        const bool more = it.valid();
+        if (more) {
+            tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
+            fetch_samples<T, kSPG>(f, loc, attn, tc, it.r0, lane, LP, num_queries, num_heads);
+        }
+
+        // ---- 2. gather: group g walks its query's samples
+        const char* vbase = reinterpret_cast<const char*>(
+            value + ((int64_t)cur.b * num_keys * num_heads + cur.m) * head_dim);
+        const int nj = min(kSPG, LP - r0);
+        const int4* gk = wk + g * kStride;
+        const float4* gw = ww + g * kStride;
+        MSDA_UNROLL(MSDA_FWD_UNROLL)
+        for (int jj = 0; jj < nj; ++jj) {
+            const int4 k4 = gk[jj];
+            const float4 w4 = gw[jj];
+            const int keys[4] = {k4.x, k4.y, k4.z, k4.w};
+            const float wc[4] = {w4.x, w4.y, w4.z, w4.w};
+            float v[4][kVPL][V];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const char* p = row_ptr(vbase, keys[c], row_bytes);
+#pragma unroll
+                for (int k = 0; k < kVPL; ++k) {
+                    const int vi = li + k * kLanes;
+#pragma unroll
+                    for (int e = 0; e < V; ++e) v[c][k][e] = 0.f;
+                    if (keys[c] >= 0 && vi < nvec) IO<T>::load_vec(p + vi * 16, v[c][k]);
+                }
             }
-            s_w[t] = w4;
-            s_k[t] = k2;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int k = 0; k < kVPL; ++k)
+#pragma unroll
+                    for (int e = 0; e < V; ++e) acc[k][e] = fmaf(wc[c], v[c][k][e], acc[k][e]);
         }
         __syncwarp();
 
-        // ---- phase 2: gather, one row per lane group
-        const int r = rbase + g;
-        if (r < rows) {
-            const int m = r % num_heads;
-            const int b = (r / num_heads) / num_queries;
-            const T* vb = value + ((int64_t)b * num_keys * num_heads + m) * head_dim;
-            float acc[kVPL][V];
+        if (last) {
+            const int q = cur.q0 + g;
+            if (q < num_queries) {
+                T* o = out + (((int64_t)cur.b * num_queries + q) * num_heads + cur.m) * head_dim;
+#pragma unroll
+                for (int k = 0; k < kVPL; ++k) {
+                    const int vi = li + k * kLanes;
+                    if (vi < nvec) IO<T>::store_vec(o + vi * V, acc[k]);
+                }
+            }
 #pragma unroll
             for (int k = 0; k < kVPL; ++k)
 #pragma unroll
                 for (int e = 0; e < V; ++e) acc[k][e] = 0.f;
-            const float4* sw = s_w + g * LP;
-            const int2* sk = s_k + g * LP;
-#pragma unroll 2
-            for (int j = 0; j < LP; ++j) {
-                const float4 w4 = sw[j];
-                const int2 k2 = sk[j];
-                const unsigned mask = (unsigned)k2.y & 15u;
-                const int W = (int)((unsigned)k2.y >> 4);
-                const float wc[4] = {w4.x, w4.y, w4.z, w4.w};
-                float v[4][kVPL][V];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const T* p = vb + (int64_t)corner_key(k2.x, W, c) * MD;
-#pragma unroll
-                    for (int k = 0; k < kVPL; ++k) {
-                        const int vi = li + k * kLanes;
-                        if ((mask >> c & 1u) && vi < nvec) {
-                            IO<T>::load_vec(p + vi * V, v[c][k]);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < V; ++e) v[c][k][e] = 0.f;
-                        }
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int k = 0; k < kVPL; ++k)
-#pragma unroll
-                        for (int e = 0; e < V; ++e) acc[k][e] = fmaf(wc[c], v[c][k][e], acc[k][e]);
-            }
-            T* o = out + (int64_t)r * head_dim;
-#pragma unroll
-            for (int k = 0; k < kVPL; ++k) {
-                const int vi = li + k * kLanes;
-                if (vi < nvec) IO<T>::store_vec(o + vi * V, acc[k]);
-            }
         }
-        __syncwarp();
+        if (!more) break;
     }
 }
 

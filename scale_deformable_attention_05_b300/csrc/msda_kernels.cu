@@ -66,89 +66,101 @@ __global__ void check_shapes_kernel(const int64_t* __restrict__ shapes,
 // ---------------------------------------------------------------- dispatch
 namespace {
 
-constexpr int kRowItersFwd = 2;  // lane-group rows per warp in one CTA, forward
-constexpr int kRowItersBwd = 2;
-constexpr int kMaxPtsPerWarpFwd = 512;
-constexpr int kMaxPtsPerWarpBwd = 256;
-
-int next_pow2(int x) {
-    int p = 1;
-    while (p < x) p <<= 1;
-    return p;
-}
-
 struct Layout {
     int lanes, vpl;
 };
 
-// Lanes per row group and 16-byte vectors per lane for a head of `nvec`
-// vectors and L*P samples per row.
-Layout choose_layout(int nvec, int LP, int max_pts_per_warp) {
-    Layout ly;
+// Lanes per lane group and 16-byte vectors per lane for a head of `nvec`
+// vectors: one vector per lane up to 32 vectors (at least 4 lanes, so a
+// warp tile holds at most 8 queries), then 2 or 4 vectors on 32 lanes.
+Layout choose_layout(int nvec) {
+    Layout ly{4, 1};
     if (nvec <= 32) {
-        ly.lanes = next_pow2(nvec);
-        ly.vpl = 1;
-        while (ly.lanes < 32 && (32 / ly.lanes) * LP > max_pts_per_warp) ly.lanes <<= 1;
+        while (ly.lanes < nvec) ly.lanes <<= 1;
     } else {
         ly.lanes = 32;
-        ly.vpl = (nvec + 31) / 32 <= 2 ? 2 : 4;
+        ly.vpl = nvec <= 64 ? 2 : 4;
     }
     return ly;
 }
 
+#ifndef MSDA_PERSISTENT_WAVES
+#define MSDA_PERSISTENT_WAVES 1
+#endif
+
+int sm_count() {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms > 0 ? sms : 1;
+}
+
+// CTAs of `kernel` that fit on one SM at once (looked up once per kernel).
 template <typename K>
-void allow_big_smem(K kernel, size_t smem) {
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+int resident_ctas(K kernel) {
+    static const int n = [&] {
+        int v = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, kThreadsPerCta, 0) !=
+                cudaSuccess ||
+            v < 1)
+            v = 1;
+        return v;
+    }();
+    return n;
+}
+
+struct TileGrid {
+    int num_qtiles, num_tiles, tiles_per_cta, grid;
+};
+
+// Warp tiles of `queries_per_tile` queries, ordered (b, m, query block).  The grid is
+// MSDA_PERSISTENT_WAVES waves of resident CTAs; each CTA takes a contiguous
+// range of tiles (a multiple of kWarpsPerCta), so consecutive tiles of one head
+// run on one SM and share its L1.
+TileGrid tile_grid(const Problem& pb, int queries_per_tile, int resident) {
+    TileGrid tg;
+    tg.num_qtiles = (pb.Q + queries_per_tile - 1) / queries_per_tile;
+    tg.num_tiles = pb.bs * pb.M * tg.num_qtiles;
+    int64_t per = kWarpsPerCta;
+    if (MSDA_PERSISTENT_WAVES > 0) {
+        const int64_t ctas = (int64_t)sm_count() * resident * MSDA_PERSISTENT_WAVES;
+        per = (tg.num_tiles + ctas - 1) / ctas;
+        per = (per + kWarpsPerCta - 1) / kWarpsPerCta * kWarpsPerCta;
+    }
+    tg.tiles_per_cta = (int)per;
+    tg.grid = (int)((tg.num_tiles + per - 1) / per);
+    return tg;
 }
 
 template <typename T, int kLanes, int kVPL>
 cudaError_t launch_forward_t(const Problem& pb, void* out, cudaStream_t st) {
-    constexpr int kGroups = 32 / kLanes;
-    const int LP = pb.L * pb.P;
-    const int rows = pb.bs * pb.Q * pb.M;
-    const int rows_per_warp = kGroups * kRowItersFwd;
-    const int rows_per_cta = rows_per_warp * kWarpsPerCta;
-    const size_t smem = sizeof(LevelInfo) * kMaxLevels +
-                        (size_t)kWarpsPerCta * kGroups * LP * (sizeof(float4) + sizeof(int2));
     auto kernel = forward_kernel<T, kLanes, kVPL>;
-    allow_big_smem(kernel, smem);
-    const int grid = (rows + rows_per_cta - 1) / rows_per_cta;
-    kernel<<<grid, kThreadsPerCta, smem, st>>>(
+    const TileGrid tg = tile_grid(pb, 32 / kLanes, resident_ctas(kernel));
+    kernel<<<tg.grid, kThreadsPerCta, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<T*>(out), pb.K, pb.M, pb.D, pb.L, pb.P, pb.Q,
-        rows, rows_per_warp);
+        tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta);
     return cudaGetLastError();
 }
 
 template <typename T, int kLanes, int kVPL>
 cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv32,
                               void* grad_loc, void* grad_attn, cudaStream_t st) {
-    constexpr int kGroups = 32 / kLanes;
-    const int LP = pb.L * pb.P;
-    const int rows = pb.bs * pb.Q * pb.M;
-    const int rows_per_warp = kGroups * kRowItersBwd;
-    const int rows_per_cta = rows_per_warp * kWarpsPerCta;
-    const size_t smem = sizeof(LevelInfo) * kMaxLevels +
-                        (size_t)kWarpsPerCta * kGroups * LP * (3 * sizeof(float4) + sizeof(int2));
     auto kernel = backward_kernel<T, kLanes, kVPL>;
-    allow_big_smem(kernel, smem);
-    const int grid = (rows + rows_per_cta - 1) / rows_per_cta;
-    kernel<<<grid, kThreadsPerCta, smem, st>>>(
+    const TileGrid tg = tile_grid(pb, 32 / kLanes, resident_ctas(kernel));
+    kernel<<<tg.grid, kThreadsPerCta, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
         static_cast<T*>(grad_loc), static_cast<T*>(grad_attn), pb.K, pb.M, pb.D, pb.L, pb.P,
-        pb.Q, rows, rows_per_warp);
+        pb.Q, tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta);
     return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t dispatch_forward(const Problem& pb, void* out, cudaStream_t st) {
-    const Layout ly = choose_layout(pb.D / IO<T>::kVec, pb.L * pb.P, kMaxPtsPerWarpFwd);
+    const Layout ly = choose_layout(pb.D / IO<T>::kVec);
     if (ly.vpl == 1) {
         switch (ly.lanes) {
-            case 1: return launch_forward_t<T, 1, 1>(pb, out, st);
-            case 2: return launch_forward_t<T, 2, 1>(pb, out, st);
             case 4: return launch_forward_t<T, 4, 1>(pb, out, st);
             case 8: return launch_forward_t<T, 8, 1>(pb, out, st);
             case 16: return launch_forward_t<T, 16, 1>(pb, out, st);
@@ -159,14 +171,40 @@ cudaError_t dispatch_forward(const Problem& pb, void* out, cudaStream_t st) {
     return launch_forward_t<T, 32, 4>(pb, out, st);
 }
 
+template <typename T, int kLanes, int kVPL>
+cudaError_t launch_backward_merge_t(const Problem& pb, int log2_points, const void* grad_out,
+                                    float* gv32, void* grad_loc, void* grad_attn,
+                                    cudaStream_t st) {
+    auto kernel = backward_merge_kernel<T, kLanes, kVPL>;
+    const TileGrid tg = tile_grid(pb, 32 / kLanes, resident_ctas(kernel));
+    kernel<<<tg.grid, kThreadsPerCta, 0, st>>>(
+        static_cast<const T*>(pb.value), pb.shapes, pb.lsi, static_cast<const T*>(pb.loc),
+        static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
+        static_cast<T*>(grad_loc), static_cast<T*>(grad_attn), pb.K, pb.M, pb.D, pb.L, pb.P,
+        log2_points, pb.Q, tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t dispatch_backward(const Problem& pb, const void* g, float* gv32, void* gl, void* ga,
                               cudaStream_t st) {
-    const Layout ly = choose_layout(pb.D / IO<T>::kVec, pb.L * pb.P, kMaxPtsPerWarpBwd);
+    const Layout ly = choose_layout(pb.D / IO<T>::kVec);
+#ifndef MSDA_NO_MERGE_PATH
+    // Merged scatter for rows of at least 512 bytes (one lane group per warp,
+    // one query per tile): duplicate corner rows among the query's samples of a
+    // 32-sample round are sent to L2 once.  For shorter rows the per-sample
+    // reds of backward_kernel measured faster (the merge costs more issue
+    // slots than the L2 write traffic it saves).
+    int log2p = 0;
+    while ((1 << log2p) < pb.P) ++log2p;
+    if (ly.lanes == 32 && (1 << log2p) == pb.P && pb.P <= 32) {
+        if (ly.vpl == 1) return launch_backward_merge_t<T, 32, 1>(pb, log2p, g, gv32, gl, ga, st);
+        if (ly.vpl == 2) return launch_backward_merge_t<T, 32, 2>(pb, log2p, g, gv32, gl, ga, st);
+        return launch_backward_merge_t<T, 32, 4>(pb, log2p, g, gv32, gl, ga, st);
+    }
+#endif
     if (ly.vpl == 1) {
         switch (ly.lanes) {
-            case 1: return launch_backward_t<T, 1, 1>(pb, g, gv32, gl, ga, st);
-            case 2: return launch_backward_t<T, 2, 1>(pb, g, gv32, gl, ga, st);
             case 4: return launch_backward_t<T, 4, 1>(pb, g, gv32, gl, ga, st);
             case 8: return launch_backward_t<T, 8, 1>(pb, g, gv32, gl, ga, st);
             case 16: return launch_backward_t<T, 16, 1>(pb, g, gv32, gl, ga, st);
@@ -178,9 +216,7 @@ cudaError_t dispatch_backward(const Problem& pb, const void* g, float* gv32, voi
 }
 
 int grid_for(size_t n, int threads) {
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = sm_count();
     const size_t want = (n + threads - 1) / threads;
     return (int)std::max<size_t>(1, std::min<size_t>(want, (size_t)sms * 8));
 }

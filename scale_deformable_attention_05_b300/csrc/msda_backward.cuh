@@ -41,21 +41,38 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
 #define MSDA_BWD_MIN_BLOCKS 2
 #endif
 
-// Stores the footprint records (corner keys, a*w_c, (a, fx, fy, level)) of
-// the round fetched in f.
+#ifndef MSDA_BWD_BATCH
+#define MSDA_BWD_BATCH 8
+#endif
+
+// Stores the footprint records of the round fetched in f: corner keys, the
+// weight each corner's grad_value red carries, and (a, fx, fy, level).
+//
+// Red weights are merged within aligned segments of kDedup lanes that hold
+// the points of one (query, level): the samples of a query share its
+// grad_output row, so when several of them touch the same pixel the lowest
+// lane sends one red with the summed weight a*w_c and the others send none.
+// Corners can only coincide within a pixel parity class, so each class is
+// compared across the segment with xor shuffles.
 template <int kSPG, int kStride>
 __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* wax,
                                                  const SampleFetch& f,
                                                  const LevelInfo* s_levels,
                                                  const unsigned char* s_level_of, int r0,
-                                                 int lane) {
+                                                 int lane, int dedup) {
 #pragma unroll
     for (int h = 0; h < kSamplesPerWarp / 32; ++h) {
         const int s = lane + 32 * h;
         const int sg = s / kSPG, sj = s % kSPG;
         int4 key = make_int4(-1, -1, -1, -1);
-        float4 aw = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 aux = make_float4(0.f, 0.f, 0.f, 0.f);
+        ClassCorners cc;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            cc.key[t] = -1;
+            cc.w[t] = 0.f;
+        }
+        int px = 0, py = 0;
         if (f.ok[h]) {
             const int l = s_level_of[r0 + sj];
             const LevelInfo lv = s_levels[l];
@@ -63,12 +80,34 @@ __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* 
             const Footprint fp = make_footprint(fmaf(f.xy[h].x, (float)lv.W, -0.5f),
                                                 fmaf(f.xy[h].y, (float)lv.H, -0.5f), lv);
             key = make_int4(fp.key[0], fp.key[1], fp.key[2], fp.key[3]);
-            aw = make_float4(fp.key[0] >= 0 ? a * fp.w[0] : 0.f, fp.key[1] >= 0 ? a * fp.w[1] : 0.f,
-                             fp.key[2] >= 0 ? a * fp.w[2] : 0.f, fp.key[3] >= 0 ? a * fp.w[3] : 0.f);
             aux = make_float4(fp.live ? a : 0.f, fp.fx, fp.fy, __int_as_float(l));
+            cc = class_corners(fp, a);
+            px = fp.x0 & 1;
+            py = fp.y0 & 1;
+        }
+        float rw[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int k = cc.key[t];
+            float A = cc.w[t];
+            bool lead = k >= 0;
+            for (int i = 1; i < dedup; ++i) {
+                const int kp = __shfl_xor_sync(0xffffffffu, k, i);
+                const float wp = __shfl_xor_sync(0xffffffffu, cc.w[t], i);
+                if (kp == k) {
+                    if ((lane ^ i) < lane) lead = false;
+                    else A += wp;
+                }
+            }
+            // class t sits at corner ((t>>1)^py, (t&1)^px)
+            const int c = (((t >> 1) ^ py) << 1) | ((t & 1) ^ px);
+            const float r = lead ? A : 0.f;
+#pragma unroll
+            for (int cc2 = 0; cc2 < 4; ++cc2)
+                if (c == cc2) rw[cc2] = r;
         }
         wk[sg * kStride + sj] = key;
-        waw[sg * kStride + sj] = aw;
+        waw[sg * kStride + sj] = make_float4(rw[0], rw[1], rw[2], rw[3]);
         wax[sg * kStride + sj] = aux;
     }
 }
@@ -93,7 +132,10 @@ __device__ __forceinline__ void load_grad_row(float (&gr)[kVPL][IO<T>::kVec],
 
 // tiles_per_cta: CTA c runs tiles [c * tiles_per_cta, (c + 1) * tiles_per_cta).
 template <typename T, int kLanes, int kVPL>
-__global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
+__global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
+                                  MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS > 0
+                                      ? MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS
+                                      : 1)
     backward_kernel(const T* __restrict__ value, const int64_t* __restrict__ spatial_shapes,
                     const int64_t* __restrict__ level_start_index, const T* __restrict__ loc,
                     const T* __restrict__ attn, const T* __restrict__ grad_out,
@@ -104,17 +146,18 @@ __global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
     using Geom = TileGeom<kLanes>;
     constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
     constexpr int V = IO<T>::kVec;
-    constexpr int kBatch = 8;                      // samples per transpose-reduce
-    constexpr int kHeld = 32 / kLanes;             // dot products a lane keeps after it
+    // samples per transpose-reduce (at least kLanes / 4, so a lane keeps >= 1 value)
+    constexpr int kBatch = MSDA_BWD_BATCH > kLanes / 4 ? MSDA_BWD_BATCH : kLanes / 4;
+    constexpr int kHeld = 4 * kBatch / kLanes;     // dot products a lane keeps after it
     constexpr int kSampPerLane = kHeld >= 4 ? kHeld / 4 : 1;
     constexpr int kLanesPerSamp = kHeld >= 4 ? 1 : 4 / kHeld;
     static_assert(kSPG % kBatch == 0, "round must hold whole batches");
 
     __shared__ LevelInfo s_levels[kMaxLevels];
     __shared__ unsigned char s_level_of[kMaxLevelPoints];
-    __shared__ int4 s_key[kWarpsPerCta][Geom::kRecords];
-    __shared__ float4 s_aw[kWarpsPerCta][Geom::kRecords];
-    __shared__ float4 s_aux[kWarpsPerCta][Geom::kRecords];
+    __shared__ int4 s_key[MSDA_BWD_WARPS][Geom::kRecords];
+    __shared__ float4 s_aw[MSDA_BWD_WARPS][Geom::kRecords];
+    __shared__ float4 s_aux[MSDA_BWD_WARPS][Geom::kRecords];
 
     load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, num_levels,
                      num_points, num_keys);
@@ -126,6 +169,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
     const int nvec = head_dim / V;
     const unsigned row_bytes = (unsigned)(num_heads * head_dim) * (unsigned)sizeof(T);
     const unsigned row_bytes32 = (unsigned)(num_heads * head_dim) * 4u;
+    // lanes that hold the points of one (query, level): an aligned segment
+    // of up to 4 lanes when the points per level tile the round
+    const int dedup = (num_points % 4 == 0 && kSPG % 4 == 0) ? 4
+                      : (num_points % 2 == 0 && kSPG % 2 == 0) ? 2 : 1;
     int4* wk = s_key[warp];
     float4* waw = s_aw[warp];
     float4* wax = s_aux[warp];
@@ -136,6 +183,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
     it.r0 = 0;
     it.LP = LP;
     it.spg = kSPG;
+    it.stride = MSDA_BWD_WARPS;
     if (!it.valid()) return;
 
     SampleFetch f;
@@ -147,7 +195,8 @@ __global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
 
     while (true) {
         // ---- 1. footprints of this round (inputs fetched one round ahead)
-        backward_records<kSPG, kStride>(wk, waw, wax, f, s_levels, s_level_of, it.r0, lane);
+        backward_records<kSPG, kStride>(wk, waw, wax, f, s_levels, s_level_of, it.r0, lane,
+                                        dedup);
         __syncwarp();
         const TileCoord cur = tc;
         const int r0 = it.r0;
@@ -203,7 +252,8 @@ __global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
 #pragma unroll
                         for (int e = 0; e < V; ++e) d = fmaf(gr[k][e], v[k][e], d);
                     dots[s8 * 4 + c] = d;
-                    if (keys[c] >= 0) {
+                    // merged duplicates carry red weight 0 and send nothing
+                    if (keys[c] >= 0 && awc[c] != 0.f) {
                         float* gp = reinterpret_cast<float*>(
                             gvbase + (size_t)(unsigned)keys[c] * row_bytes32);
 #pragma unroll
@@ -290,7 +340,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
 // queries).  The location and weight gradients come from the corner dot
 // products as in backward_kernel, each group handling its own query's samples.
 template <typename T, int kLanes, int kVPL>
-__global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
+__global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
+                                  MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS > 0
+                                      ? MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS
+                                      : 1)
     backward_merge_kernel(const T* __restrict__ value, const int64_t* __restrict__ spatial_shapes,
                           const int64_t* __restrict__ level_start_index,
                           const T* __restrict__ loc, const T* __restrict__ attn,
@@ -311,10 +364,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
 
     __shared__ LevelInfo s_levels[kMaxLevels];
     __shared__ unsigned char s_level_of[kMaxLevelPoints];
-    __shared__ int4 s_key[kWarpsPerCta][32];       // corner keys (corner order) per round sample
-    __shared__ float4 s_aux[kWarpsPerCta][32];     // (a, fx, fy, level) per round sample
-    __shared__ int s_ukey[kWarpsPerCta][kMaxUnique];
-    __shared__ float4 s_uA[kWarpsPerCta][kMaxUnique];
+    __shared__ int4 s_key[MSDA_BWD_WARPS][32];       // corner keys (corner order) per round sample
+    __shared__ float4 s_aux[MSDA_BWD_WARPS][32];     // (a, fx, fy, level) per round sample
+    __shared__ int s_ukey[MSDA_BWD_WARPS][kMaxUnique];
+    __shared__ float4 s_uA[MSDA_BWD_WARPS][kMaxUnique];
 
     load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, num_levels,
                      num_points, num_keys);
@@ -335,6 +388,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, MSDA_BWD_MIN_BLOCKS)
     it.r0 = 0;
     it.LP = S;
     it.spg = 32;
+    it.stride = MSDA_BWD_WARPS;
     if (!it.valid()) return;
 
     // round sample s = r0 + lane  ->  (level, query, point)

@@ -28,8 +28,13 @@
 
 namespace msda {
 
-constexpr int kWarpsPerCta = 8;
-constexpr int kThreadsPerCta = kWarpsPerCta * 32;
+// Warps per CTA of the forward and backward kernels.
+#ifndef MSDA_FWD_WARPS
+#define MSDA_FWD_WARPS 8
+#endif
+#ifndef MSDA_BWD_WARPS
+#define MSDA_BWD_WARPS 16
+#endif
 constexpr int kMaxLevels = 16;
 constexpr int kMaxLevelPoints = 256;
 // Samples whose footprints one warp computes per round (two per lane).
@@ -113,6 +118,95 @@ struct IO<__nv_bfloat16> {
     }
     __device__ __forceinline__ static void store_xy(T* p, float x, float y) {
         __stcs(reinterpret_cast<unsigned int*>(p), pack_bf16x2(x, y));
+    }
+};
+
+// 32-byte vectors (one 256-bit load per lane, sm_100+).  Value rows are read
+// through the non-coherent path and kept in L1.
+template <typename T>
+struct IO32;
+
+template <>
+struct IO32<float> {
+    static constexpr int kVec = 8;
+    __device__ __forceinline__ static void load(const void* p, float (&v)[kVec]) {
+        asm volatile("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                       "=f"(v[6]), "=f"(v[7])
+                     : "l"(p));
+    }
+    __device__ __forceinline__ static void load_stream(const float* p, float (&v)[kVec]) {
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+        const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+    __device__ __forceinline__ static void store(float* p, const float (&v)[kVec]) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+        __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(v[4], v[5], v[6], v[7]));
+    }
+};
+
+template <>
+struct IO32<__nv_bfloat16> {
+    using T = __nv_bfloat16;
+    static constexpr int kVec = 16;
+    __device__ __forceinline__ static void unpack(const uint32_t (&u)[8], float (&v)[kVec]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[2 * i] = bf16_lo(u[i]);
+            v[2 * i + 1] = bf16_hi(u[i]);
+        }
+    }
+    __device__ __forceinline__ static void load(const void* p, float (&v)[kVec]) {
+        uint32_t u[8];
+        asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
+                       "=r"(u[6]), "=r"(u[7])
+                     : "l"(p));
+        unpack(u, v);
+    }
+    __device__ __forceinline__ static void load_stream(const T* p, float (&v)[kVec]) {
+        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(p));
+        const uint4 b = __ldcs(reinterpret_cast<const uint4*>(p) + 1);
+        const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        unpack(u, v);
+    }
+    __device__ __forceinline__ static void store(T* p, const float (&v)[kVec]) {
+        uint4 a, b;
+        a.x = pack_bf16x2(v[0], v[1]); a.y = pack_bf16x2(v[2], v[3]);
+        a.z = pack_bf16x2(v[4], v[5]); a.w = pack_bf16x2(v[6], v[7]);
+        b.x = pack_bf16x2(v[8], v[9]); b.y = pack_bf16x2(v[10], v[11]);
+        b.z = pack_bf16x2(v[12], v[13]); b.w = pack_bf16x2(v[14], v[15]);
+        __stcs(reinterpret_cast<uint4*>(p), a);
+        __stcs(reinterpret_cast<uint4*>(p) + 1, b);
+    }
+};
+
+// Row vectors of kBytes (16 or 32) bytes: the loads of value rows and the
+// stores of output rows in the forward kernel.
+template <typename T, int kBytes>
+struct VecIO;
+
+template <typename T>
+struct VecIO<T, 16> {
+    static constexpr int kVec = IO<T>::kVec;
+    __device__ __forceinline__ static void load(const void* p, float (&v)[kVec]) {
+        IO<T>::load_vec(p, v);
+    }
+    __device__ __forceinline__ static void store(T* p, const float (&v)[kVec]) {
+        IO<T>::store_vec(p, v);
+    }
+};
+
+template <typename T>
+struct VecIO<T, 32> {
+    static constexpr int kVec = IO32<T>::kVec;
+    __device__ __forceinline__ static void load(const void* p, float (&v)[kVec]) {
+        IO32<T>::load(p, v);
+    }
+    __device__ __forceinline__ static void store(T* p, const float (&v)[kVec]) {
+        IO32<T>::store(p, v);
     }
 };
 
@@ -225,7 +319,7 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
 // Geometry of a warp tile for lane groups of kLanes lanes.
 template <int kLanes>
 struct TileGeom {
-    static_assert(kLanes == 4 || kLanes == 8 || kLanes == 16 || kLanes == 32, "lane group");
+    static_assert(kLanes >= 1 && kLanes <= 32 && (kLanes & (kLanes - 1)) == 0, "lane group");
     static constexpr int kGroups = 32 / kLanes;                  // queries per warp tile
     static constexpr int kSPG = kSamplesPerWarp / kGroups;       // samples per group per round
     static constexpr int kStride = kSPG + 1;                     // padded record stride (16 B units)
@@ -278,16 +372,16 @@ __device__ __forceinline__ void fetch_samples(SampleFetch& f, const T* __restric
 }
 
 // The (tile, round) steps one warp executes: tiles begin + warp, begin + warp
-// + kWarpsPerCta, ... below end; each tile in rounds of kSPG samples per group.
+// + stride, ... below end; each tile in rounds of spg samples per group.
 struct StepIter {
-    int t, r0, end, LP, spg;
+    int t, r0, end, LP, spg, stride;  // stride: warps per CTA
     __device__ __forceinline__ bool valid() const { return t < end; }
     __device__ __forceinline__ bool last_round() const { return r0 + spg >= LP; }
     __device__ __forceinline__ void next() {
         r0 += spg;
         if (r0 >= LP) {
             r0 = 0;
-            t += kWarpsPerCta;
+            t += stride;
         }
     }
 };

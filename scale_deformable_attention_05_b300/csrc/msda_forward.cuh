@@ -60,20 +60,43 @@ __device__ __forceinline__ void forward_records(int4* wk, float4* ww, const Samp
 }
 
 // tiles_per_cta: CTA c runs tiles [c * tiles_per_cta, (c + 1) * tiles_per_cta).
-template <typename T, int kLanes, int kVPL>
-__global__ void __launch_bounds__(kThreadsPerCta, MSDA_FWD_MIN_BLOCKS)
+#ifndef MSDA_FWD_MIN_BLOCKS8
+#define MSDA_FWD_MIN_BLOCKS8 3
+#endif
+
+// Resident warps per SM the register budget is sized for, by the number of
+// channels a lane holds (each corner's loaded vector is that many registers);
+// __launch_bounds__ takes it as CTAs of MSDA_FWD_WARPS warps.
+constexpr int forward_warps_per_sm(int channels_per_lane) {
+    return 8 * (channels_per_lane <= 4   ? MSDA_FWD_MIN_BLOCKS
+                : channels_per_lane <= 8 ? MSDA_FWD_MIN_BLOCKS8
+                : channels_per_lane <= 16 ? 2
+                                          : 1);
+}
+constexpr int forward_min_blocks(int channels_per_lane) {
+    return forward_warps_per_sm(channels_per_lane) >= MSDA_FWD_WARPS
+               ? forward_warps_per_sm(channels_per_lane) / MSDA_FWD_WARPS
+               : 1;
+}
+
+// kVB: bytes per row vector and lane (16, or 32 with 256-bit loads).
+template <typename T, int kLanes, int kVPL, int kVB>
+__global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
+                                  forward_min_blocks(kVPL * kVB / (int)sizeof(T)))
     forward_kernel(const T* __restrict__ value, const int64_t* __restrict__ spatial_shapes,
                    const int64_t* __restrict__ level_start_index, const T* __restrict__ loc,
                    const T* __restrict__ attn, T* __restrict__ out, int num_keys, int num_heads,
                    int head_dim, int num_levels, int num_points, int num_queries,
                    int num_qtiles, int num_tiles, int tiles_per_cta) {
     using Geom = TileGeom<kLanes>;
+    using VIO = VecIO<T, kVB>;
     constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
-    constexpr int V = IO<T>::kVec;
+    constexpr int V = VIO::kVec;
     __shared__ LevelInfo s_levels[kMaxLevels];
     __shared__ unsigned char s_level_of[kMaxLevelPoints];
-    __shared__ int4 s_key[kWarpsPerCta][Geom::kRecords];
-    __shared__ float4 s_w[kWarpsPerCta][Geom::kRecords];
+    constexpr int kWarps = MSDA_FWD_WARPS;
+    __shared__ int4 s_key[kWarps][Geom::kRecords];
+    __shared__ float4 s_w[kWarps][Geom::kRecords];
 
     load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, num_levels,
                      num_points, num_keys);
@@ -93,6 +116,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, MSDA_FWD_MIN_BLOCKS)
     it.r0 = 0;
     it.LP = LP;
     it.spg = kSPG;
+    it.stride = kWarps;
     if (!it.valid()) return;
 
     SampleFetch f;
@@ -139,7 +163,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, MSDA_FWD_MIN_BLOCKS)
                     const int vi = li + k * kLanes;
 #pragma unroll
                     for (int e = 0; e < V; ++e) v[c][k][e] = 0.f;
-                    if (keys[c] >= 0 && vi < nvec) IO<T>::load_vec(p + vi * 16, v[c][k]);
+                    if (keys[c] >= 0 && vi < nvec) VIO::load(p + vi * kVB, v[c][k]);
                 }
             }
 #pragma unroll
@@ -158,7 +182,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, MSDA_FWD_MIN_BLOCKS)
 #pragma unroll
                 for (int k = 0; k < kVPL; ++k) {
                     const int vi = li + k * kLanes;
-                    if (vi < nvec) IO<T>::store_vec(o + vi * V, acc[k]);
+                    if (vi < nvec) VIO::store(o + vi * V, acc[k]);
                 }
             }
 #pragma unroll

@@ -95,12 +95,19 @@ int sm_count() {
     return sms > 0 ? sms : 1;
 }
 
+#ifndef MSDA_SMEM_CARVEOUT
+#define MSDA_SMEM_CARVEOUT -1
+#endif
+
 // CTAs of `kernel` that fit on one SM at once (looked up once per kernel).
 template <typename K>
-int resident_ctas(K kernel) {
+int resident_ctas(K kernel, int threads) {
     static const int n = [&] {
+        if (MSDA_SMEM_CARVEOUT >= 0)
+            cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 MSDA_SMEM_CARVEOUT);
         int v = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, kThreadsPerCta, 0) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, 0) !=
                 cudaSuccess ||
             v < 1)
             v = 1;
@@ -115,28 +122,30 @@ struct TileGrid {
 
 // Warp tiles of `queries_per_tile` queries, ordered (b, m, query block).  The grid is
 // MSDA_PERSISTENT_WAVES waves of resident CTAs; each CTA takes a contiguous
-// range of tiles (a multiple of kWarpsPerCta), so consecutive tiles of one head
+// range of tiles (a multiple of its warps), so consecutive tiles of one head
 // run on one SM and share its L1.
-TileGrid tile_grid(const Problem& pb, int queries_per_tile, int resident) {
+TileGrid tile_grid(const Problem& pb, int queries_per_tile, int resident, int warps) {
     TileGrid tg;
     tg.num_qtiles = (pb.Q + queries_per_tile - 1) / queries_per_tile;
     tg.num_tiles = pb.bs * pb.M * tg.num_qtiles;
-    int64_t per = kWarpsPerCta;
+    int64_t per = warps;
     if (MSDA_PERSISTENT_WAVES > 0) {
         const int64_t ctas = (int64_t)sm_count() * resident * MSDA_PERSISTENT_WAVES;
         per = (tg.num_tiles + ctas - 1) / ctas;
-        per = (per + kWarpsPerCta - 1) / kWarpsPerCta * kWarpsPerCta;
+        per = (per + warps - 1) / warps * warps;
     }
     tg.tiles_per_cta = (int)per;
     tg.grid = (int)((tg.num_tiles + per - 1) / per);
     return tg;
 }
 
-template <typename T, int kLanes, int kVPL>
+template <typename T, int kLanes, int kVPL, int kVB>
 cudaError_t launch_forward_t(const Problem& pb, void* out, cudaStream_t st) {
-    auto kernel = forward_kernel<T, kLanes, kVPL>;
-    const TileGrid tg = tile_grid(pb, 32 / kLanes, resident_ctas(kernel));
-    kernel<<<tg.grid, kThreadsPerCta, 0, st>>>(
+    auto kernel = forward_kernel<T, kLanes, kVPL, kVB>;
+    constexpr int kThreads = MSDA_FWD_WARPS * 32;
+    const TileGrid tg =
+        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_FWD_WARPS);
+    kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<T*>(out), pb.K, pb.M, pb.D, pb.L, pb.P, pb.Q,
         tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta);
@@ -147,8 +156,10 @@ template <typename T, int kLanes, int kVPL>
 cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv32,
                               void* grad_loc, void* grad_attn, cudaStream_t st) {
     auto kernel = backward_kernel<T, kLanes, kVPL>;
-    const TileGrid tg = tile_grid(pb, 32 / kLanes, resident_ctas(kernel));
-    kernel<<<tg.grid, kThreadsPerCta, 0, st>>>(
+    constexpr int kThreads = MSDA_BWD_WARPS * 32;
+    const TileGrid tg =
+        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS);
+    kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
         static_cast<T*>(grad_loc), static_cast<T*>(grad_attn), pb.K, pb.M, pb.D, pb.L, pb.P,
@@ -156,19 +167,45 @@ cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv
     return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t dispatch_forward(const Problem& pb, void* out, cudaStream_t st) {
-    const Layout ly = choose_layout(pb.D / IO<T>::kVec);
+#ifndef MSDA_FWD_VEC32
+#define MSDA_FWD_VEC32 1
+#endif
+
+template <typename T, int kVB>
+cudaError_t dispatch_forward_vec(const Problem& pb, void* out, cudaStream_t st) {
+    const int nvec = pb.D * (int)sizeof(T) / kVB;
+    Layout ly{1, 1};
+    if (nvec <= 32) {
+        while (ly.lanes < nvec) ly.lanes <<= 1;
+    } else {
+        ly.lanes = 32;
+        ly.vpl = nvec <= 64 ? 2 : 4;
+    }
+    if (kVB == 16 && ly.lanes < 4) ly.lanes = 4;
     if (ly.vpl == 1) {
         switch (ly.lanes) {
-            case 4: return launch_forward_t<T, 4, 1>(pb, out, st);
-            case 8: return launch_forward_t<T, 8, 1>(pb, out, st);
-            case 16: return launch_forward_t<T, 16, 1>(pb, out, st);
-            default: return launch_forward_t<T, 32, 1>(pb, out, st);
+            case 1: return launch_forward_t<T, 1, 1, kVB>(pb, out, st);
+            case 2: return launch_forward_t<T, 2, 1, kVB>(pb, out, st);
+            case 4: return launch_forward_t<T, 4, 1, kVB>(pb, out, st);
+            case 8: return launch_forward_t<T, 8, 1, kVB>(pb, out, st);
+            case 16: return launch_forward_t<T, 16, 1, kVB>(pb, out, st);
+            default: return launch_forward_t<T, 32, 1, kVB>(pb, out, st);
         }
     }
-    if (ly.vpl == 2) return launch_forward_t<T, 32, 2>(pb, out, st);
-    return launch_forward_t<T, 32, 4>(pb, out, st);
+    if (ly.vpl == 2) return launch_forward_t<T, 32, 2, kVB>(pb, out, st);
+    return launch_forward_t<T, 32, 4, kVB>(pb, out, st);
+}
+
+// Rows of 1 KB or more (two or more 16-byte vectors per lane) use 256-bit
+// loads: half the load instructions, measured faster on head_dim 256 fp32.
+// Shorter rows keep 128-bit loads, which measured as fast or faster.
+template <typename T>
+cudaError_t dispatch_forward(const Problem& pb, void* out, cudaStream_t st) {
+    const int row = pb.D * (int)sizeof(T);
+    if (row % 32 == 0 && row <= 2048 &&
+        (MSDA_FWD_VEC32 == 2 || (MSDA_FWD_VEC32 == 1 && row >= 1024)))
+        return dispatch_forward_vec<T, 32>(pb, out, st);
+    return dispatch_forward_vec<T, 16>(pb, out, st);
 }
 
 template <typename T, int kLanes, int kVPL>
@@ -176,8 +213,10 @@ cudaError_t launch_backward_merge_t(const Problem& pb, int log2_points, const vo
                                     float* gv32, void* grad_loc, void* grad_attn,
                                     cudaStream_t st) {
     auto kernel = backward_merge_kernel<T, kLanes, kVPL>;
-    const TileGrid tg = tile_grid(pb, 32 / kLanes, resident_ctas(kernel));
-    kernel<<<tg.grid, kThreadsPerCta, 0, st>>>(
+    constexpr int kThreads = MSDA_BWD_WARPS * 32;
+    const TileGrid tg =
+        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS);
+    kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
         static_cast<T*>(grad_loc), static_cast<T*>(grad_attn), pb.K, pb.M, pb.D, pb.L, pb.P,

@@ -218,6 +218,27 @@ def _config(wl, args):
             "parallelism": f"replicas x{args.gpus} (each rank its own batch)"}
 
 
+# ------------------------------------------------------------ replica logic
+def rank_workload(wl, rank):
+    """The batch rank `rank` draws: every replica its own seeded inputs (weak scaling)."""
+    return wl.with_(seed=wl.seed + 7919 * rank)
+
+
+def max_over_ranks(x, dist=None, device=None):
+    """Max of a per-rank float over all ranks (the job's time is its slowest rank)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world_size, ms):
+    """Units all ranks processed per second, over the max-over-ranks time in ms."""
+    return units_per_rank * world_size / (ms / 1e3)
+
+
 # -------------------------------------------------------------- native arm
 def run_native(args, wl):
     import torch
@@ -230,9 +251,7 @@ def run_native(args, wl):
     from scale_deformable_attention_05_b300 import binding as B
 
     dev = torch.device("cuda", local)
-    # each rank draws its own batch (weak scaling)
-    wl_r = wl.with_(seed=wl.seed + 7919 * rank)
-    inp = gen.make_inputs(wl_r)
+    inp = gen.make_inputs(rank_workload(wl, rank))
 
     def t(name):
         if wl.dtype == "bf16":
@@ -303,11 +322,7 @@ def run_native(args, wl):
     bwd_ms = [e[2].elapsed_time(e[3]) for e in ev]
     step_ms = [e[0].elapsed_time(e[3]) for e in ev]
     mean = lambda xs: sum(xs) / len(xs)
-    ms_step = mean(step_ms)
-    if dist:
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = max_over_ranks(mean(step_ms), dist, dev)
 
     assert B.msda_last_device_error() == 0
 
@@ -342,12 +357,8 @@ def run_native(args, wl):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / n_e2e
-        if dist:
-            tt = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
-        e2e = {"value": wl.points * ws / (e2e_ms / 1e3), "unit": "points/s",
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, dev)
+        e2e = {"value": job_rate(wl.points, ws, e2e_ms), "unit": "points/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "path": "pinned host -> device copies, msda_forward, msda_backward, "
                        "device -> pinned host copies of output and the three gradients"}
@@ -383,7 +394,7 @@ def run_native(args, wl):
                 "traffic": _profiled_traffic(wl.name, kname)}
 
     line = {
-        "metric": METRIC, "value": wl.points * ws / (ms_step / 1e3), "unit": "points/s",
+        "metric": METRIC, "value": job_rate(wl.points, ws, ms_step), "unit": "points/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic", "config": _config(wl, args),

@@ -254,8 +254,9 @@ def run_native(args, wl):
     inp = gen.make_inputs(rank_workload(wl, rank))
 
     def t(name):
-        if wl.dtype == "bf16":
-            return torch.from_numpy(inp[name + "_bf16"].view(np.int16).copy()).view(torch.bfloat16)
+        if wl.dtype in ("bf16", "f16"):
+            tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+            return torch.from_numpy(inp[name + "_" + wl.dtype].view(np.int16).copy()).view(tdt)
         return torch.from_numpy(np.ascontiguousarray(inp[name]))
 
     host = {k: t(k).pin_memory() for k in ("value", "sampling_locations", "attention_weights",
@@ -268,7 +269,7 @@ def run_native(args, wl):
     gv = torch.empty_like(d["value"])
     gl = torch.empty_like(d["sampling_locations"])
     gw = torch.empty_like(d["attention_weights"])
-    code = B.MSDA_BF16 if wl.dtype == "bf16" else B.MSDA_F32
+    code = {"f32": B.MSDA_F32, "bf16": B.MSDA_BF16, "f16": B.MSDA_F16}[wl.dtype]
     ws_bytes = B.msda_backward_workspace_bytes(wl.bs, wl.num_keys, wl.num_heads, wl.head_dim, code)
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -277,7 +278,7 @@ def run_native(args, wl):
     args_fwd = (d["value"], shapes, lsi, d["sampling_locations"], d["attention_weights"])
 
     # kernels per step (ours): forward 1; backward: zero-fill 1 + main 1 (+ finalize 1 for bf16)
-    launches_per_step = 3 + (1 if wl.dtype == "bf16" else 0)
+    launches_per_step = 3 + (1 if wl.dtype != "f32" else 0)
 
     def step(evs=None):
         if evs:

@@ -22,8 +22,8 @@
  * ---------------------------------------
  *  Layouts  All tensors are dense, C-contiguous, innermost index last:
  *             value               [bs, num_keys, num_heads, head_dim]      (dtype)
- *             spatial_shapes      [num_levels, 2] int64, rows (H, W)
- *             level_start_index   [num_levels]    int64
+ *             spatial_shapes      [num_levels, 2] int64 (or int32), rows (H, W)
+ *             level_start_index   [num_levels]    int64 (or int32)
  *             sampling_loc        [bs, num_queries, num_heads, num_levels, num_points, 2] (dtype), (x, y)
  *             attn_weight         [bs, num_queries, num_heads, num_levels, num_points]    (dtype)
  *             output, grad_output [bs, num_queries, num_heads * head_dim]  (dtype)
@@ -35,11 +35,11 @@
  *  Streams  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *           default stream).  Every call only enqueues work on it and returns
  *           without synchronising, except the two calls marked BLOCKING.
- *  Numerics fp32 and bf16 inputs both accumulate in fp32.  Pixel coordinates
- *           are one fp32 fused multiply-add, loc*W - 0.5 rounded once.  A
- *           sample contributes only when -1 < x_im < W and -1 < y_im < H;
- *           pixels outside the map count as zero.  bf16 results are rounded
- *           to nearest even.
+ *  Numerics fp32, bf16 and fp16 inputs all accumulate in fp32.  Pixel
+ *           coordinates are one fp32 fused multiply-add, loc*W - 0.5 rounded
+ *           once.  A sample contributes only when -1 < x_im < W and
+ *           -1 < y_im < H; pixels outside the map count as zero.  bf16 and
+ *           fp16 results are rounded to nearest even.
  *  Errors   Arguments are validated on the host before anything is enqueued;
  *           a failed check returns a non-zero msda_status and enqueues
  *           nothing.  MSDA_ERR_CUDA reports a launch error from the CUDA
@@ -72,10 +72,15 @@ extern "C" {
 #define MSDA_API
 #endif
 
-/* Element type of value, sampling_loc, attn_weight, output and all gradients.
- * The Ascend page ("参数说明") lists float32 and float16; bf16 with fp32
- * accumulation is this library's half-width type. */
-typedef enum { MSDA_F32 = 0, MSDA_BF16 = 1 } msda_dtype;
+/* Element type of value, sampling_loc, attn_weight, output and all gradients
+ * (the low byte of the `dtype` argument).  The Ascend page ("参数说明") lists
+ * float32 and float16; bf16 is the other half-width type.  All of them
+ * accumulate in fp32. */
+typedef enum { MSDA_F32 = 0, MSDA_BF16 = 1, MSDA_F16 = 2 } msda_dtype;
+
+/* OR-ed into `dtype`: spatial_shapes and level_start_index are int32 arrays
+ * instead of int64 (the Ascend page lists both index types). */
+#define MSDA_INDEX_INT32 0x100
 
 typedef enum {
     MSDA_OK = 0,
@@ -83,7 +88,7 @@ typedef enum {
     MSDA_ERR_DIM = 2,           /* a dimension is negative, or a size overflows the index range */
     MSDA_ERR_UNSUPPORTED = 3,   /* head_dim % 8 != 0 or > MSDA_MAX_HEAD_DIM, num_levels >
                                    MSDA_MAX_LEVELS, num_levels*num_points > MSDA_MAX_LEVEL_POINTS,
-                                   unknown dtype or flag */
+                                   unknown dtype, index type or flag */
     MSDA_ERR_ALIGN = 4,         /* a tensor pointer is not 16-byte aligned */
     MSDA_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than msda_backward_workspace_bytes() */
     MSDA_ERR_CUDA = 6,          /* the CUDA runtime reported an error */
@@ -107,16 +112,16 @@ typedef enum {
  * with the interface of mx_driving.multi_scale_deformable_attn (Ascend page,
  * "接口原型").  output is fully overwritten.  One kernel launch.
  */
-MSDA_API int msda_forward(const void* value, const int64_t* spatial_shapes,
-                 const int64_t* level_start_index, const void* sampling_loc,
+MSDA_API int msda_forward(const void* value, const void* spatial_shapes,
+                 const void* level_start_index, const void* sampling_loc,
                  const void* attn_weight, void* output, int bs, int num_keys, int num_heads,
                  int head_dim, int num_levels, int num_points, int num_queries, int dtype,
                  void* stream);
 
 /*
  * Bytes of device workspace msda_backward needs: 0 for MSDA_F32; for
- * MSDA_BF16 an fp32 accumulator of bs*num_keys*num_heads*head_dim floats.
- * Returns 0 for invalid arguments as well.
+ * MSDA_BF16 and MSDA_F16 an fp32 accumulator of bs*num_keys*num_heads*head_dim
+ * floats.  Returns 0 for invalid arguments as well.
  */
 MSDA_API size_t msda_backward_workspace_bytes(int bs, int num_keys, int num_heads, int head_dim,
                                      int dtype);
@@ -134,10 +139,10 @@ MSDA_API size_t msda_backward_workspace_bytes(int bs, int num_keys, int num_head
  * gradient at an integer pixel coordinate is the one of the cell to its
  * right.  grad_value is summed with fp32 atomics: its last bits may differ
  * between runs.  Launches: zero-fill (unless accumulating), the gather /
- * scatter kernel, and for bf16 one fp32->bf16 finalize kernel.
+ * scatter kernel, and for bf16 / fp16 one fp32 -> half finalize kernel.
  */
-MSDA_API int msda_backward(const void* value, const int64_t* spatial_shapes,
-                  const int64_t* level_start_index, const void* sampling_loc,
+MSDA_API int msda_backward(const void* value, const void* spatial_shapes,
+                  const void* level_start_index, const void* sampling_loc,
                   const void* attn_weight, const void* grad_output, void* grad_value,
                   void* grad_sampling_loc, void* grad_attn_weight, void* workspace,
                   size_t workspace_bytes, int bs, int num_keys, int num_heads, int head_dim,
@@ -153,7 +158,7 @@ MSDA_API int msda_backward(const void* value, const int64_t* spatial_shapes,
 MSDA_API int msda_zero_fill(void* ptr, size_t bytes, void* stream);
 
 /*
- * BLOCKING.  Checks on the device that level_start_index is the exclusive
+ * BLOCKING.  For int64 index arrays: checks on the device that level_start_index is the exclusive
  * prefix sum of H*W (Ascend page call example; walk-through "2.3.1") and
  * that the levels add up to num_keys (the assertion at the top of
  * MSDeformAttn.forward).  Returns MSDA_OK or MSDA_ERR_SHAPES.  Synchronises
@@ -184,7 +189,8 @@ MSDA_API const char* msda_status_string(int status);
  * every GPU that loads the library holds until the process exits.
  *   - Returns MSDA_ERR_WORKSPACE when bs*num_keys*num_heads*head_dim*4 exceeds
  *     MSDA_NOALLOC_MAX_WORKSPACE_BYTES, and MSDA_ERR_UNSUPPORTED for any dtype
- *     but MSDA_BF16 (the fp32 backward needs no workspace: use msda_backward).
+ *     but MSDA_BF16 (optionally with MSDA_INDEX_INT32; the fp32 backward needs
+ *     no workspace: use msda_backward).
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture.
@@ -194,8 +200,8 @@ MSDA_API const char* msda_status_string(int status);
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
 #define MSDA_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)64 << 20)
-MSDA_API int msda_backward_noalloc(const void* value, const int64_t* spatial_shapes,
-                                   const int64_t* level_start_index, const void* sampling_loc,
+MSDA_API int msda_backward_noalloc(const void* value, const void* spatial_shapes,
+                                   const void* level_start_index, const void* sampling_loc,
                                    const void* attn_weight, const void* grad_output,
                                    void* grad_value, void* grad_sampling_loc,
                                    void* grad_attn_weight, int bs, int num_keys, int num_heads,

@@ -16,7 +16,8 @@ from typing import Optional, Sequence, Tuple
 import torch
 
 __all__ = [
-    "MSDA_F32", "MSDA_BF16", "MSDA_GRAD_VALUE_ACCUMULATE", "MsdaError", "LIB_PATH",
+    "MSDA_F32", "MSDA_BF16", "MSDA_F16", "MSDA_INDEX_INT32", "MSDA_GRAD_VALUE_ACCUMULATE",
+    "MsdaError", "LIB_PATH",
     "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
     "msda_backward_noalloc", "MSDeformAttnFunction", "ms_deform_attn", "EXPORTED_SYMBOLS", "load_library",
@@ -24,6 +25,8 @@ __all__ = [
 
 MSDA_F32 = 0
 MSDA_BF16 = 1
+MSDA_F16 = 2
+MSDA_INDEX_INT32 = 0x100
 MSDA_GRAD_VALUE_ACCUMULATE = 1
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsda.so")
@@ -87,12 +90,20 @@ def _check(fn: str, status: int) -> None:
         raise MsdaError(fn, status)
 
 
-def _dtype_code(t: torch.Tensor) -> int:
+def _dtype_code(t: torch.Tensor, index: Optional[torch.Tensor] = None) -> int:
+    """ABI dtype code of value tensor t, with MSDA_INDEX_INT32 when the index
+    tensors are int32."""
     if t.dtype == torch.float32:
-        return MSDA_F32
-    if t.dtype == torch.bfloat16:
-        return MSDA_BF16
-    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+        code = MSDA_F32
+    elif t.dtype == torch.bfloat16:
+        code = MSDA_BF16
+    elif t.dtype == torch.float16:
+        code = MSDA_F16
+    else:
+        raise TypeError(f"unsupported dtype {t.dtype} (float32, bfloat16 or float16)")
+    if index is not None and index.dtype == torch.int32:
+        code |= MSDA_INDEX_INT32
+    return code
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -122,9 +133,11 @@ def _dims(value: torch.Tensor, spatial_shapes: torch.Tensor, sampling_loc: torch
     return int(bs), int(K), int(M), int(D), int(L), int(P), int(Q)
 
 
-def _index(t: torch.Tensor) -> torch.Tensor:
-    if t.dtype != torch.int64:
-        raise TypeError("spatial_shapes and level_start_index must be int64")
+def _index(t: torch.Tensor, like: Optional[torch.Tensor] = None) -> torch.Tensor:
+    if t.dtype not in (torch.int64, torch.int32):
+        raise TypeError("spatial_shapes and level_start_index must be int64 or int32")
+    if like is not None and t.dtype != like.dtype:
+        raise TypeError("spatial_shapes and level_start_index must have the same dtype")
     return t
 
 
@@ -134,11 +147,11 @@ def msda_forward(value: torch.Tensor, spatial_shapes: torch.Tensor,
                  stream=None) -> torch.Tensor:
     """output [bs, Q, M*D] = MSDeformAttn forward (see include/msda.h)."""
     bs, K, M, D, L, P, Q = _dims(value, spatial_shapes, sampling_loc)
-    code = _dtype_code(value)
+    code = _dtype_code(value, spatial_shapes)
     if output is None:
         output = torch.empty((bs, Q, M * D), dtype=value.dtype, device=value.device)
     _check("msda_forward", _LIB.msda_forward(
-        _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index)),
+        _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index, spatial_shapes)),
         _ptr(sampling_loc), _ptr(attn_weight), _ptr(output), bs, K, M, D, L, P, Q, code,
         _stream(stream)))
     return output
@@ -155,7 +168,7 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_loc, attn_w
                   stream=None):
     """(grad_value, grad_sampling_loc, grad_attn_weight) of MSDeformAttn (see include/msda.h)."""
     bs, K, M, D, L, P, Q = _dims(value, spatial_shapes, sampling_loc)
-    code = _dtype_code(value)
+    code = _dtype_code(value, spatial_shapes)
     dev, dt = value.device, value.dtype
     if grad_value is None:
         grad_value = torch.empty_like(value)
@@ -168,7 +181,7 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_loc, attn_w
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("msda_backward", _LIB.msda_backward(
-        _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index)),
+        _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index, spatial_shapes)),
         _ptr(sampling_loc), _ptr(attn_weight), _ptr(grad_output), _ptr(grad_value),
         _ptr(grad_sampling_loc), _ptr(grad_attn_weight),
         _ptr(workspace) if workspace is not None else None, ws_bytes,
@@ -185,10 +198,11 @@ def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_loc
     include/msda.h); the library allocates nothing."""
     bs, K, M, D, L, P, Q = _dims(value, spatial_shapes, sampling_loc)
     _check("msda_backward_noalloc", _LIB.msda_backward_noalloc(
-        _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index)),
+        _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index, spatial_shapes)),
         _ptr(sampling_loc), _ptr(attn_weight), _ptr(grad_output), _ptr(grad_value),
         _ptr(grad_sampling_loc), _ptr(grad_attn_weight), bs, K, M, D, L, P, Q,
-        _dtype_code(value), MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0, _stream(stream)))
+        _dtype_code(value, spatial_shapes), MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0,
+        _stream(stream)))
     return grad_value, grad_sampling_loc, grad_attn_weight
 
 
@@ -200,7 +214,9 @@ def msda_zero_fill(t: torch.Tensor, stream=None) -> torch.Tensor:
 
 def msda_check_shapes(spatial_shapes: torch.Tensor, level_start_index: torch.Tensor,
                       num_keys: int, stream=None) -> int:
-    """BLOCKING. 0 (MSDA_OK) or 7 (MSDA_ERR_SHAPES); raises on other errors."""
+    """BLOCKING. 0 (MSDA_OK) or 7 (MSDA_ERR_SHAPES); raises on other errors (int64 indices)."""
+    if spatial_shapes.dtype != torch.int64 or level_start_index.dtype != torch.int64:
+        raise TypeError("msda_check_shapes takes int64 index tensors")
     st = _LIB.msda_check_shapes(_ptr(_index(spatial_shapes)), _ptr(_index(level_start_index)),
                                 int(spatial_shapes.shape[0]), int(num_keys), _stream(stream))
     if st not in (0, 7):

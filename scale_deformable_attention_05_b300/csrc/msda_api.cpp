@@ -14,7 +14,15 @@ constexpr int64_t kIntMax = 2147483647;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int elem_bytes(int dtype) { return dtype == MSDA_BF16 ? 2 : 4; }
+// The element type is the low byte of `dtype`; MSDA_INDEX_INT32 may be OR-ed in.
+int value_type(int dtype) { return dtype & 0xff; }
+int index32(int dtype) { return (dtype & MSDA_INDEX_INT32) ? 1 : 0; }
+bool known_dtype(int dtype) {
+    const int v = value_type(dtype);
+    return (dtype & ~(0xff | MSDA_INDEX_INT32)) == 0 &&
+           (v == MSDA_F32 || v == MSDA_BF16 || v == MSDA_F16);
+}
+int elem_bytes(int dtype) { return value_type(dtype) == MSDA_F32 ? 4 : 2; }
 
 struct Dims {
     int64_t bs, K, M, D, L, P, Q;
@@ -26,7 +34,7 @@ struct Dims {
 
 // Shared checks of forward and backward (everything but the pointers).
 int check_dims(const Dims& d, int dtype) {
-    if (dtype != MSDA_F32 && dtype != MSDA_BF16) return MSDA_ERR_UNSUPPORTED;
+    if (!known_dtype(dtype)) return MSDA_ERR_UNSUPPORTED;
     if (d.bs < 0 || d.K < 0 || d.M < 0 || d.D < 0 || d.L < 0 || d.P < 0 || d.Q < 0)
         return MSDA_ERR_DIM;
     if (d.L > MSDA_MAX_LEVELS || d.L * d.P > MSDA_MAX_LEVEL_POINTS) return MSDA_ERR_UNSUPPORTED;
@@ -70,8 +78,8 @@ const char* msda_status_string(int status) {
         case MSDA_ERR_NULL: return "a required pointer is NULL";
         case MSDA_ERR_DIM: return "invalid dimension (negative, or index range exceeded)";
         case MSDA_ERR_UNSUPPORTED:
-            return "unsupported configuration (dtype, flags, head_dim % 8, head_dim > 512, "
-                   "num_levels > 16 or num_levels*num_points > 256)";
+            return "unsupported configuration (dtype, index type, flags, head_dim % 8, "
+                   "head_dim > 512, num_levels > 16 or num_levels*num_points > 256)";
         case MSDA_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
         case MSDA_ERR_WORKSPACE: return "workspace missing or too small";
         case MSDA_ERR_CUDA: return "CUDA runtime error";
@@ -83,8 +91,8 @@ const char* msda_status_string(int status) {
     }
 }
 
-int msda_forward(const void* value, const int64_t* spatial_shapes,
-                 const int64_t* level_start_index, const void* sampling_loc,
+int msda_forward(const void* value, const void* spatial_shapes,
+                 const void* level_start_index, const void* sampling_loc,
                  const void* attn_weight, void* output, int bs, int num_keys, int num_heads,
                  int head_dim, int num_levels, int num_points, int num_queries, int dtype,
                  void* stream) {
@@ -104,19 +112,19 @@ int msda_forward(const void* value, const int64_t* spatial_shapes,
         return cuda_status(msda::launch_zero_fill(output, d.out_elems() * elem_bytes(dtype), st));
     const msda::Problem pb{value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
                            bs, num_keys, num_heads, head_dim, num_levels, num_points,
-                           num_queries};
-    return cuda_status(msda::launch_forward(pb, output, dtype, st));
+                           num_queries, index32(dtype)};
+    return cuda_status(msda::launch_forward(pb, output, value_type(dtype), st));
 }
 
 size_t msda_backward_workspace_bytes(int bs, int num_keys, int num_heads, int head_dim,
                                      int dtype) {
-    if (dtype != MSDA_BF16) return 0;
+    if (!known_dtype(dtype) || value_type(dtype) == MSDA_F32) return 0;
     if (bs < 0 || num_keys < 0 || num_heads < 0 || head_dim < 0) return 0;
     return (size_t)bs * (size_t)num_keys * (size_t)num_heads * (size_t)head_dim * sizeof(float);
 }
 
-int msda_backward(const void* value, const int64_t* spatial_shapes,
-                  const int64_t* level_start_index, const void* sampling_loc,
+int msda_backward(const void* value, const void* spatial_shapes,
+                  const void* level_start_index, const void* sampling_loc,
                   const void* attn_weight, const void* grad_output, void* grad_value,
                   void* grad_sampling_loc, void* grad_attn_weight, void* workspace,
                   size_t workspace_bytes, int bs, int num_keys, int num_heads, int head_dim,
@@ -154,9 +162,10 @@ int msda_backward(const void* value, const int64_t* spatial_shapes,
     }
     const msda::Problem pb{value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
                            bs, num_keys, num_heads, head_dim, num_levels, num_points,
-                           num_queries};
+                           num_queries, index32(dtype)};
+    const int vt = value_type(dtype);
     float* gv32;
-    if (dtype == MSDA_F32) {
+    if (vt == MSDA_F32) {
         gv32 = static_cast<float*>(grad_value);
         if (!accumulate) MSDA_TRY(cuda_status(msda::launch_zero_fill(gv32, value_bytes, st)));
     } else {
@@ -164,10 +173,10 @@ int msda_backward(const void* value, const int64_t* spatial_shapes,
         MSDA_TRY(cuda_status(msda::launch_zero_fill(gv32, ws_need, st)));
     }
     MSDA_TRY(cuda_status(msda::launch_backward(pb, grad_output, gv32, grad_sampling_loc,
-                                               grad_attn_weight, dtype, st)));
-    if (dtype == MSDA_BF16)
-        return cuda_status(msda::launch_finalize_bf16(gv32, grad_value, (size_t)d.value_elems(),
-                                                      accumulate, st));
+                                               grad_attn_weight, vt, st)));
+    if (vt != MSDA_F32)
+        return cuda_status(msda::launch_finalize_half(gv32, grad_value, (size_t)d.value_elems(),
+                                                      accumulate, vt, st));
     return MSDA_OK;
 }
 

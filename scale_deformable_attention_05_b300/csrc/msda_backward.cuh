@@ -136,8 +136,8 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                                   MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS > 0
                                       ? MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS
                                       : 1)
-    backward_kernel(const T* __restrict__ value, const int64_t* __restrict__ spatial_shapes,
-                    const int64_t* __restrict__ level_start_index, const T* __restrict__ loc,
+    backward_kernel(const T* __restrict__ value, const void* __restrict__ spatial_shapes,
+                    const void* __restrict__ level_start_index, int idx32, const T* __restrict__ loc,
                     const T* __restrict__ attn, const T* __restrict__ grad_out,
                     float* __restrict__ grad_value_f32, T* __restrict__ grad_loc,
                     T* __restrict__ grad_attn, int num_keys, int num_heads, int head_dim,
@@ -159,8 +159,8 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     __shared__ float4 s_aw[MSDA_BWD_WARPS][Geom::kRecords];
     __shared__ float4 s_aux[MSDA_BWD_WARPS][Geom::kRecords];
 
-    load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, num_levels,
-                     num_points, num_keys);
+    load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, idx32,
+                     num_levels, num_points, num_keys);
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -344,8 +344,8 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                                   MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS > 0
                                       ? MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS
                                       : 1)
-    backward_merge_kernel(const T* __restrict__ value, const int64_t* __restrict__ spatial_shapes,
-                          const int64_t* __restrict__ level_start_index,
+    backward_merge_kernel(const T* __restrict__ value, const void* __restrict__ spatial_shapes,
+                          const void* __restrict__ level_start_index, int idx32,
                           const T* __restrict__ loc, const T* __restrict__ attn,
                           const T* __restrict__ grad_out, float* __restrict__ grad_value_f32,
                           T* __restrict__ grad_loc, T* __restrict__ grad_attn, int num_keys,
@@ -369,8 +369,8 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     __shared__ int s_ukey[MSDA_BWD_WARPS][kMaxUnique];
     __shared__ float4 s_uA[MSDA_BWD_WARPS][kMaxUnique];
 
-    load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, num_levels,
-                     num_points, num_keys);
+    load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, idx32,
+                     num_levels, num_points, num_keys);
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

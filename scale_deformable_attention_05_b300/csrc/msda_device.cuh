@@ -23,6 +23,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -121,6 +122,53 @@ struct IO<__nv_bfloat16> {
     }
 };
 
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t u) {
+    __half2 h;
+    *reinterpret_cast<uint32_t*>(&h) = u;
+    return __half22float2(h);
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <>
+struct IO<__half> {
+    using T = __half;
+    static constexpr int kVec = 8;
+    __device__ __forceinline__ static void unpack(const uint4 t, float (&v)[kVec]) {
+        const float2 a = half2_bits_to_float2(t.x), b = half2_bits_to_float2(t.y);
+        const float2 c = half2_bits_to_float2(t.z), d = half2_bits_to_float2(t.w);
+        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+        v[4] = c.x; v[5] = c.y; v[6] = d.x; v[7] = d.y;
+    }
+    __device__ __forceinline__ static void load_vec(const void* p, float (&v)[kVec]) {
+        unpack(__ldg(reinterpret_cast<const uint4*>(p)), v);
+    }
+    __device__ __forceinline__ static void load_vec_stream(const T* p, float (&v)[kVec]) {
+        unpack(__ldcs(reinterpret_cast<const uint4*>(p)), v);
+    }
+    __device__ __forceinline__ static float2 load_xy(const T* p) {
+        return half2_bits_to_float2(__ldcs(reinterpret_cast<const unsigned int*>(p)));
+    }
+    __device__ __forceinline__ static float load_one(const T* p) {
+        const unsigned short u = __ldcs(reinterpret_cast<const unsigned short*>(p));
+        return __half2float(__ushort_as_half(u));
+    }
+    __device__ __forceinline__ static void store_vec(T* p, const float (&v)[kVec]) {
+        uint4 t;
+        t.x = pack_half2(v[0], v[1]); t.y = pack_half2(v[2], v[3]);
+        t.z = pack_half2(v[4], v[5]); t.w = pack_half2(v[6], v[7]);
+        __stcs(reinterpret_cast<uint4*>(p), t);
+    }
+    __device__ __forceinline__ static void store_one(T* p, float v) {
+        __stcs(reinterpret_cast<unsigned short*>(p), __half_as_ushort(__float2half_rn(v)));
+    }
+    __device__ __forceinline__ static void store_xy(T* p, float x, float y) {
+        __stcs(reinterpret_cast<unsigned int*>(p), pack_half2(x, y));
+    }
+};
+
 // 32-byte vectors (one 256-bit load per lane, sm_100+).  Value rows are read
 // through the non-coherent path and kept in L1.
 template <typename T>
@@ -183,6 +231,34 @@ struct IO32<__nv_bfloat16> {
     }
 };
 
+template <>
+struct IO32<__half> {
+    using T = __half;
+    static constexpr int kVec = 16;
+    __device__ __forceinline__ static void load(const void* p, float (&v)[kVec]) {
+        uint32_t u[8];
+        asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
+                       "=r"(u[6]), "=r"(u[7])
+                     : "l"(p));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float2 f = half2_bits_to_float2(u[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    __device__ __forceinline__ static void store(T* p, const float (&v)[kVec]) {
+        uint4 a, b;
+        a.x = pack_half2(v[0], v[1]); a.y = pack_half2(v[2], v[3]);
+        a.z = pack_half2(v[4], v[5]); a.w = pack_half2(v[6], v[7]);
+        b.x = pack_half2(v[8], v[9]); b.y = pack_half2(v[10], v[11]);
+        b.z = pack_half2(v[12], v[13]); b.w = pack_half2(v[14], v[15]);
+        __stcs(reinterpret_cast<uint4*>(p), a);
+        __stcs(reinterpret_cast<uint4*>(p) + 1, b);
+    }
+};
+
 // Row vectors of kBytes (16 or 32) bytes: the loads of value rows and the
 // stores of output rows in the forward kernel.
 template <typename T, int kBytes>
@@ -218,14 +294,21 @@ struct LevelInfo {
     int H, W, start, ok;
 };
 
+// spatial_shapes / level_start_index hold int64, or int32 when idx32.
+__device__ __forceinline__ int64_t index_at(const void* p, int i, int idx32) {
+    return idx32 ? (int64_t) static_cast<const int32_t*>(p)[i] : static_cast<const int64_t*>(p)[i];
+}
+
 __device__ __forceinline__ void load_level_table(LevelInfo* s_levels, unsigned char* s_level_of,
-                                                 const int64_t* __restrict__ spatial_shapes,
-                                                 const int64_t* __restrict__ level_start_index,
-                                                 int num_levels, int num_points, int num_keys) {
+                                                 const void* __restrict__ spatial_shapes,
+                                                 const void* __restrict__ level_start_index,
+                                                 int idx32, int num_levels, int num_points,
+                                                 int num_keys) {
     if (threadIdx.x < num_levels) {
         const int l = threadIdx.x;
-        const int64_t H = spatial_shapes[2 * l], W = spatial_shapes[2 * l + 1];
-        const int64_t s = level_start_index[l];
+        const int64_t H = index_at(spatial_shapes, 2 * l, idx32);
+        const int64_t W = index_at(spatial_shapes, 2 * l + 1, idx32);
+        const int64_t s = index_at(level_start_index, l, idx32);
         const bool ok = H >= 0 && W >= 0 && H < (1 << 24) && W < (1 << 24) && s >= 0 &&
                         s + H * W <= (int64_t)num_keys;
         LevelInfo li;

@@ -83,8 +83,8 @@ constexpr int forward_min_blocks(int channels_per_lane) {
 template <typename T, int kLanes, int kVPL, int kVB>
 __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
                                   forward_min_blocks(kVPL * kVB / (int)sizeof(T)))
-    forward_kernel(const T* __restrict__ value, const int64_t* __restrict__ spatial_shapes,
-                   const int64_t* __restrict__ level_start_index, const T* __restrict__ loc,
+    forward_kernel(const T* __restrict__ value, const void* __restrict__ spatial_shapes,
+                   const void* __restrict__ level_start_index, int idx32, const T* __restrict__ loc,
                    const T* __restrict__ attn, T* __restrict__ out, int num_keys, int num_heads,
                    int head_dim, int num_levels, int num_points, int num_queries,
                    int num_qtiles, int num_tiles, int tiles_per_cta) {
@@ -98,8 +98,8 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
     __shared__ int4 s_key[kWarps][Geom::kRecords];
     __shared__ float4 s_w[kWarps][Geom::kRecords];
 
-    load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, num_levels,
-                     num_points, num_keys);
+    load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, idx32,
+                     num_levels, num_points, num_keys);
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

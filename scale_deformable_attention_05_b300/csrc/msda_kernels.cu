@@ -24,25 +24,23 @@ __global__ void zero_fill_kernel(uint4* __restrict__ p, size_t n16, int tail_byt
         reinterpret_cast<unsigned char*>(p + n16)[threadIdx.x] = 0;
 }
 
-// bf16 grad_value from the fp32 workspace: overwrite, or add when accumulating.
-// n8 = number of 8-element groups (head_dim % 8 == 0 makes the total a multiple of 8).
-__global__ void finalize_bf16_kernel(const float4* __restrict__ ws, uint4* __restrict__ gv,
+// Half-precision grad_value from the fp32 workspace: overwrite, or add when
+// accumulating.  n8 = number of 8-element groups (head_dim % 8 == 0 makes the
+// total a multiple of 8).
+template <typename T>
+__global__ void finalize_half_kernel(const float4* __restrict__ ws, T* __restrict__ gv,
                                      size_t n8, int accumulate) {
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
          i += (size_t)gridDim.x * blockDim.x) {
         const float4 a = __ldcs(ws + 2 * i), b = __ldcs(ws + 2 * i + 1);
         float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         if (accumulate) {
-            const uint4 old = gv[i];
-            v[0] += bf16_lo(old.x); v[1] += bf16_hi(old.x);
-            v[2] += bf16_lo(old.y); v[3] += bf16_hi(old.y);
-            v[4] += bf16_lo(old.z); v[5] += bf16_hi(old.z);
-            v[6] += bf16_lo(old.w); v[7] += bf16_hi(old.w);
+            float old[8];
+            IO<T>::load_vec_stream(gv + 8 * i, old);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] += old[e];
         }
-        uint4 o;
-        o.x = pack_bf16x2(v[0], v[1]); o.y = pack_bf16x2(v[2], v[3]);
-        o.z = pack_bf16x2(v[4], v[5]); o.w = pack_bf16x2(v[6], v[7]);
-        __stcs(gv + i, o);
+        IO<T>::store_vec(gv + 8 * i, v);
     }
 }
 
@@ -146,7 +144,7 @@ cudaError_t launch_forward_t(const Problem& pb, void* out, cudaStream_t st) {
     const TileGrid tg =
         tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_FWD_WARPS);
     kernel<<<tg.grid, kThreads, 0, st>>>(
-        static_cast<const T*>(pb.value), pb.shapes, pb.lsi, static_cast<const T*>(pb.loc),
+        static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<T*>(out), pb.K, pb.M, pb.D, pb.L, pb.P, pb.Q,
         tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta);
     return cudaGetLastError();
@@ -160,7 +158,7 @@ cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv
     const TileGrid tg =
         tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS);
     kernel<<<tg.grid, kThreads, 0, st>>>(
-        static_cast<const T*>(pb.value), pb.shapes, pb.lsi, static_cast<const T*>(pb.loc),
+        static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
         static_cast<T*>(grad_loc), static_cast<T*>(grad_attn), pb.K, pb.M, pb.D, pb.L, pb.P,
         pb.Q, tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta);
@@ -217,7 +215,7 @@ cudaError_t launch_backward_merge_t(const Problem& pb, int log2_points, const vo
     const TileGrid tg =
         tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS);
     kernel<<<tg.grid, kThreads, 0, st>>>(
-        static_cast<const T*>(pb.value), pb.shapes, pb.lsi, static_cast<const T*>(pb.loc),
+        static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
         static_cast<T*>(grad_loc), static_cast<T*>(grad_attn), pb.K, pb.M, pb.D, pb.L, pb.P,
         log2_points, pb.Q, tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta);
@@ -263,13 +261,15 @@ int grid_for(size_t n, int threads) {
 }  // namespace
 
 cudaError_t launch_forward(const Problem& pb, void* out, int dtype, cudaStream_t st) {
-    if (dtype == 0) return dispatch_forward<float>(pb, out, st);
+    if (dtype == kF32) return dispatch_forward<float>(pb, out, st);
+    if (dtype == kF16) return dispatch_forward<__half>(pb, out, st);
     return dispatch_forward<__nv_bfloat16>(pb, out, st);
 }
 
 cudaError_t launch_backward(const Problem& pb, const void* grad_out, float* gv32, void* grad_loc,
                             void* grad_attn, int dtype, cudaStream_t st) {
-    if (dtype == 0) return dispatch_backward<float>(pb, grad_out, gv32, grad_loc, grad_attn, st);
+    if (dtype == kF32) return dispatch_backward<float>(pb, grad_out, gv32, grad_loc, grad_attn, st);
+    if (dtype == kF16) return dispatch_backward<__half>(pb, grad_out, gv32, grad_loc, grad_attn, st);
     return dispatch_backward<__nv_bfloat16>(pb, grad_out, gv32, grad_loc, grad_attn, st);
 }
 
@@ -281,13 +281,18 @@ cudaError_t launch_zero_fill(void* p, size_t bytes, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_finalize_bf16(const float* ws, void* grad_value, size_t elems, bool accumulate,
-                                 cudaStream_t st) {
+cudaError_t launch_finalize_half(const float* ws, void* grad_value, size_t elems, bool accumulate,
+                                 int dtype, cudaStream_t st) {
     const size_t n8 = elems / 8;
     if (n8 == 0) return cudaSuccess;
-    finalize_bf16_kernel<<<grid_for(n8, 256), 256, 0, st>>>(
-        reinterpret_cast<const float4*>(ws), static_cast<uint4*>(grad_value), n8,
-        accumulate ? 1 : 0);
+    if (dtype == kF16)
+        finalize_half_kernel<__half><<<grid_for(n8, 256), 256, 0, st>>>(
+            reinterpret_cast<const float4*>(ws), static_cast<__half*>(grad_value), n8,
+            accumulate ? 1 : 0);
+    else
+        finalize_half_kernel<__nv_bfloat16><<<grid_for(n8, 256), 256, 0, st>>>(
+            reinterpret_cast<const float4*>(ws), static_cast<__nv_bfloat16*>(grad_value), n8,
+            accumulate ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -60,12 +60,14 @@ int check_tensor(const void* p, int64_t elems) {
 }  // namespace
 
 extern "C" MSDA_API int msda_backward_noalloc(
-    const void* value, const int64_t* spatial_shapes, const int64_t* level_start_index,
+    const void* value, const void* spatial_shapes, const void* level_start_index,
     const void* sampling_loc, const void* attn_weight, const void* grad_output, void* grad_value,
     void* grad_sampling_loc, void* grad_attn_weight, int bs, int num_keys, int num_heads,
     int head_dim, int num_levels, int num_points, int num_queries, int dtype, unsigned flags,
     void* stream) {
-    if (dtype != MSDA_BF16) return MSDA_ERR_UNSUPPORTED;  // only bf16 needs scratch
+    // only the bf16 backward (optionally with int32 index arrays) runs here
+    if ((dtype & ~MSDA_INDEX_INT32) != MSDA_BF16) return MSDA_ERR_UNSUPPORTED;
+    const int idx32 = (dtype & MSDA_INDEX_INT32) ? 1 : 0;
     if (flags & ~MSDA_GRAD_VALUE_ACCUMULATE) return MSDA_ERR_UNSUPPORTED;
     if (bs < 0 || num_keys < 0 || num_heads < 0 || head_dim < 0 || num_levels < 0 ||
         num_points < 0 || num_queries < 0)
@@ -111,12 +113,12 @@ extern "C" MSDA_API int msda_backward_noalloc(
         return MSDA_ERR_CUDA;
     const msda::Problem pb{value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
                            bs, num_keys, num_heads, head_dim, num_levels, num_points,
-                           num_queries};
+                           num_queries, idx32};
     if (msda::launch_backward(pb, grad_output, scratch, grad_sampling_loc, grad_attn_weight,
-                              MSDA_BF16, st) != cudaSuccess)
+                              msda::kBF16, st) != cudaSuccess)
         return MSDA_ERR_CUDA;
-    return msda::launch_finalize_bf16(scratch, grad_value, (size_t)value_elems, accumulate, st) ==
-                   cudaSuccess
+    return msda::launch_finalize_half(scratch, grad_value, (size_t)value_elems, accumulate,
+                                      msda::kBF16, st) == cudaSuccess
                ? MSDA_OK
                : MSDA_ERR_CUDA;
 }

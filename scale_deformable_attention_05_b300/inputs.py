@@ -38,6 +38,8 @@ __all__ = [
     "grid_reference_points",
     "f32_to_bf16_bits",
     "bf16_bits_to_f32",
+    "f32_to_f16_bits",
+    "f16_bits_to_f32",
     "make_inputs",
     "random_workload",
 ]
@@ -98,7 +100,7 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
-        return 2 if self.dtype == "bf16" else 4
+        return 2 if self.dtype in ("bf16", "f16") else 4
 
     def compulsory_bytes(self, backward: bool) -> int:
         """Bytes every implementation must move to or from HBM at least once.
@@ -177,6 +179,16 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to IEEE half (numpy's cast: round to nearest, ties to even); uint16 bits."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen IEEE half bits to float32 exactly."""
+    return np.ascontiguousarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
 def _softmax_lastdim(x: np.ndarray) -> np.ndarray:
     z = x - x.max(axis=-1, keepdims=True)
     e = np.exp(z)
@@ -194,8 +206,8 @@ def make_inputs(wl: Workload, with_grad: bool = True) -> Dict[str, np.ndarray]:
     Returned keys: ``value``, ``sampling_locations``, ``attention_weights``,
     ``grad_output`` (float32 arrays holding exactly the values the operator
     sees, i.e. bf16-representable for bf16 workloads), ``spatial_shapes``,
-    ``level_start_index`` (int64), and for bf16 workloads the uint16 bit
-    patterns under ``*_bf16`` keys.
+    ``level_start_index`` (int64), and for bf16 / f16 workloads the uint16 bit
+    patterns under ``*_bf16`` / ``*_f16`` keys.
     """
     rng = np.random.default_rng(wl.seed)
     bs, Q, M, D = wl.bs, wl.num_queries, wl.num_heads, wl.head_dim
@@ -270,6 +282,10 @@ def make_inputs(wl: Workload, with_grad: bool = True) -> Dict[str, np.ndarray]:
             bits = f32_to_bf16_bits(a)
             out[k + "_bf16"] = bits
             out[k] = bf16_bits_to_f32(bits).reshape(a.shape)
+        elif wl.dtype == "f16":
+            bits = f32_to_f16_bits(a)
+            out[k + "_f16"] = bits
+            out[k] = f16_bits_to_f32(bits).reshape(a.shape)
         elif wl.dtype == "f32":
             out[k] = np.ascontiguousarray(a)
         else:

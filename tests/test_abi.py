@@ -58,6 +58,12 @@ def test_version_and_status_strings():
 def test_workspace_bytes():
     assert B.msda_backward_workspace_bytes(2, 22223, 8, 32, B.MSDA_F32) == 0
     assert B.msda_backward_workspace_bytes(4, 22223, 8, 32, B.MSDA_BF16) == 4 * 22223 * 8 * 32 * 4
+    assert B.msda_backward_workspace_bytes(1, 100, 2, 8, B.MSDA_F16) == 100 * 2 * 8 * 4
+    assert B.msda_backward_workspace_bytes(
+        1, 100, 2, 8, B.MSDA_F16 | B.MSDA_INDEX_INT32) == 100 * 2 * 8 * 4
+    assert B.msda_backward_workspace_bytes(1, 100, 2, 8, B.MSDA_F32 | B.MSDA_INDEX_INT32) == 0
+    assert B.msda_backward_workspace_bytes(1, 100, 2, 8, 3) == 0          # unknown dtype
+    assert B.msda_backward_workspace_bytes(1, 100, 2, 8, 0x201) == 0      # unknown flag bit
     assert B.msda_backward_workspace_bytes(-1, 10, 8, 32, B.MSDA_BF16) == 0
 
 
@@ -93,7 +99,9 @@ def _bwd(value=A, shapes=A, lsi=A, loc=A, w=A, g=A, gv=A, gl=A, gw=A, ws=None, w
     (dict(D=520), 3),
     (dict(L=17, P=1), 3),
     (dict(L=4, P=65), 3),
-    (dict(dtype=2), 3),
+    (dict(dtype=3), 3),          # unknown element type
+    (dict(dtype=0x200), 3),      # unknown flag bit
+    (dict(dtype=0x103), 3),      # int32 indices with an unknown element type
     (dict(value=A + 8), 4),
     (dict(loc=A + 4), 4),
     (dict(out=A + 2), 4),
@@ -112,6 +120,9 @@ def test_forward_rejects_on_host(kw, status):
     (dict(D=4), 3),
     (dict(gl=A + 8), 4),
     (dict(dtype=1), 5),                       # bf16 needs a workspace
+    (dict(dtype=2), 5),                       # so does fp16
+    (dict(dtype=2 | 0x100), 5),               # with int32 indices too
+    (dict(dtype=3), 3),                       # unknown element type
     (dict(dtype=1, ws=A, ws_bytes=16), 5),    # too small
     (dict(dtype=1, ws=A + 4, ws_bytes=1 << 30), 4),
 ])

@@ -82,6 +82,12 @@ RANDOM_CASES = [
     (14, 1, tuple((3, 2) for _ in range(16)), 2, 8, 16, 6, "f32"),
     (15, 2, ((4, 5), (2, 3)), 3, 8, 128, 3, "f32"),
     (16, 2, ((4, 5), (2, 3)), 1, 8, 128, 40, "bf16"),
+    # fp16 I/O (the Ascend page's half type)
+    (17, 2, ((9, 7), (5, 4)), 2, 32, 4, 33, "f16"),
+    (18, 1, ((31, 17), (16, 9)), 8, 256, 16, 9, "f16"),
+    (19, 2, ((5, 3), (1, 1)), 3, 16, 2, 7, "f16"),
+    (20, 1, ((6, 6),), 2, 512, 3, 5, "f16"),
+    (21, 3, ((9, 7), (5, 4), (3, 2), (2, 1), (1, 1)), 5, 64, 5, 17, "f16"),
 ]
 
 
@@ -92,6 +98,36 @@ def test_random_shape_parity(B, case):
     inp = gen.make_inputs(wl)
     out, grads = _run(B, wl, inp)
     _check(wl, inp, out, grads)
+
+
+def test_encoder_shape_fp16(B):
+    """The encoder pyramid and sampling pattern in fp16 I/O (one image)."""
+    wl = gen.WORKLOADS["encoder"].with_(name="encoder_f16", seed=1006, bs=1, dtype="f16")
+    inp = gen.make_inputs(wl)
+    out, grads = _run(B, wl, inp)
+    _check(wl, inp, out, grads)
+    empty_cache()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_int32_index_tensors_give_the_same_results(B, dtype):
+    """spatial_shapes / level_start_index as int32 (MSDA_INDEX_INT32) select the
+    same pixels: output and the per-sample gradients are bit-identical to the
+    int64 call; grad_value (fp32 atomics) agrees within the gradient tolerance."""
+    wl = gen.random_workload(33, 2, ((9, 7), (5, 4), (3, 3)), 2, 32, 4, 21, dtype=dtype)
+    inp = gen.make_inputs(wl)
+    d = to_device(inp, wl)
+    a64 = (d["value"], d["spatial_shapes"], d["level_start_index"], d["sampling_locations"],
+           d["attention_weights"])
+    a32 = (d["value"], d["spatial_shapes"].int(), d["level_start_index"].int(),
+           d["sampling_locations"], d["attention_weights"])
+    o64, o32 = B.msda_forward(*a64), B.msda_forward(*a32)
+    g64 = B.msda_backward(*a64, d["grad_output"])
+    g32 = B.msda_backward(*a32, d["grad_output"])
+    torch.cuda.synchronize()
+    assert torch.equal(o64, o32)
+    assert torch.equal(g64[1], g32[1]) and torch.equal(g64[2], g32[2])
+    assert_grad_close(host(g32[0]), host(g64[0]), wl.dtype, "grad_value (int32 indices)")
 
 
 def test_key_index_field_is_exact(B):

@@ -410,3 +410,14 @@ def test_bf16_rounding_is_round_to_nearest_even():
     # 1 + 2^-8 is a tie between 1 and 1 + 2^-7 (bf16 has 7 fraction bits): even -> 1.0
     np.testing.assert_array_equal(back, np.array([1.0, 1.0, 1.0 + 2 ** -7, 1.0, -2.5, 3.140625],
                                                  np.float32))
+
+
+def test_f16_rounding_is_round_to_nearest_even():
+    # IEEE half has 10 fraction bits: 1 + 2^-11 is a tie between 1 and 1 + 2^-10 (even -> 1),
+    # 1 + 3*2^-11 a tie between 1 + 2^-10 and 1 + 2^-9 (even -> 1 + 2^-9)
+    x = np.array([1.0, 1.0 + 2 ** -11, 1.0 + 3 * 2 ** -11, 1.0 + 2 ** -12, -2.5, 65504.0],
+                 np.float32)
+    bits = gen.f32_to_f16_bits(x)
+    assert bits[0] == 0x3C00 and bits[5] == 0x7BFF
+    np.testing.assert_array_equal(gen.f16_bits_to_f32(bits),
+                                  np.array([1.0, 1.0, 1.0 + 2 ** -9, 1.0, -2.5, 65504.0], np.float32))

@@ -214,6 +214,9 @@ def _config(wl, args):
             "num_heads": wl.num_heads, "head_dim": wl.head_dim, "num_levels": wl.num_levels,
             "num_points": wl.num_points, "io_dtype": wl.dtype,
             "passes": "forward+backward",
+            "entry_points": ("msda_forward_fused / msda_backward_fused (2-d reference points, "
+                             "offsets, logits)" if getattr(args, "path", "plain") == "fused"
+                             else "msda_forward / msda_backward"),
             "l2": "flushed before every step (write of 2x L2 size, outside the timed events)",
             "parallelism": f"replicas x{args.gpus} (each rank its own batch)"}
 
@@ -251,7 +254,12 @@ def run_native(args, wl):
     from scale_deformable_attention_05_b300 import binding as B
 
     dev = torch.device("cuda", local)
-    inp = gen.make_inputs(rank_workload(wl, rank))
+    fused = args.path == "fused"
+    wl_r = rank_workload(wl, rank)
+    inp = gen.make_fused_inputs(wl_r, 2) if fused else gen.make_inputs(wl_r)
+    names = (("value", "reference_points", "sampling_offsets", "attention_logits",
+              "grad_output") if fused else
+             ("value", "sampling_locations", "attention_weights", "grad_output"))
 
     def t(name):
         if wl.dtype in ("bf16", "f16"):
@@ -259,23 +267,36 @@ def run_native(args, wl):
             return torch.from_numpy(inp[name + "_" + wl.dtype].view(np.int16).copy()).view(tdt)
         return torch.from_numpy(np.ascontiguousarray(inp[name]))
 
-    host = {k: t(k).pin_memory() for k in ("value", "sampling_locations", "attention_weights",
-                                          "grad_output")}
+    host = {k: t(k).pin_memory() for k in names}
     d = {k: v.to(dev) for k, v in host.items()}
     shapes = torch.from_numpy(inp["spatial_shapes"]).to(dev)
     lsi = torch.from_numpy(inp["level_start_index"]).to(dev)
     out = torch.empty((wl.bs, wl.num_queries, wl.num_heads * wl.head_dim), dtype=d["value"].dtype,
                       device=dev)
     gv = torch.empty_like(d["value"])
-    gl = torch.empty_like(d["sampling_locations"])
-    gw = torch.empty_like(d["attention_weights"])
+    gl = torch.empty_like(d[names[2] if fused else "sampling_locations"])
+    gw = torch.empty_like(d[names[3] if fused else "attention_weights"])
     code = {"f32": B.MSDA_F32, "bf16": B.MSDA_BF16, "f16": B.MSDA_F16}[wl.dtype]
     ws_bytes = B.msda_backward_workspace_bytes(wl.bs, wl.num_keys, wl.num_heads, wl.head_dim, code)
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    args_fwd = (d["value"], shapes, lsi, d["sampling_locations"], d["attention_weights"])
+    args_fwd = (d["value"], shapes, lsi) + tuple(d[k] for k in names[1:-1])
+
+    def run_forward():
+        if fused:
+            B.msda_forward_fused(*args_fwd, output=out, stream=stream)
+        else:
+            B.msda_forward(*args_fwd, output=out, stream=stream)
+
+    def run_backward(accumulate):
+        if fused:     # the encoder's reference points are constants: no reference gradient
+            B.msda_backward_fused(*args_fwd, d["grad_output"], gv, gl, gw, reference_grad=False,
+                                  workspace=workspace, accumulate=accumulate, stream=stream)
+        else:
+            B.msda_backward(*args_fwd, d["grad_output"], gv, gl, gw, workspace=workspace,
+                            accumulate=accumulate, stream=stream)
 
     # kernels per step (ours): forward 1; backward: zero-fill 1 + main 1 (+ finalize 1 for bf16)
     launches_per_step = 3 + (1 if wl.dtype != "f32" else 0)
@@ -283,15 +304,14 @@ def run_native(args, wl):
     def step(evs=None):
         if evs:
             evs[0].record(stream)
-        B.msda_forward(*args_fwd, output=out, stream=stream)
+        run_forward()
         if evs:
             evs[1].record(stream)
         if wl.dtype == "f32":
             B.msda_zero_fill(gv, stream=stream)
         if evs:
             evs[2].record(stream)
-        B.msda_backward(*args_fwd, d["grad_output"], gv, gl, gw, workspace=workspace,
-                        accumulate=(wl.dtype == "f32"), stream=stream)
+        run_backward(accumulate=(wl.dtype == "f32"))
         if evs:
             evs[3].record(stream)
 
@@ -340,9 +360,8 @@ def run_native(args, wl):
         def e2e_step():
             for k in host:
                 d[k].copy_(host[k], non_blocking=True)
-            B.msda_forward(*args_fwd, output=out, stream=stream)
-            B.msda_backward(*args_fwd, d["grad_output"], gv, gl, gw, workspace=workspace,
-                            stream=stream)
+            run_forward()
+            run_backward(accumulate=False)
             h_out.copy_(out, non_blocking=True)
             h_gv.copy_(gv, non_blocking=True)
             h_gl.copy_(gl, non_blocking=True)
@@ -361,8 +380,9 @@ def run_native(args, wl):
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, dev)
         e2e = {"value": job_rate(wl.points, ws, e2e_ms), "unit": "points/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "path": "pinned host -> device copies, msda_forward, msda_backward, "
-                       "device -> pinned host copies of output and the three gradients"}
+               "path": "pinned host -> device copies, msda_forward%s, msda_backward%s, "
+                       "device -> pinned host copies of output and the three gradients"
+                       % (("_fused",) * 2 if fused else ("", ""))}
 
     if rank != 0:
         if dist:
@@ -370,8 +390,15 @@ def run_native(args, wl):
         return 0
 
     hbm_gbs, peak_src = _peaks()
-    fb = wl.compulsory_bytes(backward=False)
-    bb = wl.compulsory_bytes(backward=True)
+    if fused:
+        # reference points [bs, Q, L, 2] replace nothing; offsets and logits have the
+        # sizes of locations and weights
+        ref_bytes = wl.bs * wl.num_queries * wl.num_levels * 2 * wl.elem_bytes
+        fb = wl.compulsory_bytes(backward=False) + ref_bytes
+        bb = wl.compulsory_bytes(backward=True) + ref_bytes
+    else:
+        fb = wl.compulsory_bytes(backward=False)
+        bb = wl.compulsory_bytes(backward=True)
     passes = {
         "forward": {"kernel": "forward_kernel", "ms": mean(fwd_ms), "min_ms": min(fwd_ms),
                     "points_per_s": wl.points / (mean(fwd_ms) / 1e3),
@@ -417,6 +444,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="encoder", choices=sorted(gen.WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--path", default="plain", choices=["plain", "fused"],
+                    help="fused: msda_forward_fused / msda_backward_fused from reference "
+                         "points, offsets and logits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()

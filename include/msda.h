@@ -102,6 +102,8 @@ typedef enum {
 #define MSDA_MAX_LEVELS 16
 #define MSDA_MAX_LEVEL_POINTS 256
 #define MSDA_MAX_HEAD_DIM 512
+/* num_levels*num_points limit of the fused entry points (the Ascend envelope). */
+#define MSDA_MAX_FUSED_LEVEL_POINTS 64
 
 /* Flags of msda_backward. */
 #define MSDA_GRAD_VALUE_ACCUMULATE 1u /* add into grad_value instead of overwriting it */
@@ -148,6 +150,52 @@ MSDA_API int msda_backward(const void* value, const void* spatial_shapes,
                   size_t workspace_bytes, int bs, int num_keys, int num_heads, int head_dim,
                   int num_levels, int num_points, int num_queries, int dtype, unsigned flags,
                   void* stream);
+
+/*
+ * Fused preparation + forward: the step before the operator in
+ * MSDeformAttn.forward (walk-through, "2.2.4 源码分析"; 4-d references from
+ * section "2.4") is done inside the kernel.  Instead of locations and weights
+ * it takes
+ *   reference_points  [bs, num_queries, num_levels, ref_dim] (dtype), ref_dim
+ *                     2: (x, y), or 4: (x, y, w, h) boxes
+ *   sampling_offsets  [bs, num_queries, num_heads, num_levels, num_points, 2]
+ *   attn_logits       [bs, num_queries, num_heads, num_levels*num_points]
+ * and computes, per sample, a = softmax of its (b, q, m) row of logits and
+ *   ref_dim 2: loc = ref + off / (W_l, H_l)
+ *   ref_dim 4: loc = ref_xy + off / num_points * ref_wh * 0.5
+ * in binary32, each operation rounded to nearest, with the reciprocals rounded
+ * once: fl(ref + fl(off * fl(1/W))) and fl(ref_xy + fl(fl(off * w) *
+ * fl(1/(2*num_points)))), then the same sum as msda_forward.  num_levels*num_points must not exceed
+ * MSDA_MAX_FUSED_LEVEL_POINTS (else MSDA_ERR_UNSUPPORTED), ref_dim must be 2 or
+ * 4.  Saves the caller's softmax and location kernels and their
+ * [bs, Q, M, L, P, 3] round trip through memory.  One kernel launch.
+ */
+MSDA_API int msda_forward_fused(const void* value, const void* spatial_shapes,
+                                const void* level_start_index, const void* reference_points,
+                                const void* sampling_offsets, const void* attn_logits,
+                                void* output, int bs, int num_keys, int num_heads, int head_dim,
+                                int num_levels, int num_points, int num_queries, int ref_dim,
+                                int dtype, void* stream);
+
+/*
+ * Backward of msda_forward_fused: grad_value (as msda_backward, same
+ * workspace rule and flags), grad_sampling_offsets (shape and dtype of the
+ * offsets), grad_attn_logits (through the softmax: a * (g_a - sum_j a_j g_a_j)
+ * per row), and, when grad_reference_points is not NULL, the gradient of the
+ * reference points summed over heads and points into that fp32
+ * [bs, num_queries, num_levels, ref_dim] buffer (16-byte aligned, overwritten).
+ * Launches: zero-fills, one gather / scatter kernel, and for half types the
+ * finalize kernel.
+ */
+MSDA_API int msda_backward_fused(const void* value, const void* spatial_shapes,
+                                 const void* level_start_index, const void* reference_points,
+                                 const void* sampling_offsets, const void* attn_logits,
+                                 const void* grad_output, void* grad_value,
+                                 void* grad_sampling_offsets, void* grad_attn_logits,
+                                 float* grad_reference_points, void* workspace,
+                                 size_t workspace_bytes, int bs, int num_keys, int num_heads,
+                                 int head_dim, int num_levels, int num_points, int num_queries,
+                                 int ref_dim, int dtype, unsigned flags, void* stream);
 
 /*
  * Zero `bytes` bytes of device memory at `ptr` on `stream` with the

@@ -15,9 +15,10 @@ steps of ``MSDeformAttn.forward`` in the Deformable DETR walk-through
 The locations decide which pixels are read, so they are formed in the same
 binary32 operations, in the same order, as the CUDA kernels take them (the
 reading of "where floating point decides an integer, both sides decide in the
-same precision"): 2-d: loc = fl(ref + fl(off / W)); 4-d: loc = fl(ref_xy +
-fl(fl(off * ref_wh) / (2P))).  ``exact=True`` forms them in fp64 instead (for
-finite differences).  The backward is the chain rule through the same steps:
+same precision"), dividing by multiplying with the once-rounded reciprocal:
+2-d: loc = fl(ref + fl(off * fl(1/W))); 4-d: loc = fl(ref_xy + fl(fl(off *
+ref_wh) * fl(1/(2P)))).  ``exact=True`` forms them in fp64 instead (for finite
+differences).  The backward is the chain rule through the same steps:
 
     grad_logits = a * (grad_a - sum_j a_j grad_a_j)          (softmax Jacobian)
     2-d: grad_off = grad_loc / (W, H);        grad_ref = sum_{m,p} grad_loc
@@ -52,12 +53,13 @@ def locations(reference_points: np.ndarray, sampling_offsets: np.ndarray,
     ft = np.float64 if exact else np.float32
     ref = ref.astype(ft)[:, :, None, :, None, :]              # [bs, Q, 1, L, 1, 2|4]
     off = off.astype(ft)
+    one = ft(1.0)
     if ref.shape[-1] == 2:
         norm = np.stack([np.asarray(spatial_shapes)[:, 1], np.asarray(spatial_shapes)[:, 0]], -1)
-        norm = norm.astype(ft)[None, None, None, :, None, :]  # (W, H) per level
-        return ref + off / norm
+        inv = one / norm.astype(ft)[None, None, None, :, None, :]   # fl(1/W), fl(1/H) per level
+        return ref + off * inv
     if ref.shape[-1] == 4:
-        return ref[..., :2] + (off * ref[..., 2:]) / ft(2 * P)
+        return ref[..., :2] + (off * ref[..., 2:]) * (one / ft(2 * P))
     raise ValueError("reference_points must end in 2 or 4")
 
 

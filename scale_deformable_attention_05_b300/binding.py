@@ -20,7 +20,9 @@ __all__ = [
     "MsdaError", "LIB_PATH",
     "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
-    "msda_backward_noalloc", "MSDeformAttnFunction", "ms_deform_attn", "EXPORTED_SYMBOLS", "load_library",
+    "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused",
+    "MSDeformAttnFunction", "MSDeformAttnFusedFunction", "ms_deform_attn", "ms_deform_attn_fused",
+    "EXPORTED_SYMBOLS", "load_library",
 ]
 
 MSDA_F32 = 0
@@ -33,7 +35,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsda.so"
 EXPORTED_SYMBOLS = (
     "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
-    "msda_backward_noalloc",
+    "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused",
 )
 
 _vp = ctypes.c_void_p
@@ -71,6 +73,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msda_version.restype = _int
     lib.msda_backward_noalloc.argtypes = [_vp] * 9 + _DIMS + [_int, ctypes.c_uint, _vp]
     lib.msda_backward_noalloc.restype = _int
+    lib.msda_forward_fused.argtypes = [_vp] * 7 + _DIMS + [_int, _int, _vp]
+    lib.msda_forward_fused.restype = _int
+    lib.msda_backward_fused.argtypes = ([_vp] * 12 + [ctypes.c_size_t] + _DIMS +
+                                        [_int, _int, ctypes.c_uint, _vp])
+    lib.msda_backward_fused.restype = _int
     return lib
 
 
@@ -206,6 +213,65 @@ def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_loc
     return grad_value, grad_sampling_loc, grad_attn_weight
 
 
+def _fused_dims(value, spatial_shapes, reference_points, sampling_offsets, attn_logits):
+    bs, K, M, D, L, P, Q = _dims(value, spatial_shapes, sampling_offsets)
+    if reference_points.dim() != 4 or tuple(reference_points.shape[:3]) != (bs, Q, L):
+        raise ValueError("reference_points must be [bs, Q, L, 2 or 4]")
+    ref_dim = int(reference_points.shape[3])
+    if tuple(attn_logits.shape) != (bs, Q, M, L * P):
+        raise ValueError("attn_logits must be [bs, Q, M, L*P]")
+    return bs, K, M, D, L, P, Q, ref_dim
+
+
+def msda_forward_fused(value, spatial_shapes, level_start_index, reference_points,
+                       sampling_offsets, attn_logits, output=None, stream=None) -> torch.Tensor:
+    """output [bs, Q, M*D]: softmax of the logits and locations from the reference
+    points and offsets, then the operator, in one kernel (see include/msda.h)."""
+    bs, K, M, D, L, P, Q, ref_dim = _fused_dims(value, spatial_shapes, reference_points,
+                                                sampling_offsets, attn_logits)
+    code = _dtype_code(value, spatial_shapes)
+    if output is None:
+        output = torch.empty((bs, Q, M * D), dtype=value.dtype, device=value.device)
+    _check("msda_forward_fused", _LIB.msda_forward_fused(
+        _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index, spatial_shapes)),
+        _ptr(reference_points), _ptr(sampling_offsets), _ptr(attn_logits), _ptr(output),
+        bs, K, M, D, L, P, Q, ref_dim, code, _stream(stream)))
+    return output
+
+
+def msda_backward_fused(value, spatial_shapes, level_start_index, reference_points,
+                        sampling_offsets, attn_logits, grad_output, grad_value=None,
+                        grad_sampling_offsets=None, grad_attn_logits=None,
+                        reference_grad: bool = True, workspace: Optional[torch.Tensor] = None,
+                        accumulate: bool = False, stream=None):
+    """(grad_value, grad_sampling_offsets, grad_attn_logits, grad_reference_points or None);
+    the reference-point gradient is an fp32 tensor [bs, Q, L, ref_dim]."""
+    bs, K, M, D, L, P, Q, ref_dim = _fused_dims(value, spatial_shapes, reference_points,
+                                                sampling_offsets, attn_logits)
+    code = _dtype_code(value, spatial_shapes)
+    dev = value.device
+    if grad_value is None:
+        grad_value = torch.empty_like(value)
+    if grad_sampling_offsets is None:
+        grad_sampling_offsets = torch.empty_like(sampling_offsets)
+    if grad_attn_logits is None:
+        grad_attn_logits = torch.empty_like(attn_logits)
+    grad_ref = (torch.empty((bs, Q, L, ref_dim), dtype=torch.float32, device=dev)
+                if reference_grad else None)
+    need = msda_backward_workspace_bytes(bs, K, M, D, code)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("msda_backward_fused", _LIB.msda_backward_fused(
+        _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index, spatial_shapes)),
+        _ptr(reference_points), _ptr(sampling_offsets), _ptr(attn_logits), _ptr(grad_output),
+        _ptr(grad_value), _ptr(grad_sampling_offsets), _ptr(grad_attn_logits), _ptr(grad_ref),
+        _ptr(workspace) if workspace is not None else None, ws_bytes,
+        bs, K, M, D, L, P, Q, ref_dim, code, MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0,
+        _stream(stream)))
+    return grad_value, grad_sampling_offsets, grad_attn_logits, grad_ref
+
+
 def msda_zero_fill(t: torch.Tensor, stream=None) -> torch.Tensor:
     _check("msda_zero_fill", _LIB.msda_zero_fill(_ptr(t), t.numel() * t.element_size(),
                                                  _stream(stream)))
@@ -254,6 +320,39 @@ class MSDeformAttnFunction(torch.autograd.Function):
         gv, gl, ga = msda_backward(value, spatial_shapes, level_start_index, sampling_loc,
                                    attn_weight, grad_output.contiguous())
         return gv, None, None, gl, ga, None
+
+
+class MSDeformAttnFusedFunction(torch.autograd.Function):
+    """Autograd wrapper of the fused entry points: (value, spatial_shapes,
+    level_start_index, reference_points, sampling_offsets, attn_logits) ->
+    output; backward returns gradients for value, reference_points (when it
+    requires grad), sampling_offsets and attn_logits."""
+
+    @staticmethod
+    def forward(ctx, value, spatial_shapes, level_start_index, reference_points,
+                sampling_offsets, attn_logits):
+        value, reference_points = value.contiguous(), reference_points.contiguous()
+        sampling_offsets, attn_logits = sampling_offsets.contiguous(), attn_logits.contiguous()
+        out = msda_forward_fused(value, spatial_shapes, level_start_index, reference_points,
+                                 sampling_offsets, attn_logits)
+        ctx.save_for_backward(value, spatial_shapes, level_start_index, reference_points,
+                              sampling_offsets, attn_logits)
+        return out
+
+    @staticmethod
+    def backward(ctx, grad_output):
+        value, shapes, lsi, ref, off, logits = ctx.saved_tensors
+        need_ref = ctx.needs_input_grad[3]
+        gv, goff, glog, gref = msda_backward_fused(value, shapes, lsi, ref, off, logits,
+                                                   grad_output.contiguous(),
+                                                   reference_grad=need_ref)
+        return gv, None, None, (gref.to(ref.dtype) if need_ref else None), goff, glog
+
+
+def ms_deform_attn_fused(value, spatial_shapes, level_start_index, reference_points,
+                         sampling_offsets, attn_logits):
+    return MSDeformAttnFusedFunction.apply(value, spatial_shapes, level_start_index,
+                                           reference_points, sampling_offsets, attn_logits)
 
 
 def ms_deform_attn(value, spatial_shapes, level_start_index, sampling_loc, attn_weight):

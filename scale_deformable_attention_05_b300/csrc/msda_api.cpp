@@ -47,6 +47,14 @@ int check_dims(const Dims& d, int dtype) {
     return MSDA_OK;
 }
 
+// The fused entry points keep each (b, q, m) row's L*P samples in one round of
+// a warp: at most MSDA_MAX_FUSED_LEVEL_POINTS of them.
+int check_fused(const Dims& d, int ref_dim) {
+    if (ref_dim != 2 && ref_dim != 4) return MSDA_ERR_UNSUPPORTED;
+    if (d.L * d.P > MSDA_MAX_FUSED_LEVEL_POINTS) return MSDA_ERR_UNSUPPORTED;
+    return MSDA_OK;
+}
+
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA; }
@@ -91,29 +99,128 @@ const char* msda_status_string(int status) {
     }
 }
 
-int msda_forward(const void* value, const void* spatial_shapes,
-                 const void* level_start_index, const void* sampling_loc,
-                 const void* attn_weight, void* output, int bs, int num_keys, int num_heads,
-                 int head_dim, int num_levels, int num_points, int num_queries, int dtype,
-                 void* stream) {
-    const Dims d{bs, num_keys, num_heads, head_dim, num_levels, num_points, num_queries};
+}  // extern "C"
+
+namespace {
+
+// Shared body of msda_forward (ref_dim 0: sampling_loc / attn_weight are
+// locations and weights) and msda_forward_fused (ref_dim 2 or 4:
+// sampling_loc / attn_weight are offsets and logits, ref the reference points).
+int forward_impl(const void* value, const void* spatial_shapes, const void* level_start_index,
+                 const void* sampling_loc, const void* attn_weight, const void* ref,
+                 int ref_dim, void* output, const Dims& d, int dtype, void* stream) {
     MSDA_TRY(check_dims(d, dtype));
+    if (ref_dim != 0) MSDA_TRY(check_fused(d, ref_dim));
     MSDA_TRY(check_ptr(output, d.out_elems()));
     const bool work = d.points() > 0 && d.out_elems() > 0;
     if (work) {
         MSDA_TRY(check_ptr(value, d.value_elems()));
         MSDA_TRY(check_ptr(sampling_loc, d.points()));
         MSDA_TRY(check_ptr(attn_weight, d.points()));
+        if (ref_dim != 0) MSDA_TRY(check_ptr(ref, d.bs * d.Q * d.L * ref_dim));
         if (spatial_shapes == nullptr || level_start_index == nullptr) return MSDA_ERR_NULL;
     }
     if (d.out_elems() == 0) return MSDA_OK;
     cudaStream_t st = as_stream(stream);
     if (!work)  // no samples: the output is all zeros
         return cuda_status(msda::launch_zero_fill(output, d.out_elems() * elem_bytes(dtype), st));
-    const msda::Problem pb{value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
-                           bs, num_keys, num_heads, head_dim, num_levels, num_points,
-                           num_queries, index32(dtype)};
+    msda::Problem pb{value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
+                     (int)d.bs, (int)d.K, (int)d.M, (int)d.D, (int)d.L, (int)d.P, (int)d.Q,
+                     index32(dtype)};
+    pb.ref = ref;
+    pb.ref_dim = ref_dim;
     return cuda_status(msda::launch_forward(pb, output, value_type(dtype), st));
+}
+
+// Shared body of msda_backward and msda_backward_fused (see forward_impl);
+// grad_ref (fused only, fp32, may be null) is zero-filled and accumulated.
+int backward_impl(const void* value, const void* spatial_shapes, const void* level_start_index,
+                  const void* sampling_loc, const void* attn_weight, const void* ref, int ref_dim,
+                  const void* grad_output, void* grad_value, void* grad_sampling_loc,
+                  void* grad_attn_weight, float* grad_ref, void* workspace,
+                  size_t workspace_bytes, const Dims& d, int dtype, unsigned flags,
+                  void* stream) {
+    MSDA_TRY(check_dims(d, dtype));
+    if (ref_dim != 0) MSDA_TRY(check_fused(d, ref_dim));
+    if (flags & ~MSDA_GRAD_VALUE_ACCUMULATE) return MSDA_ERR_UNSUPPORTED;
+    const bool accumulate = (flags & MSDA_GRAD_VALUE_ACCUMULATE) != 0;
+    MSDA_TRY(check_ptr(grad_value, d.value_elems()));
+    MSDA_TRY(check_ptr(grad_sampling_loc, 2 * d.points()));
+    MSDA_TRY(check_ptr(grad_attn_weight, d.points()));
+    const int64_t ref_elems = ref_dim != 0 ? d.bs * d.Q * d.L * ref_dim : 0;
+    if (grad_ref != nullptr && !aligned16(grad_ref)) return MSDA_ERR_ALIGN;
+    const bool work = d.points() > 0 && d.value_elems() > 0;
+    if (work) {
+        MSDA_TRY(check_ptr(value, d.value_elems()));
+        MSDA_TRY(check_ptr(sampling_loc, d.points()));
+        MSDA_TRY(check_ptr(attn_weight, d.points()));
+        MSDA_TRY(check_ptr(grad_output, d.out_elems()));
+        if (ref_dim != 0) MSDA_TRY(check_ptr(ref, ref_elems));
+        if (spatial_shapes == nullptr || level_start_index == nullptr) return MSDA_ERR_NULL;
+    }
+    const size_t ws_need =
+        msda_backward_workspace_bytes((int)d.bs, (int)d.K, (int)d.M, (int)d.D, dtype);
+    if (ws_need > 0) {
+        if (workspace == nullptr || workspace_bytes < ws_need) return MSDA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return MSDA_ERR_ALIGN;
+    }
+    cudaStream_t st = as_stream(stream);
+    const int e = elem_bytes(dtype);
+    const size_t value_bytes = (size_t)d.value_elems() * e;
+    if (grad_ref != nullptr && ref_elems > 0)
+        MSDA_TRY(cuda_status(msda::launch_zero_fill(grad_ref, ref_elems * sizeof(float), st)));
+    if (!work) {
+        // No sample reads value: zero location / weight grads, and grad_value
+        // stays as it is (accumulate) or becomes zero.
+        if (!accumulate) MSDA_TRY(cuda_status(msda::launch_zero_fill(grad_value, value_bytes, st)));
+        MSDA_TRY(cuda_status(msda::launch_zero_fill(grad_sampling_loc, 2 * d.points() * e, st)));
+        return cuda_status(msda::launch_zero_fill(grad_attn_weight, d.points() * e, st));
+    }
+    msda::Problem pb{value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
+                     (int)d.bs, (int)d.K, (int)d.M, (int)d.D, (int)d.L, (int)d.P, (int)d.Q,
+                     index32(dtype)};
+    pb.ref = ref;
+    pb.ref_dim = ref_dim;
+    const int vt = value_type(dtype);
+    float* gv32;
+    if (vt == MSDA_F32) {
+        gv32 = static_cast<float*>(grad_value);
+        if (!accumulate) MSDA_TRY(cuda_status(msda::launch_zero_fill(gv32, value_bytes, st)));
+    } else {
+        gv32 = static_cast<float*>(workspace);
+        MSDA_TRY(cuda_status(msda::launch_zero_fill(gv32, ws_need, st)));
+    }
+    MSDA_TRY(cuda_status(msda::launch_backward(pb, grad_output, gv32, grad_sampling_loc,
+                                               grad_attn_weight, vt, st, grad_ref)));
+    if (vt != MSDA_F32)
+        return cuda_status(msda::launch_finalize_half(gv32, grad_value, (size_t)d.value_elems(),
+                                                      accumulate, vt, st));
+    return MSDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int msda_forward(const void* value, const void* spatial_shapes,
+                 const void* level_start_index, const void* sampling_loc,
+                 const void* attn_weight, void* output, int bs, int num_keys, int num_heads,
+                 int head_dim, int num_levels, int num_points, int num_queries, int dtype,
+                 void* stream) {
+    const Dims d{bs, num_keys, num_heads, head_dim, num_levels, num_points, num_queries};
+    return forward_impl(value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
+                        nullptr, 0, output, d, dtype, stream);
+}
+
+int msda_forward_fused(const void* value, const void* spatial_shapes,
+                       const void* level_start_index, const void* reference_points,
+                       const void* sampling_offsets, const void* attn_logits, void* output,
+                       int bs, int num_keys, int num_heads, int head_dim, int num_levels,
+                       int num_points, int num_queries, int ref_dim, int dtype, void* stream) {
+    const Dims d{bs, num_keys, num_heads, head_dim, num_levels, num_points, num_queries};
+    if (ref_dim != 2 && ref_dim != 4) return MSDA_ERR_UNSUPPORTED;
+    return forward_impl(value, spatial_shapes, level_start_index, sampling_offsets, attn_logits,
+                        reference_points, ref_dim, output, d, dtype, stream);
 }
 
 size_t msda_backward_workspace_bytes(int bs, int num_keys, int num_heads, int head_dim,
@@ -131,53 +238,26 @@ int msda_backward(const void* value, const void* spatial_shapes,
                   int num_levels, int num_points, int num_queries, int dtype, unsigned flags,
                   void* stream) {
     const Dims d{bs, num_keys, num_heads, head_dim, num_levels, num_points, num_queries};
-    MSDA_TRY(check_dims(d, dtype));
-    if (flags & ~MSDA_GRAD_VALUE_ACCUMULATE) return MSDA_ERR_UNSUPPORTED;
-    const bool accumulate = (flags & MSDA_GRAD_VALUE_ACCUMULATE) != 0;
-    MSDA_TRY(check_ptr(grad_value, d.value_elems()));
-    MSDA_TRY(check_ptr(grad_sampling_loc, 2 * d.points()));
-    MSDA_TRY(check_ptr(grad_attn_weight, d.points()));
-    const bool work = d.points() > 0 && d.value_elems() > 0;
-    if (work) {
-        MSDA_TRY(check_ptr(value, d.value_elems()));
-        MSDA_TRY(check_ptr(sampling_loc, d.points()));
-        MSDA_TRY(check_ptr(attn_weight, d.points()));
-        MSDA_TRY(check_ptr(grad_output, d.out_elems()));
-        if (spatial_shapes == nullptr || level_start_index == nullptr) return MSDA_ERR_NULL;
-    }
-    const size_t ws_need = msda_backward_workspace_bytes(bs, num_keys, num_heads, head_dim, dtype);
-    if (ws_need > 0) {
-        if (workspace == nullptr || workspace_bytes < ws_need) return MSDA_ERR_WORKSPACE;
-        if (!aligned16(workspace)) return MSDA_ERR_ALIGN;
-    }
-    cudaStream_t st = as_stream(stream);
-    const int e = elem_bytes(dtype);
-    const size_t value_bytes = (size_t)d.value_elems() * e;
-    if (!work) {
-        // No sample reads value: zero location / weight grads, and grad_value
-        // stays as it is (accumulate) or becomes zero.
-        if (!accumulate) MSDA_TRY(cuda_status(msda::launch_zero_fill(grad_value, value_bytes, st)));
-        MSDA_TRY(cuda_status(msda::launch_zero_fill(grad_sampling_loc, 2 * d.points() * e, st)));
-        return cuda_status(msda::launch_zero_fill(grad_attn_weight, d.points() * e, st));
-    }
-    const msda::Problem pb{value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
-                           bs, num_keys, num_heads, head_dim, num_levels, num_points,
-                           num_queries, index32(dtype)};
-    const int vt = value_type(dtype);
-    float* gv32;
-    if (vt == MSDA_F32) {
-        gv32 = static_cast<float*>(grad_value);
-        if (!accumulate) MSDA_TRY(cuda_status(msda::launch_zero_fill(gv32, value_bytes, st)));
-    } else {
-        gv32 = static_cast<float*>(workspace);
-        MSDA_TRY(cuda_status(msda::launch_zero_fill(gv32, ws_need, st)));
-    }
-    MSDA_TRY(cuda_status(msda::launch_backward(pb, grad_output, gv32, grad_sampling_loc,
-                                               grad_attn_weight, vt, st)));
-    if (vt != MSDA_F32)
-        return cuda_status(msda::launch_finalize_half(gv32, grad_value, (size_t)d.value_elems(),
-                                                      accumulate, vt, st));
-    return MSDA_OK;
+    return backward_impl(value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
+                         nullptr, 0, grad_output, grad_value, grad_sampling_loc,
+                         grad_attn_weight, nullptr, workspace, workspace_bytes, d, dtype, flags,
+                         stream);
+}
+
+int msda_backward_fused(const void* value, const void* spatial_shapes,
+                        const void* level_start_index, const void* reference_points,
+                        const void* sampling_offsets, const void* attn_logits,
+                        const void* grad_output, void* grad_value, void* grad_sampling_offsets,
+                        void* grad_attn_logits, float* grad_reference_points, void* workspace,
+                        size_t workspace_bytes, int bs, int num_keys, int num_heads,
+                        int head_dim, int num_levels, int num_points, int num_queries,
+                        int ref_dim, int dtype, unsigned flags, void* stream) {
+    const Dims d{bs, num_keys, num_heads, head_dim, num_levels, num_points, num_queries};
+    if (ref_dim != 2 && ref_dim != 4) return MSDA_ERR_UNSUPPORTED;
+    return backward_impl(value, spatial_shapes, level_start_index, sampling_offsets,
+                         attn_logits, reference_points, ref_dim, grad_output, grad_value,
+                         grad_sampling_offsets, grad_attn_logits, grad_reference_points,
+                         workspace, workspace_bytes, d, dtype, flags, stream);
 }
 
 int msda_zero_fill(void* ptr, size_t bytes, void* stream) {

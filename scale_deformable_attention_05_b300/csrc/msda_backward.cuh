@@ -54,10 +54,15 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
 // lane sends one red with the summed weight a*w_c and the others send none.
 // Corners can only coincide within a pixel parity class, so each class is
 // compared across the segment with xor shuffles.
-template <int kSPG, int kStride>
+// kPrep: the round holds offsets and softmax weights (fused entry points);
+// the location is formed from pf's reference point first, aux.x keeps the
+// softmax weight of every sample (finite by construction), and the sample's
+// offset and box size go to woff / wwh for the reference-point gradient.
+template <int kSPG, int kStride, bool kPrep>
 __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* wax,
-                                                 const SampleFetch& f,
-                                                 const LevelInfo* s_levels,
+                                                 float4* woffwh, const SampleFetch& f,
+                                                 const PrepFetch& pf, int ref_dim,
+                                                 int num_points, const LevelInfo* s_levels,
                                                  const unsigned char* s_level_of, int r0,
                                                  int lane, int dedup) {
 #pragma unroll
@@ -77,10 +82,16 @@ __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* 
             const int l = s_level_of[r0 + sj];
             const LevelInfo lv = s_levels[l];
             const float a = f.a[h];
-            const Footprint fp = make_footprint(fmaf(f.xy[h].x, (float)lv.W, -0.5f),
-                                                fmaf(f.xy[h].y, (float)lv.H, -0.5f), lv);
+            float2 xy = f.xy[h];
+            if constexpr (kPrep) {
+                woffwh[sg * kStride + sj] = make_float4(xy.x, xy.y, pf.rwh[h].x, pf.rwh[h].y);
+                xy = prep_location(pf.rxy[h], pf.rwh[h], xy, ref_dim, __frcp_rn((float)lv.W),
+                                   __frcp_rn((float)lv.H), __frcp_rn((float)(2 * num_points)));
+            }
+            const Footprint fp = make_footprint(fmaf(xy.x, (float)lv.W, -0.5f),
+                                                fmaf(xy.y, (float)lv.H, -0.5f), lv);
             key = make_int4(fp.key[0], fp.key[1], fp.key[2], fp.key[3]);
-            aux = make_float4(fp.live ? a : 0.f, fp.fx, fp.fy, __int_as_float(l));
+            aux = make_float4(fp.live || kPrep ? a : 0.f, fp.fx, fp.fy, __int_as_float(l));
             cc = class_corners(fp, a);
             px = fp.x0 & 1;
             py = fp.y0 & 1;
@@ -131,7 +142,12 @@ __device__ __forceinline__ void load_grad_row(float (&gr)[kVPL][IO<T>::kVec],
 }
 
 // tiles_per_cta: CTA c runs tiles [c * tiles_per_cta, (c + 1) * tiles_per_cta).
-template <typename T, int kLanes, int kVPL>
+// kPrep: fused entry point -- loc holds sampling offsets, attn the attention
+// logits, ref the reference points; grad_loc receives the offset gradient,
+// grad_attn the logit gradient (softmax Jacobian), grad_ref (fp32, may be
+// null) the reference-point gradient summed over heads and points.  Requires
+// L*P <= kSPG (every row in one round).
+template <typename T, int kLanes, int kVPL, bool kPrep>
 __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                                   MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS > 0
                                       ? MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS
@@ -142,7 +158,8 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                     float* __restrict__ grad_value_f32, T* __restrict__ grad_loc,
                     T* __restrict__ grad_attn, int num_keys, int num_heads, int head_dim,
                     int num_levels, int num_points, int num_queries, int num_qtiles,
-                    int num_tiles, int tiles_per_cta) {
+                    int num_tiles, int tiles_per_cta, const T* __restrict__ ref, int ref_dim,
+                    float* __restrict__ grad_ref) {
     using Geom = TileGeom<kLanes>;
     constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
     constexpr int V = IO<T>::kVec;
@@ -158,6 +175,10 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     __shared__ int4 s_key[MSDA_BWD_WARPS][Geom::kRecords];
     __shared__ float4 s_aw[MSDA_BWD_WARPS][Geom::kRecords];
     __shared__ float4 s_aux[MSDA_BWD_WARPS][Geom::kRecords];
+    // fused mode: per sample (offset, box size), (grad_loc, grad_a)
+    constexpr int kPrepRecords = kPrep ? Geom::kRecords : 1;
+    __shared__ float4 s_offwh[kPrep ? MSDA_BWD_WARPS : 1][kPrepRecords];
+    __shared__ float4 s_gla[kPrep ? MSDA_BWD_WARPS : 1][kPrepRecords];
 
     load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, idx32,
                      num_levels, num_points, num_keys);
@@ -176,6 +197,8 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     int4* wk = s_key[warp];
     float4* waw = s_aw[warp];
     float4* wax = s_aux[warp];
+    float4* woffwh = s_offwh[kPrep ? warp : 0];
+    float4* wgla = s_gla[kPrep ? warp : 0];
 
     StepIter it;
     it.t = blockIdx.x * tiles_per_cta + warp;
@@ -187,16 +210,21 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     if (!it.valid()) return;
 
     SampleFetch f;
+    PrepFetch pf;
     TileCoord tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
     fetch_samples<T, kSPG>(f, loc, attn, tc, 0, lane, LP, num_queries, num_heads);
+    if constexpr (kPrep)
+        fetch_refs<T, kSPG>(pf, f, ref, ref_dim, tc, 0, lane, num_queries, num_levels,
+                            s_level_of);
     float gr[kVPL][V], gnext[kVPL][V];
     load_grad_row<T, kLanes, kVPL>(gnext, grad_out, tc, g, li, nvec, num_queries, num_heads,
                                    head_dim);
 
     while (true) {
         // ---- 1. footprints of this round (inputs fetched one round ahead)
-        backward_records<kSPG, kStride>(wk, waw, wax, f, s_levels, s_level_of, it.r0, lane,
-                                        dedup);
+        if constexpr (kPrep) softmax_rows<kSPG>(f);
+        backward_records<kSPG, kStride, kPrep>(wk, waw, wax, woffwh, f, pf, ref_dim, num_points,
+                                               s_levels, s_level_of, it.r0, lane, dedup);
         __syncwarp();
         const TileCoord cur = tc;
         const int r0 = it.r0;
@@ -211,6 +239,9 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
         if (more) {
             tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
             fetch_samples<T, kSPG>(f, loc, attn, tc, it.r0, lane, LP, num_queries, num_heads);
+            if constexpr (kPrep)
+                fetch_refs<T, kSPG>(pf, f, ref, ref_dim, tc, it.r0, lane, num_queries,
+                                    num_levels, s_level_of);
             if (it.r0 == 0)
                 load_grad_row<T, kLanes, kVPL>(gnext, grad_out, tc, g, li, nvec, num_queries,
                                                num_heads, head_dim);
@@ -311,9 +342,63 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                 if (li % kLanesPerSamp == 0 && jb + s8 < nj && q < num_queries) {
                     const LevelInfo lv = s_levels[__float_as_int(ax.w)];
                     const int64_t pt = row * LP + r0 + jb + s8;
-                    IO<T>::store_xy(grad_loc + 2 * pt, (float)lv.W * (a * gx),
-                                    (float)lv.H * (a * gy));
-                    IO<T>::store_one(grad_attn + pt, ga);
+                    const float glx = (float)lv.W * (a * gx), gly = (float)lv.H * (a * gy);
+                    if constexpr (kPrep) {
+                        // offset gradient now; weight and location gradients kept for
+                        // the softmax Jacobian and the reference-point sums below
+                        const int rec = g * kStride + jb + s8;
+                        wgla[rec] = make_float4(glx, gly, ga, 0.f);
+                        float ox = a * gx, oy = a * gy;             // grad_loc / (W, H)
+                        if (ref_dim == 4) {
+                            const float4 ow = woffwh[rec];
+                            const float two_p = (float)(2 * num_points);
+                            ox = glx * ow.z / two_p;                // grad_loc * box / (2P)
+                            oy = gly * ow.w / two_p;
+                        }
+                        IO<T>::store_xy(grad_loc + 2 * pt, ox, oy);
+                    } else {
+                        IO<T>::store_xy(grad_loc + 2 * pt, glx, gly);
+                        IO<T>::store_one(grad_attn + pt, ga);
+                    }
+                }
+            }
+        }
+        if constexpr (kPrep) {
+            // ---- 5. the row's logit gradients a_j (g_j - sum_i a_i g_i) and its
+            //         reference-point gradient sums (the row is this round's whole tile)
+            __syncwarp();
+            const bool qok = q < num_queries;
+            float S = 0.f;
+            for (int jj = li; qok && jj < LP; jj += kLanes) {
+                const int rec = g * kStride + jj;
+                S = fmaf(wax[rec].x, wgla[rec].z, S);
+            }
+#pragma unroll
+            for (int o = 1; o < kLanes; o <<= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+            for (int jj = li; qok && jj < LP; jj += kLanes) {
+                const int rec = g * kStride + jj;
+                IO<T>::store_one(grad_attn + row * LP + jj, wax[rec].x * (wgla[rec].z - S));
+            }
+            if (grad_ref != nullptr && qok) {
+                const float two_p = (float)(2 * num_points);
+                for (int pi = li; pi < num_levels * ref_dim; pi += kLanes) {
+                    const int l = pi / ref_dim, c = pi - l * ref_dim;
+                    float sum = 0.f;
+                    for (int p = 0; p < num_points; ++p) {
+                        const int rec = g * kStride + l * num_points + p;
+                        const float4 gla = wgla[rec];
+                        const float glc = (c & 1) ? gla.y : gla.x;
+                        if (c < 2) {
+                            sum += glc;
+                        } else {
+                            const float4 ow = woffwh[rec];
+                            sum += glc * ((c & 1) ? ow.y : ow.x) / two_p;
+                        }
+                    }
+                    atomicAdd(grad_ref +
+                                  (((int64_t)cur.b * num_queries + q) * num_levels + l) * ref_dim +
+                                  c,
+                              sum);
                 }
             }
         }

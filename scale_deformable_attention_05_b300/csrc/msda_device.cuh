@@ -454,6 +454,88 @@ __device__ __forceinline__ void fetch_samples(SampleFetch& f, const T* __restric
     }
 }
 
+// ---------------------------------------------------------- fused preparation
+// The fused entry points take, instead of locations and weights, reference
+// points [bs, Q, L, ref_dim] (ref_dim 2: (x, y); 4: (x, y, w, h)), sampling
+// offsets in the layout of sampling_locations and attention logits in the
+// layout of attention_weights (Deformable DETR walk-through, "2.2.4 源码分析",
+// MSDeformAttn.forward; 4-d references from section "2.4").  A fused round
+// fetches, per sample, the offsets into SampleFetch::xy, the logit into
+// SampleFetch::a, and the reference point into PrepFetch.
+struct PrepFetch {
+    float2 rxy[2], rwh[2];
+};
+
+template <typename T, int kSPG>
+__device__ __forceinline__ void fetch_refs(PrepFetch& pf, const SampleFetch& f,
+                                           const T* __restrict__ ref, int ref_dim,
+                                           const TileCoord& tc, int r0, int lane,
+                                           int num_queries, int num_levels,
+                                           const unsigned char* s_level_of) {
+#pragma unroll
+    for (int h = 0; h < kSamplesPerWarp / 32; ++h) {
+        const int s = lane + 32 * h;
+        const int sg = s / kSPG, sj = s % kSPG;
+        pf.rxy[h] = make_float2(0.f, 0.f);
+        pf.rwh[h] = make_float2(0.f, 0.f);
+        if (f.ok[h]) {
+            const int l = s_level_of[r0 + sj];
+            const int64_t base =
+                (((int64_t)tc.b * num_queries + tc.q0 + sg) * num_levels + l) * ref_dim;
+            pf.rxy[h] = IO<T>::load_xy(ref + base);
+            if (ref_dim == 4) pf.rwh[h] = IO<T>::load_xy(ref + base + 2);
+        }
+    }
+}
+
+// Sampling location of one sample, in the binary32 operations (each rounded
+// to nearest) the oracle replays, with the reciprocals rounded once:
+//   2-d: loc = ref + off * fl(1/W)           (ref + off / (W, H))
+//   4-d: loc = ref_xy + (off * ref_wh) * fl(1/(2P))   (ref_xy + off / P * ref_wh * 0.5)
+__device__ __forceinline__ float2 prep_location(float2 rxy, float2 rwh, float2 off, int ref_dim,
+                                                float inv_w, float inv_h, float inv_2p) {
+    if (ref_dim == 2)
+        return make_float2(__fadd_rn(rxy.x, __fmul_rn(off.x, inv_w)),
+                           __fadd_rn(rxy.y, __fmul_rn(off.y, inv_h)));
+    return make_float2(__fadd_rn(rxy.x, __fmul_rn(__fmul_rn(off.x, rwh.x), inv_2p)),
+                       __fadd_rn(rxy.y, __fmul_rn(__fmul_rn(off.y, rwh.y), inv_2p)));
+}
+
+// Replaces the logits in f.a by the softmax over each row's L*P samples.  A
+// fused round holds whole rows (L*P <= kSPG): for kSPG <= 32 a row is an
+// aligned segment of kSPG lanes of one half (h) of the round, for kSPG = 64 it
+// is both halves of all 32 lanes.  Samples past the row's end do not count; a
+// row with no sample (a query past the last) gets weights 0.
+template <int kSPG>
+__device__ __forceinline__ void softmax_rows(SampleFetch& f) {
+    constexpr int kSeg = kSPG < 32 ? kSPG : 32;
+    if constexpr (kSPG == 64) {
+        float m = fmaxf(f.ok[0] ? f.a[0] : -INFINITY, f.ok[1] ? f.a[1] : -INFINITY);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float e0 = f.ok[0] && m != -INFINITY ? expf(f.a[0] - m) : 0.f;
+        const float e1 = f.ok[1] && m != -INFINITY ? expf(f.a[1] - m) : 0.f;
+        float sum = e0 + e1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float inv = sum > 0.f ? __frcp_rn(sum) : 0.f;
+        f.a[0] = e0 * inv;
+        f.a[1] = e1 * inv;
+    } else {
+#pragma unroll
+        for (int h = 0; h < kSamplesPerWarp / 32; ++h) {
+            float m = f.ok[h] ? f.a[h] : -INFINITY;
+#pragma unroll
+            for (int o = 1; o < kSeg; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const float e = f.ok[h] && m != -INFINITY ? expf(f.a[h] - m) : 0.f;
+            float sum = e;
+#pragma unroll
+            for (int o = 1; o < kSeg; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            f.a[h] = sum > 0.f ? e * __frcp_rn(sum) : 0.f;
+        }
+    }
+}
+
 // The (tile, round) steps one warp executes: tiles begin + warp, begin + warp
 // + stride, ... below end; each tile in rounds of spg samples per group.
 struct StepIter {

@@ -34,9 +34,12 @@ namespace msda {
 #define MSDA_UNROLL(n) MSDA_PRAGMA(unroll n)
 
 // Stores the footprint records of the round fetched in f.
-template <int kSPG, int kStride>
+// kPrep: the round holds offsets and softmax weights (fused entry points);
+// the location is formed from pf's reference point first.
+template <int kSPG, int kStride, bool kPrep>
 __device__ __forceinline__ void forward_records(int4* wk, float4* ww, const SampleFetch& f,
-                                                const LevelInfo* s_levels,
+                                                const PrepFetch& pf, int ref_dim,
+                                                int num_points, const LevelInfo* s_levels,
                                                 const unsigned char* s_level_of, int r0,
                                                 int lane) {
 #pragma unroll
@@ -48,8 +51,12 @@ __device__ __forceinline__ void forward_records(int4* wk, float4* ww, const Samp
         if (f.ok[h]) {
             const LevelInfo lv = s_levels[s_level_of[r0 + sj]];
             const float a = f.a[h];
-            const Footprint fp = make_footprint(fmaf(f.xy[h].x, (float)lv.W, -0.5f),
-                                                fmaf(f.xy[h].y, (float)lv.H, -0.5f), lv);
+            float2 xy = f.xy[h];
+            if constexpr (kPrep)
+                xy = prep_location(pf.rxy[h], pf.rwh[h], xy, ref_dim, __frcp_rn((float)lv.W),
+                                   __frcp_rn((float)lv.H), __frcp_rn((float)(2 * num_points)));
+            const Footprint fp = make_footprint(fmaf(xy.x, (float)lv.W, -0.5f),
+                                                fmaf(xy.y, (float)lv.H, -0.5f), lv);
             key = make_int4(fp.key[0], fp.key[1], fp.key[2], fp.key[3]);
             w = make_float4(fp.key[0] >= 0 ? a * fp.w[0] : 0.f, fp.key[1] >= 0 ? a * fp.w[1] : 0.f,
                             fp.key[2] >= 0 ? a * fp.w[2] : 0.f, fp.key[3] >= 0 ? a * fp.w[3] : 0.f);
@@ -80,14 +87,17 @@ constexpr int forward_min_blocks(int channels_per_lane) {
 }
 
 // kVB: bytes per row vector and lane (16, or 32 with 256-bit loads).
-template <typename T, int kLanes, int kVPL, int kVB>
+// kPrep: fused entry point -- loc holds sampling offsets, attn the attention
+// logits, ref the reference points (ref_dim 2 or 4); requires L*P <= kSPG.
+template <typename T, int kLanes, int kVPL, int kVB, bool kPrep>
 __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
                                   forward_min_blocks(kVPL * kVB / (int)sizeof(T)))
     forward_kernel(const T* __restrict__ value, const void* __restrict__ spatial_shapes,
                    const void* __restrict__ level_start_index, int idx32, const T* __restrict__ loc,
                    const T* __restrict__ attn, T* __restrict__ out, int num_keys, int num_heads,
                    int head_dim, int num_levels, int num_points, int num_queries,
-                   int num_qtiles, int num_tiles, int tiles_per_cta) {
+                   int num_qtiles, int num_tiles, int tiles_per_cta, const T* __restrict__ ref,
+                   int ref_dim) {
     using Geom = TileGeom<kLanes>;
     using VIO = VecIO<T, kVB>;
     constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
@@ -120,8 +130,12 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
     if (!it.valid()) return;
 
     SampleFetch f;
+    PrepFetch pf;
     TileCoord tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
     fetch_samples<T, kSPG>(f, loc, attn, tc, 0, lane, LP, num_queries, num_heads);
+    if constexpr (kPrep)
+        fetch_refs<T, kSPG>(pf, f, ref, ref_dim, tc, 0, lane, num_queries, num_levels,
+                            s_level_of);
     float acc[kVPL][V];
 #pragma unroll
     for (int k = 0; k < kVPL; ++k)
@@ -130,7 +144,9 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
 
     while (true) {
         // ---- 1. footprints of this round (inputs fetched one round ahead)
-        forward_records<kSPG, kStride>(wk, ww, f, s_levels, s_level_of, it.r0, lane);
+        if constexpr (kPrep) softmax_rows<kSPG>(f);
+        forward_records<kSPG, kStride, kPrep>(wk, ww, f, pf, ref_dim, num_points, s_levels,
+                                              s_level_of, it.r0, lane);
         __syncwarp();
         const TileCoord cur = tc;
         const int r0 = it.r0;
@@ -140,6 +156,9 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
         if (more) {
             tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
             fetch_samples<T, kSPG>(f, loc, attn, tc, it.r0, lane, LP, num_queries, num_heads);
+            if constexpr (kPrep)
+                fetch_refs<T, kSPG>(pf, f, ref, ref_dim, tc, it.r0, lane, num_queries,
+                                    num_levels, s_level_of);
         }
 
         // ---- 2. gather: group g walks its query's samples

@@ -137,23 +137,25 @@ TileGrid tile_grid(const Problem& pb, int queries_per_tile, int resident, int wa
     return tg;
 }
 
-template <typename T, int kLanes, int kVPL, int kVB>
+template <typename T, int kLanes, int kVPL, int kVB, bool kPrep = false>
 cudaError_t launch_forward_t(const Problem& pb, void* out, cudaStream_t st) {
-    auto kernel = forward_kernel<T, kLanes, kVPL, kVB>;
+    auto kernel = forward_kernel<T, kLanes, kVPL, kVB, kPrep>;
     constexpr int kThreads = MSDA_FWD_WARPS * 32;
     const TileGrid tg =
         tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_FWD_WARPS);
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<T*>(out), pb.K, pb.M, pb.D, pb.L, pb.P, pb.Q,
-        tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta);
+        tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta, static_cast<const T*>(pb.ref),
+        pb.ref_dim);
     return cudaGetLastError();
 }
 
-template <typename T, int kLanes, int kVPL>
+template <typename T, int kLanes, int kVPL, bool kPrep = false>
 cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv32,
-                              void* grad_loc, void* grad_attn, cudaStream_t st) {
-    auto kernel = backward_kernel<T, kLanes, kVPL>;
+                              void* grad_loc, void* grad_attn, cudaStream_t st,
+                              float* grad_ref = nullptr) {
+    auto kernel = backward_kernel<T, kLanes, kVPL, kPrep>;
     constexpr int kThreads = MSDA_BWD_WARPS * 32;
     const TileGrid tg =
         tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS);
@@ -161,7 +163,8 @@ cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
         static_cast<T*>(grad_loc), static_cast<T*>(grad_attn), pb.K, pb.M, pb.D, pb.L, pb.P,
-        pb.Q, tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta);
+        pb.Q, tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta, static_cast<const T*>(pb.ref),
+        pb.ref_dim, grad_ref);
     return cudaGetLastError();
 }
 
@@ -197,8 +200,35 @@ cudaError_t dispatch_forward_vec(const Problem& pb, void* out, cudaStream_t st) 
 // Rows of 1 KB or more (two or more 16-byte vectors per lane) use 256-bit
 // loads: half the load instructions, measured faster on head_dim 256 fp32.
 // Shorter rows keep 128-bit loads, which measured as fast or faster.
+// Lane groups of the fused kernels: enough for the row's vectors, at least
+// `min_lanes`, and enough that one round (2 * lanes samples per group) holds
+// a whole (b, q, m) row of L*P <= 64 samples.
+Layout fused_layout(const Problem& pb, int nvec, int min_lanes) {
+    Layout ly = choose_layout(nvec);
+    int need = min_lanes;
+    while (2 * need < pb.L * pb.P) need <<= 1;
+    if (ly.lanes < need) ly.lanes = need;
+    return ly;
+}
+
+template <typename T>
+cudaError_t dispatch_forward_fused(const Problem& pb, void* out, cudaStream_t st) {
+    const Layout ly = fused_layout(pb, pb.D / IO<T>::kVec, 4);
+    if (ly.vpl == 1) {
+        switch (ly.lanes) {
+            case 4: return launch_forward_t<T, 4, 1, 16, true>(pb, out, st);
+            case 8: return launch_forward_t<T, 8, 1, 16, true>(pb, out, st);
+            case 16: return launch_forward_t<T, 16, 1, 16, true>(pb, out, st);
+            default: return launch_forward_t<T, 32, 1, 16, true>(pb, out, st);
+        }
+    }
+    if (ly.vpl == 2) return launch_forward_t<T, 32, 2, 16, true>(pb, out, st);
+    return launch_forward_t<T, 32, 4, 16, true>(pb, out, st);
+}
+
 template <typename T>
 cudaError_t dispatch_forward(const Problem& pb, void* out, cudaStream_t st) {
+    if (pb.ref_dim != 0) return dispatch_forward_fused<T>(pb, out, st);
     const int row = pb.D * (int)sizeof(T);
     if (row % 32 == 0 && row <= 2048 &&
         (MSDA_FWD_VEC32 == 2 || (MSDA_FWD_VEC32 == 1 && row >= 1024)))
@@ -223,8 +253,24 @@ cudaError_t launch_backward_merge_t(const Problem& pb, int log2_points, const vo
 }
 
 template <typename T>
+cudaError_t dispatch_backward_fused(const Problem& pb, const void* g, float* gv32, void* gl,
+                                    void* ga, cudaStream_t st, float* gref) {
+    const Layout ly = fused_layout(pb, pb.D / IO<T>::kVec, 8);
+    if (ly.vpl == 1) {
+        switch (ly.lanes) {
+            case 8: return launch_backward_t<T, 8, 1, true>(pb, g, gv32, gl, ga, st, gref);
+            case 16: return launch_backward_t<T, 16, 1, true>(pb, g, gv32, gl, ga, st, gref);
+            default: return launch_backward_t<T, 32, 1, true>(pb, g, gv32, gl, ga, st, gref);
+        }
+    }
+    if (ly.vpl == 2) return launch_backward_t<T, 32, 2, true>(pb, g, gv32, gl, ga, st, gref);
+    return launch_backward_t<T, 32, 4, true>(pb, g, gv32, gl, ga, st, gref);
+}
+
+template <typename T>
 cudaError_t dispatch_backward(const Problem& pb, const void* g, float* gv32, void* gl, void* ga,
-                              cudaStream_t st) {
+                              cudaStream_t st, float* gref) {
+    if (pb.ref_dim != 0) return dispatch_backward_fused<T>(pb, g, gv32, gl, ga, st, gref);
     const Layout ly = choose_layout(pb.D / IO<T>::kVec);
 #ifndef MSDA_NO_MERGE_PATH
     // Merged scatter for rows of at least 512 bytes (one lane group per warp,
@@ -267,10 +313,13 @@ cudaError_t launch_forward(const Problem& pb, void* out, int dtype, cudaStream_t
 }
 
 cudaError_t launch_backward(const Problem& pb, const void* grad_out, float* gv32, void* grad_loc,
-                            void* grad_attn, int dtype, cudaStream_t st) {
-    if (dtype == kF32) return dispatch_backward<float>(pb, grad_out, gv32, grad_loc, grad_attn, st);
-    if (dtype == kF16) return dispatch_backward<__half>(pb, grad_out, gv32, grad_loc, grad_attn, st);
-    return dispatch_backward<__nv_bfloat16>(pb, grad_out, gv32, grad_loc, grad_attn, st);
+                            void* grad_attn, int dtype, cudaStream_t st, float* grad_ref) {
+    if (dtype == kF32)
+        return dispatch_backward<float>(pb, grad_out, gv32, grad_loc, grad_attn, st, grad_ref);
+    if (dtype == kF16)
+        return dispatch_backward<__half>(pb, grad_out, gv32, grad_loc, grad_attn, st, grad_ref);
+    return dispatch_backward<__nv_bfloat16>(pb, grad_out, gv32, grad_loc, grad_attn, st,
+                                            grad_ref);
 }
 
 cudaError_t launch_zero_fill(void* p, size_t bytes, cudaStream_t st) {

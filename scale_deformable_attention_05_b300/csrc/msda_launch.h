@@ -16,6 +16,10 @@ struct Problem {
     const void* attn;
     int bs, K, M, D, L, P, Q;
     int idx32;            // index arrays are int32
+    // Fused entry points: loc holds sampling offsets, attn the attention
+    // logits, ref the reference points [bs, Q, L, ref_dim]; ref_dim 0 otherwise.
+    const void* ref = nullptr;
+    int ref_dim = 0;
 };
 
 // Element type codes (the low byte of the ABI's dtype argument).
@@ -24,8 +28,10 @@ constexpr int kF32 = 0, kBF16 = 1, kF16 = 2;
 cudaError_t launch_forward(const Problem& pb, void* out, int dtype, cudaStream_t st);
 // gv32: fp32 grad_value accumulator (the caller's fp32 grad_value, or the
 // bf16 path's workspace), already zeroed or holding the sum to add to.
+// grad_ref: fused mode's fp32 reference-point gradient (already zeroed), or null.
 cudaError_t launch_backward(const Problem& pb, const void* grad_out, float* gv32, void* grad_loc,
-                            void* grad_attn, int dtype, cudaStream_t st);
+                            void* grad_attn, int dtype, cudaStream_t st,
+                            float* grad_ref = nullptr);
 // Zeroes `bytes` bytes at p (16-byte aligned; any byte count).
 cudaError_t launch_zero_fill(void* p, size_t bytes, cudaStream_t st);
 // fp32 workspace -> bf16 (dtype kBF16) or fp16 (kF16) grad_value.

@@ -41,6 +41,7 @@ __all__ = [
     "f32_to_f16_bits",
     "f16_bits_to_f32",
     "make_inputs",
+    "make_fused_inputs",
     "random_workload",
 ]
 
@@ -290,6 +291,58 @@ def make_inputs(wl: Workload, with_grad: bool = True) -> Dict[str, np.ndarray]:
             out[k] = np.ascontiguousarray(a)
         else:
             raise ValueError(wl.dtype)
+    return out
+
+
+def make_fused_inputs(wl: Workload, ref_dim: int = 2, offset_sigma: float = 2.0
+                      ) -> Dict[str, np.ndarray]:
+    """Seeded inputs of the fused entry points for workload ``wl``.
+
+    Draw order: value, reference points (and box sizes for ``ref_dim == 4``),
+    offsets, logits, grad_output.  Reference points follow ``wl.loc_kind``:
+    ``encoder`` uses each query's pixel centre (all levels, valid ratios 1),
+    ``grid`` the row-major grid of cell centres, anything else U[0.1, 0.9]^2
+    per (b, q); the same point serves every level.  Box sizes are U[0.05, 0.4]
+    per (b, q).  Offsets are N(0, offset_sigma) and logits N(0, 1).  Rounded to
+    ``wl.dtype`` like ``make_inputs``; returned under ``reference_points``,
+    ``sampling_offsets``, ``attention_logits`` (plus ``*_bf16`` / ``*_f16`` bits).
+    """
+    rng = np.random.default_rng(wl.seed + 50000 * ref_dim)
+    bs, Q, M, D = wl.bs, wl.num_queries, wl.num_heads, wl.head_dim
+    L, P, K = wl.num_levels, wl.num_points, wl.num_keys
+    value = rng.standard_normal((bs, K, M, D))
+    if wl.loc_kind == "encoder":
+        ref = np.broadcast_to(encoder_reference_points(wl.spatial_shapes)[None], (bs, Q, 2))
+    elif wl.loc_kind == "grid":
+        n = int(round(np.sqrt(Q)))
+        ref = np.broadcast_to(grid_reference_points(n)[None], (bs, Q, 2))
+    else:
+        ref = rng.uniform(0.1, 0.9, (bs, Q, 2))
+    ref = np.broadcast_to(ref[:, :, None, :], (bs, Q, L, 2))
+    if ref_dim == 4:
+        wh = rng.uniform(0.05, 0.4, (bs, Q, 1, 2))
+        ref = np.concatenate([ref, np.broadcast_to(wh, (bs, Q, L, 2))], -1)
+    off = rng.normal(0.0, offset_sigma, (bs, Q, M, L, P, 2))
+    logits = rng.standard_normal((bs, Q, M, L * P))
+    g = rng.standard_normal((bs, Q, M * D))
+    out: Dict[str, np.ndarray] = {
+        "spatial_shapes": np.array(wl.spatial_shapes, dtype=np.int64).reshape(L, 2),
+        "level_start_index": level_start_index(wl.spatial_shapes),
+    }
+    arrays = {"value": value, "reference_points": ref, "sampling_offsets": off,
+              "attention_logits": logits, "grad_output": g}
+    for k, a in arrays.items():
+        a = np.ascontiguousarray(a, dtype=np.float32)
+        if wl.dtype == "bf16":
+            bits = f32_to_bf16_bits(a)
+            out[k + "_bf16"] = bits
+            out[k] = bf16_bits_to_f32(bits).reshape(a.shape)
+        elif wl.dtype == "f16":
+            bits = f32_to_f16_bits(a)
+            out[k + "_f16"] = bits
+            out[k] = f16_bits_to_f32(bits).reshape(a.shape)
+        else:
+            out[k] = a
     return out
 
 

@@ -1,0 +1,100 @@
+"""GPU results of the fused entry points (msda_forward_fused / msda_backward_fused)
+against the fused oracle (oracle/fused.py), through the C ABI, element by
+element with the tolerances of the parity tests (tests/gpu_helpers.py).  The
+locations select pixels in the same binary32 operations on both sides, so
+which value rows receive gradient is compared exactly."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import fused as ofused
+from scale_deformable_attention_05_b300 import inputs as gen
+from tests.gpu_helpers import TOL, assert_grad_close, assert_out_close, empty_cache, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from scale_deformable_attention_05_b300 import binding
+    return binding
+
+
+def _dev(inp, wl, name):
+    if wl.dtype in ("bf16", "f16"):
+        tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+        return torch.from_numpy(inp[name + "_" + wl.dtype].view(np.int16).copy()).view(tdt).cuda()
+    return torch.from_numpy(np.ascontiguousarray(inp[name])).cuda()
+
+
+def _run_and_check(B, wl, ref_dim, sigma=2.0):
+    inp = gen.make_fused_inputs(wl, ref_dim, offset_sigma=sigma)
+    names = ("value", "reference_points", "sampling_offsets", "attention_logits", "grad_output")
+    d = {k: _dev(inp, wl, k) for k in names}
+    sh = torch.from_numpy(inp["spatial_shapes"]).cuda()
+    lsi = torch.from_numpy(inp["level_start_index"]).cuda()
+    args = (d["value"], sh, lsi, d["reference_points"], d["sampling_offsets"],
+            d["attention_logits"])
+    out = B.msda_forward_fused(*args)
+    gv, goff, glog, gref = B.msda_backward_fused(*args, d["grad_output"])
+    torch.cuda.synchronize()
+    assert B.msda_last_device_error() == 0
+    oargs = (inp["value"], inp["spatial_shapes"], inp["level_start_index"],
+             inp["reference_points"], inp["sampling_offsets"], inp["attention_logits"])
+    assert_out_close(host(out), ofused.forward(*oargs), wl.dtype)
+    rv, roff, rlog, rref = ofused.backward(*oargs, inp["grad_output"])
+    assert_grad_close(host(gv), rv, wl.dtype, "grad_value")
+    assert_grad_close(host(goff), roff, wl.dtype, "grad_sampling_offsets")
+    assert_grad_close(host(glog), rlog, wl.dtype, "grad_attn_logits")
+    assert_grad_close(host(gref), rref, wl.dtype, "grad_reference_points")
+    np.testing.assert_array_equal(np.any(host(gv) != 0, -1), np.any(rv != 0, -1))
+    empty_cache()
+
+
+CASES = [
+    # (name, seed, bs, shapes, M, D, P, Q, dtype, ref_dim)
+    ("one-level", 61, 1, ((12, 10),), 2, 32, 8, 9, "f32", 2),
+    ("pyramid", 62, 2, ((9, 7), (5, 4), (3, 2), (2, 1)), 3, 32, 4, 17, "f32", 2),
+    ("boxes", 63, 2, ((9, 7), (5, 4), (3, 2), (2, 1)), 3, 32, 4, 17, "f32", 4),
+    ("wide-head", 64, 1, ((16, 12), (8, 6)), 2, 256, 16, 7, "f32", 4),
+    ("lp64", 65, 1, ((10, 9), (5, 5), (3, 3), (2, 2)), 2, 64, 16, 5, "f32", 2),
+    ("bf16", 66, 2, ((9, 7), (5, 4)), 2, 32, 8, 11, "bf16", 2),
+    ("f16-boxes", 67, 2, ((9, 7), (5, 4)), 2, 64, 4, 11, "f16", 4),
+    ("odd-points", 68, 1, ((7, 5), (4, 3), (2, 2)), 2, 16, 3, 13, "f32", 2),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c[0])
+def test_fused_random_shapes(B, case):
+    _, seed, bs, shapes, M, D, P, Q, dtype, ref_dim = case
+    wl = gen.random_workload(seed, bs, shapes, M, D, P, Q, dtype=dtype)
+    _run_and_check(B, wl, ref_dim)
+
+
+@pytest.mark.parametrize("ref_dim", [2, 4])
+def test_fused_decoder_shape(B, ref_dim):
+    _run_and_check(B, gen.WORKLOADS["decoder"], ref_dim)
+
+
+def test_fused_encoder_shape(B):
+    wl = gen.WORKLOADS["encoder"].with_(bs=1, seed=1007)
+    _run_and_check(B, wl, 2, sigma=1.5)
+
+
+def test_fused_autograd_wrapper(B):
+    wl = gen.random_workload(69, 2, ((9, 7), (5, 4)), 2, 32, 4, 9)
+    inp = gen.make_fused_inputs(wl, 2)
+    t = lambda k, rg=False: torch.tensor(inp[k], device="cuda", requires_grad=rg)
+    v, ref, off, lg = t("value", True), t("reference_points", True), t("sampling_offsets", True), \
+        t("attention_logits", True)
+    sh = torch.from_numpy(inp["spatial_shapes"]).cuda()
+    lsi = torch.from_numpy(inp["level_start_index"]).cuda()
+    out = B.ms_deform_attn_fused(v, sh, lsi, ref, off, lg)
+    out.backward(t("grad_output"))
+    oargs = (inp["value"], inp["spatial_shapes"], inp["level_start_index"],
+             inp["reference_points"], inp["sampling_offsets"], inp["attention_logits"])
+    rv, roff, rlog, rref = ofused.backward(*oargs, inp["grad_output"])
+    for got, want in ((v.grad, rv), (off.grad, roff), (lg.grad, rlog), (ref.grad, rref)):
+        assert_grad_close(host(got), want, "f32")

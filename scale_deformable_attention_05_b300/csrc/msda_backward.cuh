@@ -54,15 +54,18 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
 // lane sends one red with the summed weight a*w_c and the others send none.
 // Corners can only coincide within a pixel parity class, so each class is
 // compared across the segment with xor shuffles.
-// kPrep: the round holds offsets and softmax weights (fused entry points);
+// kRef: 0 on the plain path; 2 or 4, the width of the reference points, on the
+// fused entry points, where the round holds offsets and softmax weights;
 // the location is formed from pf's reference point first, aux.x keeps the
 // softmax weight of every sample (finite by construction), and the sample's
-// offset and box size go to woff / wwh for the reference-point gradient.
-template <int kSPG, int kStride, bool kPrep>
+// offset and box size (4-d references only) go to woffwh for the offset and
+// reference-point gradients.
+template <int kSPG, int kStride, int kRef>
 __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* wax,
                                                  float4* woffwh, const SampleFetch& f,
-                                                 const PrepFetch& pf, int ref_dim,
-                                                 int num_points, const LevelInfo* s_levels,
+                                                 const PrepFetch& pf,
+                                                 const float2* s_inv, float inv_2p,
+                                                 const LevelInfo* s_levels,
                                                  const unsigned char* s_level_of, int r0,
                                                  int lane, int dedup) {
 #pragma unroll
@@ -83,15 +86,16 @@ __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* 
             const LevelInfo lv = s_levels[l];
             const float a = f.a[h];
             float2 xy = f.xy[h];
-            if constexpr (kPrep) {
-                woffwh[sg * kStride + sj] = make_float4(xy.x, xy.y, pf.rwh[h].x, pf.rwh[h].y);
-                xy = prep_location(pf.rxy[h], pf.rwh[h], xy, ref_dim, __frcp_rn((float)lv.W),
-                                   __frcp_rn((float)lv.H), __frcp_rn((float)(2 * num_points)));
+            if constexpr (kRef != 0) {
+                if constexpr (kRef == 4)
+                    woffwh[sg * kStride + sj] = make_float4(xy.x, xy.y, pf.rwh[h].x, pf.rwh[h].y);
+                const float2 inv = s_inv[l];
+                xy = prep_location<kRef>(pf.rxy[h], pf.rwh[h], xy, inv.x, inv.y, inv_2p);
             }
             const Footprint fp = make_footprint(fmaf(xy.x, (float)lv.W, -0.5f),
                                                 fmaf(xy.y, (float)lv.H, -0.5f), lv);
             key = make_int4(fp.key[0], fp.key[1], fp.key[2], fp.key[3]);
-            aux = make_float4(fp.live || kPrep ? a : 0.f, fp.fx, fp.fy, __int_as_float(l));
+            aux = make_float4(fp.live || kRef != 0 ? a : 0.f, fp.fx, fp.fy, __int_as_float(l));
             cc = class_corners(fp, a);
             px = fp.x0 & 1;
             py = fp.y0 & 1;
@@ -142,12 +146,12 @@ __device__ __forceinline__ void load_grad_row(float (&gr)[kVPL][IO<T>::kVec],
 }
 
 // tiles_per_cta: CTA c runs tiles [c * tiles_per_cta, (c + 1) * tiles_per_cta).
-// kPrep: fused entry point -- loc holds sampling offsets, attn the attention
+// kRef != 0: fused entry point -- loc holds sampling offsets, attn the attention
 // logits, ref the reference points; grad_loc receives the offset gradient,
 // grad_attn the logit gradient (softmax Jacobian), grad_ref (fp32, may be
 // null) the reference-point gradient summed over heads and points.  Requires
 // L*P <= kSPG (every row in one round).
-template <typename T, int kLanes, int kVPL, bool kPrep>
+template <typename T, int kLanes, int kVPL, int kRef>
 __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                                   MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS > 0
                                       ? MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS
@@ -158,8 +162,9 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                     float* __restrict__ grad_value_f32, T* __restrict__ grad_loc,
                     T* __restrict__ grad_attn, int num_keys, int num_heads, int head_dim,
                     int num_levels, int num_points, int num_queries, int num_qtiles,
-                    int num_tiles, int tiles_per_cta, const T* __restrict__ ref, int ref_dim,
+                    int num_tiles, int tiles_per_cta, const T* __restrict__ ref,
                     float* __restrict__ grad_ref) {
+    constexpr bool kPrep = kRef != 0;
     using Geom = TileGeom<kLanes>;
     constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
     constexpr int V = IO<T>::kVec;
@@ -175,14 +180,17 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     __shared__ int4 s_key[MSDA_BWD_WARPS][Geom::kRecords];
     __shared__ float4 s_aw[MSDA_BWD_WARPS][Geom::kRecords];
     __shared__ float4 s_aux[MSDA_BWD_WARPS][Geom::kRecords];
-    // fused mode: per sample (offset, box size), (grad_loc, grad_a)
+    // fused mode: per sample (offset, box size) for 4-d references, (grad_loc, grad_a)
     constexpr int kPrepRecords = kPrep ? Geom::kRecords : 1;
-    __shared__ float4 s_offwh[kPrep ? MSDA_BWD_WARPS : 1][kPrepRecords];
+    constexpr int kBoxRecords = kRef == 4 ? Geom::kRecords : 1;
+    __shared__ float4 s_offwh[kRef == 4 ? MSDA_BWD_WARPS : 1][kBoxRecords];
     __shared__ float4 s_gla[kPrep ? MSDA_BWD_WARPS : 1][kPrepRecords];
+    __shared__ float2 s_inv[kPrep ? kMaxLevels : 1];  // fl(1/W), fl(1/H) per level
 
     load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, idx32,
-                     num_levels, num_points, num_keys);
+                     num_levels, num_points, num_keys, kPrep ? s_inv : nullptr);
     __syncthreads();
+    const float inv_2p = kPrep ? __frcp_rn((float)(2 * num_points)) : 0.f;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / kLanes, li = lane % kLanes;
@@ -197,7 +205,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     int4* wk = s_key[warp];
     float4* waw = s_aw[warp];
     float4* wax = s_aux[warp];
-    float4* woffwh = s_offwh[kPrep ? warp : 0];
+    float4* woffwh = s_offwh[kRef == 4 ? warp : 0];
     float4* wgla = s_gla[kPrep ? warp : 0];
 
     StepIter it;
@@ -213,18 +221,18 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     PrepFetch pf;
     TileCoord tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
     fetch_samples<T, kSPG>(f, loc, attn, tc, 0, lane, LP, num_queries, num_heads);
-    if constexpr (kPrep)
-        fetch_refs<T, kSPG>(pf, f, ref, ref_dim, tc, 0, lane, num_queries, num_levels,
-                            s_level_of);
+    PrepLane pl;
+    if constexpr (kPrep) pl = prep_lane<kSPG>(lane, num_levels, LP, kRef, s_level_of);
     float gr[kVPL][V], gnext[kVPL][V];
     load_grad_row<T, kLanes, kVPL>(gnext, grad_out, tc, g, li, nvec, num_queries, num_heads,
                                    head_dim);
 
     while (true) {
-        // ---- 1. footprints of this round (inputs fetched one round ahead)
+        // ---- 1. footprints of this round (inputs fetched, references prefetched, a round ahead)
+        if constexpr (kPrep) fetch_refs<T, kRef>(pf, f, ref, tc, num_queries, num_levels, pl);
         if constexpr (kPrep) softmax_rows<kSPG>(f);
-        backward_records<kSPG, kStride, kPrep>(wk, waw, wax, woffwh, f, pf, ref_dim, num_points,
-                                               s_levels, s_level_of, it.r0, lane, dedup);
+        backward_records<kSPG, kStride, kRef>(wk, waw, wax, woffwh, f, pf, s_inv,
+                                               inv_2p, s_levels, s_level_of, it.r0, lane, dedup);
         __syncwarp();
         const TileCoord cur = tc;
         const int r0 = it.r0;
@@ -239,9 +247,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
         if (more) {
             tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
             fetch_samples<T, kSPG>(f, loc, attn, tc, it.r0, lane, LP, num_queries, num_heads);
-            if constexpr (kPrep)
-                fetch_refs<T, kSPG>(pf, f, ref, ref_dim, tc, it.r0, lane, num_queries,
-                                    num_levels, s_level_of);
+            if constexpr (kPrep) prefetch_refs<T, kRef>(f, ref, tc, num_queries, num_levels, pl);
             if (it.r0 == 0)
                 load_grad_row<T, kLanes, kVPL>(gnext, grad_out, tc, g, li, nvec, num_queries,
                                                num_heads, head_dim);
@@ -349,11 +355,10 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                         const int rec = g * kStride + jb + s8;
                         wgla[rec] = make_float4(glx, gly, ga, 0.f);
                         float ox = a * gx, oy = a * gy;             // grad_loc / (W, H)
-                        if (ref_dim == 4) {
+                        if constexpr (kRef == 4) {
                             const float4 ow = woffwh[rec];
-                            const float two_p = (float)(2 * num_points);
-                            ox = glx * ow.z / two_p;                // grad_loc * box / (2P)
-                            oy = gly * ow.w / two_p;
+                            ox = glx * ow.z * inv_2p;               // grad_loc * box / (2P)
+                            oy = gly * ow.w * inv_2p;
                         }
                         IO<T>::store_xy(grad_loc + 2 * pt, ox, oy);
                     } else {
@@ -380,9 +385,8 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                 IO<T>::store_one(grad_attn + row * LP + jj, wax[rec].x * (wgla[rec].z - S));
             }
             if (grad_ref != nullptr && qok) {
-                const float two_p = (float)(2 * num_points);
-                for (int pi = li; pi < num_levels * ref_dim; pi += kLanes) {
-                    const int l = pi / ref_dim, c = pi - l * ref_dim;
+                for (int pi = li; pi < num_levels * kRef; pi += kLanes) {
+                    const int l = pi / kRef, c = pi - l * kRef;
                     float sum = 0.f;
                     for (int p = 0; p < num_points; ++p) {
                         const int rec = g * kStride + l * num_points + p;
@@ -392,11 +396,11 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                             sum += glc;
                         } else {
                             const float4 ow = woffwh[rec];
-                            sum += glc * ((c & 1) ? ow.y : ow.x) / two_p;
+                            sum += glc * ((c & 1) ? ow.y : ow.x) * inv_2p;
                         }
                     }
                     atomicAdd(grad_ref +
-                                  (((int64_t)cur.b * num_queries + q) * num_levels + l) * ref_dim +
+                                  (((int64_t)cur.b * num_queries + q) * num_levels + l) * kRef +
                                   c,
                               sum);
                 }

@@ -69,6 +69,9 @@ struct IO<float> {
         return __ldcs(reinterpret_cast<const float2*>(p));
     }
     __device__ __forceinline__ static float load_one(const float* p) { return __ldcs(p); }
+    __device__ __forceinline__ static float4 load_xywh(const float* p) {
+        return __ldg(reinterpret_cast<const float4*>(p));
+    }
     __device__ __forceinline__ static void store_vec(float* p, const float (&v)[kVec]) {
         __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
     }
@@ -106,6 +109,10 @@ struct IO<__nv_bfloat16> {
     __device__ __forceinline__ static float load_one(const T* p) {
         const unsigned short u = __ldcs(reinterpret_cast<const unsigned short*>(p));
         return __uint_as_float(static_cast<uint32_t>(u) << 16);
+    }
+    __device__ __forceinline__ static float4 load_xywh(const T* p) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
     }
     __device__ __forceinline__ static void store_vec(T* p, const float (&v)[kVec]) {
         uint4 t;
@@ -154,6 +161,11 @@ struct IO<__half> {
     __device__ __forceinline__ static float load_one(const T* p) {
         const unsigned short u = __ldcs(reinterpret_cast<const unsigned short*>(p));
         return __half2float(__ushort_as_half(u));
+    }
+    __device__ __forceinline__ static float4 load_xywh(const T* p) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        const float2 a = half2_bits_to_float2(u.x), b = half2_bits_to_float2(u.y);
+        return make_float4(a.x, a.y, b.x, b.y);
     }
     __device__ __forceinline__ static void store_vec(T* p, const float (&v)[kVec]) {
         uint4 t;
@@ -303,7 +315,7 @@ __device__ __forceinline__ void load_level_table(LevelInfo* s_levels, unsigned c
                                                  const void* __restrict__ spatial_shapes,
                                                  const void* __restrict__ level_start_index,
                                                  int idx32, int num_levels, int num_points,
-                                                 int num_keys) {
+                                                 int num_keys, float2* s_inv = nullptr) {
     if (threadIdx.x < num_levels) {
         const int l = threadIdx.x;
         const int64_t H = index_at(spatial_shapes, 2 * l, idx32);
@@ -317,6 +329,7 @@ __device__ __forceinline__ void load_level_table(LevelInfo* s_levels, unsigned c
         li.start = ok ? (int)s : 0;
         li.ok = ok;
         s_levels[l] = li;
+        if (s_inv) s_inv[l] = make_float2(__frcp_rn((float)li.W), __frcp_rn((float)li.H));
         if (!ok && blockIdx.x == 0) atomicOr(&g_error_word, kErrLevelOutOfRange);
     }
     const int LP = num_levels * num_points;
@@ -466,35 +479,70 @@ struct PrepFetch {
     float2 rxy[2], rwh[2];
 };
 
-template <typename T, int kSPG>
-__device__ __forceinline__ void fetch_refs(PrepFetch& pf, const SampleFetch& f,
-                                           const T* __restrict__ ref, int ref_dim,
-                                           const TileCoord& tc, int r0, int lane,
-                                           int num_queries, int num_levels,
-                                           const unsigned char* s_level_of) {
+// A fused tile is one round (L*P <= kSPG), so the level of each of a lane's
+// two samples, and the offset of its reference point inside the tile's block
+// of references, stay the same for every tile the lane visits.
+struct PrepLane {
+    int ref_off[2];  // (group * L + level) * ref_dim
+};
+
+template <int kSPG>
+__device__ __forceinline__ PrepLane prep_lane(int lane, int num_levels, int LP, int ref_dim,
+                                              const unsigned char* s_level_of) {
+    PrepLane pl;
 #pragma unroll
     for (int h = 0; h < kSamplesPerWarp / 32; ++h) {
         const int s = lane + 32 * h;
         const int sg = s / kSPG, sj = s % kSPG;
+        const int l = sj < LP ? s_level_of[sj] : 0;
+        pl.ref_off[h] = (sg * num_levels + l) * ref_dim;
+    }
+    return pl;
+}
+
+// Reference points are only prefetched into L1 one round ahead (prefetch_refs)
+// and loaded when their round starts (fetch_refs), so they are not live in
+// registers across the gather; measured faster than loading them a round ahead.
+template <typename T, int kRef>
+__device__ __forceinline__ void fetch_refs(PrepFetch& pf, const SampleFetch& f,
+                                           const T* __restrict__ ref,
+                                           const TileCoord& tc, int num_queries, int num_levels,
+                                           const PrepLane& pl) {
+    const T* rt = ref + ((int64_t)tc.b * num_queries + tc.q0) * (num_levels * kRef);
+#pragma unroll
+    for (int h = 0; h < kSamplesPerWarp / 32; ++h) {
         pf.rxy[h] = make_float2(0.f, 0.f);
         pf.rwh[h] = make_float2(0.f, 0.f);
         if (f.ok[h]) {
-            const int l = s_level_of[r0 + sj];
-            const int64_t base =
-                (((int64_t)tc.b * num_queries + tc.q0 + sg) * num_levels + l) * ref_dim;
-            pf.rxy[h] = IO<T>::load_xy(ref + base);
-            if (ref_dim == 4) pf.rwh[h] = IO<T>::load_xy(ref + base + 2);
+            if constexpr (kRef == 4) {
+                const float4 r = IO<T>::load_xywh(rt + pl.ref_off[h]);
+                pf.rxy[h] = make_float2(r.x, r.y);
+                pf.rwh[h] = make_float2(r.z, r.w);
+            } else {
+                pf.rxy[h] = IO<T>::load_xy(rt + pl.ref_off[h]);
+            }
         }
     }
+}
+
+template <typename T, int kRef>
+__device__ __forceinline__ void prefetch_refs(const SampleFetch& f, const T* __restrict__ ref,
+                                              const TileCoord& tc, int num_queries,
+                                              int num_levels, const PrepLane& pl) {
+    const T* rt = ref + ((int64_t)tc.b * num_queries + tc.q0) * (num_levels * kRef);
+#pragma unroll
+    for (int h = 0; h < kSamplesPerWarp / 32; ++h)
+        if (f.ok[h]) asm volatile("prefetch.global.L1 [%0];" ::"l"(rt + pl.ref_off[h]));
 }
 
 // Sampling location of one sample, in the binary32 operations (each rounded
 // to nearest) the oracle replays, with the reciprocals rounded once:
 //   2-d: loc = ref + off * fl(1/W)           (ref + off / (W, H))
 //   4-d: loc = ref_xy + (off * ref_wh) * fl(1/(2P))   (ref_xy + off / P * ref_wh * 0.5)
-__device__ __forceinline__ float2 prep_location(float2 rxy, float2 rwh, float2 off, int ref_dim,
+template <int kRef>
+__device__ __forceinline__ float2 prep_location(float2 rxy, float2 rwh, float2 off,
                                                 float inv_w, float inv_h, float inv_2p) {
-    if (ref_dim == 2)
+    if constexpr (kRef == 2)
         return make_float2(__fadd_rn(rxy.x, __fmul_rn(off.x, inv_w)),
                            __fadd_rn(rxy.y, __fmul_rn(off.y, inv_h)));
     return make_float2(__fadd_rn(rxy.x, __fmul_rn(__fmul_rn(off.x, rwh.x), inv_2p)),

@@ -34,12 +34,14 @@ namespace msda {
 #define MSDA_UNROLL(n) MSDA_PRAGMA(unroll n)
 
 // Stores the footprint records of the round fetched in f.
-// kPrep: the round holds offsets and softmax weights (fused entry points);
+// kRef: 0 on the plain path; 2 or 4, the width of the reference points, on the
+// fused entry points, where the round holds offsets and softmax weights;
 // the location is formed from pf's reference point first.
-template <int kSPG, int kStride, bool kPrep>
+template <int kSPG, int kStride, int kRef>
 __device__ __forceinline__ void forward_records(int4* wk, float4* ww, const SampleFetch& f,
-                                                const PrepFetch& pf, int ref_dim,
-                                                int num_points, const LevelInfo* s_levels,
+                                                const PrepFetch& pf,
+                                                const float2* s_inv, float inv_2p,
+                                                const LevelInfo* s_levels,
                                                 const unsigned char* s_level_of, int r0,
                                                 int lane) {
 #pragma unroll
@@ -52,9 +54,10 @@ __device__ __forceinline__ void forward_records(int4* wk, float4* ww, const Samp
             const LevelInfo lv = s_levels[s_level_of[r0 + sj]];
             const float a = f.a[h];
             float2 xy = f.xy[h];
-            if constexpr (kPrep)
-                xy = prep_location(pf.rxy[h], pf.rwh[h], xy, ref_dim, __frcp_rn((float)lv.W),
-                                   __frcp_rn((float)lv.H), __frcp_rn((float)(2 * num_points)));
+            if constexpr (kRef != 0) {
+                const float2 inv = s_inv[s_level_of[r0 + sj]];
+                xy = prep_location<kRef>(pf.rxy[h], pf.rwh[h], xy, inv.x, inv.y, inv_2p);
+            }
             const Footprint fp = make_footprint(fmaf(xy.x, (float)lv.W, -0.5f),
                                                 fmaf(xy.y, (float)lv.H, -0.5f), lv);
             key = make_int4(fp.key[0], fp.key[1], fp.key[2], fp.key[3]);
@@ -87,33 +90,35 @@ constexpr int forward_min_blocks(int channels_per_lane) {
 }
 
 // kVB: bytes per row vector and lane (16, or 32 with 256-bit loads).
-// kPrep: fused entry point -- loc holds sampling offsets, attn the attention
-// logits, ref the reference points (ref_dim 2 or 4); requires L*P <= kSPG.
-template <typename T, int kLanes, int kVPL, int kVB, bool kPrep>
+// kRef != 0: fused entry point -- loc holds sampling offsets, attn the attention
+// logits, ref the reference points [bs, Q, L, kRef]; requires L*P <= kSPG.
+template <typename T, int kLanes, int kVPL, int kVB, int kRef>
 __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
                                   forward_min_blocks(kVPL * kVB / (int)sizeof(T)))
     forward_kernel(const T* __restrict__ value, const void* __restrict__ spatial_shapes,
                    const void* __restrict__ level_start_index, int idx32, const T* __restrict__ loc,
                    const T* __restrict__ attn, T* __restrict__ out, int num_keys, int num_heads,
                    int head_dim, int num_levels, int num_points, int num_queries,
-                   int num_qtiles, int num_tiles, int tiles_per_cta, const T* __restrict__ ref,
-                   int ref_dim) {
+                   int num_qtiles, int num_tiles, int tiles_per_cta, const T* __restrict__ ref) {
+    constexpr bool kPrep = kRef != 0;
     using Geom = TileGeom<kLanes>;
     using VIO = VecIO<T, kVB>;
     constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
     constexpr int V = VIO::kVec;
     __shared__ LevelInfo s_levels[kMaxLevels];
     __shared__ unsigned char s_level_of[kMaxLevelPoints];
+    __shared__ float2 s_inv[kPrep ? kMaxLevels : 1];  // fl(1/W), fl(1/H) per level
     constexpr int kWarps = MSDA_FWD_WARPS;
     __shared__ int4 s_key[kWarps][Geom::kRecords];
     __shared__ float4 s_w[kWarps][Geom::kRecords];
 
     load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, idx32,
-                     num_levels, num_points, num_keys);
+                     num_levels, num_points, num_keys, kPrep ? s_inv : nullptr);
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / kLanes, li = lane % kLanes;
+    const float inv_2p = kPrep ? __frcp_rn((float)(2 * num_points)) : 0.f;
     const int LP = num_levels * num_points;
     const int nvec = head_dim / V;
     const unsigned row_bytes = (unsigned)(num_heads * head_dim) * (unsigned)sizeof(T);
@@ -133,9 +138,8 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
     PrepFetch pf;
     TileCoord tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
     fetch_samples<T, kSPG>(f, loc, attn, tc, 0, lane, LP, num_queries, num_heads);
-    if constexpr (kPrep)
-        fetch_refs<T, kSPG>(pf, f, ref, ref_dim, tc, 0, lane, num_queries, num_levels,
-                            s_level_of);
+    PrepLane pl;
+    if constexpr (kPrep) pl = prep_lane<kSPG>(lane, num_levels, LP, kRef, s_level_of);
     float acc[kVPL][V];
 #pragma unroll
     for (int k = 0; k < kVPL; ++k)
@@ -143,9 +147,10 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
         for (int e = 0; e < V; ++e) acc[k][e] = 0.f;
 
     while (true) {
-        // ---- 1. footprints of this round (inputs fetched one round ahead)
+        // ---- 1. footprints of this round (inputs fetched, references prefetched, a round ahead)
+        if constexpr (kPrep) fetch_refs<T, kRef>(pf, f, ref, tc, num_queries, num_levels, pl);
         if constexpr (kPrep) softmax_rows<kSPG>(f);
-        forward_records<kSPG, kStride, kPrep>(wk, ww, f, pf, ref_dim, num_points, s_levels,
+        forward_records<kSPG, kStride, kRef>(wk, ww, f, pf, s_inv, inv_2p, s_levels,
                                               s_level_of, it.r0, lane);
         __syncwarp();
         const TileCoord cur = tc;
@@ -156,9 +161,7 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
         if (more) {
             tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
             fetch_samples<T, kSPG>(f, loc, attn, tc, it.r0, lane, LP, num_queries, num_heads);
-            if constexpr (kPrep)
-                fetch_refs<T, kSPG>(pf, f, ref, ref_dim, tc, it.r0, lane, num_queries,
-                                    num_levels, s_level_of);
+            if constexpr (kPrep) prefetch_refs<T, kRef>(f, ref, tc, num_queries, num_levels, pl);
         }
 
         // ---- 2. gather: group g walks its query's samples

@@ -137,25 +137,24 @@ TileGrid tile_grid(const Problem& pb, int queries_per_tile, int resident, int wa
     return tg;
 }
 
-template <typename T, int kLanes, int kVPL, int kVB, bool kPrep = false>
+template <typename T, int kLanes, int kVPL, int kVB, int kRef = 0>
 cudaError_t launch_forward_t(const Problem& pb, void* out, cudaStream_t st) {
-    auto kernel = forward_kernel<T, kLanes, kVPL, kVB, kPrep>;
+    auto kernel = forward_kernel<T, kLanes, kVPL, kVB, kRef>;
     constexpr int kThreads = MSDA_FWD_WARPS * 32;
     const TileGrid tg =
         tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_FWD_WARPS);
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<T*>(out), pb.K, pb.M, pb.D, pb.L, pb.P, pb.Q,
-        tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta, static_cast<const T*>(pb.ref),
-        pb.ref_dim);
+        tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta, static_cast<const T*>(pb.ref));
     return cudaGetLastError();
 }
 
-template <typename T, int kLanes, int kVPL, bool kPrep = false>
+template <typename T, int kLanes, int kVPL, int kRef = 0>
 cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv32,
                               void* grad_loc, void* grad_attn, cudaStream_t st,
                               float* grad_ref = nullptr) {
-    auto kernel = backward_kernel<T, kLanes, kVPL, kPrep>;
+    auto kernel = backward_kernel<T, kLanes, kVPL, kRef>;
     constexpr int kThreads = MSDA_BWD_WARPS * 32;
     const TileGrid tg =
         tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS);
@@ -164,7 +163,7 @@ cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
         static_cast<T*>(grad_loc), static_cast<T*>(grad_attn), pb.K, pb.M, pb.D, pb.L, pb.P,
         pb.Q, tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta, static_cast<const T*>(pb.ref),
-        pb.ref_dim, grad_ref);
+        grad_ref);
     return cudaGetLastError();
 }
 
@@ -211,19 +210,25 @@ Layout fused_layout(const Problem& pb, int nvec, int min_lanes) {
     return ly;
 }
 
-template <typename T>
-cudaError_t dispatch_forward_fused(const Problem& pb, void* out, cudaStream_t st) {
+template <typename T, int kRef>
+cudaError_t dispatch_forward_fused_ref(const Problem& pb, void* out, cudaStream_t st) {
     const Layout ly = fused_layout(pb, pb.D / IO<T>::kVec, 4);
     if (ly.vpl == 1) {
         switch (ly.lanes) {
-            case 4: return launch_forward_t<T, 4, 1, 16, true>(pb, out, st);
-            case 8: return launch_forward_t<T, 8, 1, 16, true>(pb, out, st);
-            case 16: return launch_forward_t<T, 16, 1, 16, true>(pb, out, st);
-            default: return launch_forward_t<T, 32, 1, 16, true>(pb, out, st);
+            case 4: return launch_forward_t<T, 4, 1, 16, kRef>(pb, out, st);
+            case 8: return launch_forward_t<T, 8, 1, 16, kRef>(pb, out, st);
+            case 16: return launch_forward_t<T, 16, 1, 16, kRef>(pb, out, st);
+            default: return launch_forward_t<T, 32, 1, 16, kRef>(pb, out, st);
         }
     }
-    if (ly.vpl == 2) return launch_forward_t<T, 32, 2, 16, true>(pb, out, st);
-    return launch_forward_t<T, 32, 4, 16, true>(pb, out, st);
+    if (ly.vpl == 2) return launch_forward_t<T, 32, 2, 16, kRef>(pb, out, st);
+    return launch_forward_t<T, 32, 4, 16, kRef>(pb, out, st);
+}
+
+template <typename T>
+cudaError_t dispatch_forward_fused(const Problem& pb, void* out, cudaStream_t st) {
+    return pb.ref_dim == 4 ? dispatch_forward_fused_ref<T, 4>(pb, out, st)
+                           : dispatch_forward_fused_ref<T, 2>(pb, out, st);
 }
 
 template <typename T>
@@ -252,19 +257,26 @@ cudaError_t launch_backward_merge_t(const Problem& pb, int log2_points, const vo
     return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t dispatch_backward_fused(const Problem& pb, const void* g, float* gv32, void* gl,
-                                    void* ga, cudaStream_t st, float* gref) {
+template <typename T, int kRef>
+cudaError_t dispatch_backward_fused_ref(const Problem& pb, const void* g, float* gv32, void* gl,
+                                        void* ga, cudaStream_t st, float* gref) {
     const Layout ly = fused_layout(pb, pb.D / IO<T>::kVec, 8);
     if (ly.vpl == 1) {
         switch (ly.lanes) {
-            case 8: return launch_backward_t<T, 8, 1, true>(pb, g, gv32, gl, ga, st, gref);
-            case 16: return launch_backward_t<T, 16, 1, true>(pb, g, gv32, gl, ga, st, gref);
-            default: return launch_backward_t<T, 32, 1, true>(pb, g, gv32, gl, ga, st, gref);
+            case 8: return launch_backward_t<T, 8, 1, kRef>(pb, g, gv32, gl, ga, st, gref);
+            case 16: return launch_backward_t<T, 16, 1, kRef>(pb, g, gv32, gl, ga, st, gref);
+            default: return launch_backward_t<T, 32, 1, kRef>(pb, g, gv32, gl, ga, st, gref);
         }
     }
-    if (ly.vpl == 2) return launch_backward_t<T, 32, 2, true>(pb, g, gv32, gl, ga, st, gref);
-    return launch_backward_t<T, 32, 4, true>(pb, g, gv32, gl, ga, st, gref);
+    if (ly.vpl == 2) return launch_backward_t<T, 32, 2, kRef>(pb, g, gv32, gl, ga, st, gref);
+    return launch_backward_t<T, 32, 4, kRef>(pb, g, gv32, gl, ga, st, gref);
+}
+
+template <typename T>
+cudaError_t dispatch_backward_fused(const Problem& pb, const void* g, float* gv32, void* gl,
+                                    void* ga, cudaStream_t st, float* gref) {
+    return pb.ref_dim == 4 ? dispatch_backward_fused_ref<T, 4>(pb, g, gv32, gl, ga, st, gref)
+                           : dispatch_backward_fused_ref<T, 2>(pb, g, gv32, gl, ga, st, gref);
 }
 
 template <typename T>

@@ -10,7 +10,11 @@ steps of ``MSDeformAttn.forward`` in the Deformable DETR walk-through
      (the walk-through's ``offset_normalizer = stack([W, H])``);
    * 4-d references (two-stage / box refinement, walk-through "2.4"):
      loc = ref[b,q,l,:2] + off[b,q,m,l,p,:] / P * ref[b,q,l,2:] * 0.5;
-3. the core op (O1) on those locations and weights.
+3. the core op (O1) on those locations and weights;
+4. optional key padding mask: the walk-through's ``value.masked_fill(
+   input_padding_mask[..., None], 0)`` -- every head's value row of a padded
+   key (b, k) is zero before sampling, so those rows contribute nothing and,
+   through the masked_fill, receive no gradient.
 
 The locations decide which pixels are read, so they are formed in the same
 binary32 operations, in the same order, as the CUDA kernels take them (the
@@ -63,28 +67,50 @@ def locations(reference_points: np.ndarray, sampling_offsets: np.ndarray,
     raise ValueError("reference_points must end in 2 or 4")
 
 
+def keep_rows(value: np.ndarray, padding_mask) -> np.ndarray:
+    """[bs, K, 1, 1] factor: 0 for padded keys (mask true), 1 elsewhere."""
+    bs, K = np.asarray(value).shape[:2]
+    if padding_mask is None:
+        return np.ones((bs, K, 1, 1))
+    m = np.asarray(padding_mask).astype(bool)
+    if m.shape != (bs, K):
+        raise ValueError(f"padding_mask must be [bs, num_keys] = {(bs, K)}, got {m.shape}")
+    return (~m).astype(np.float64)[:, :, None, None]
+
+
+def masked_fill_grad(grad_value: np.ndarray, keep: np.ndarray) -> np.ndarray:
+    """Gradient through masked_fill: padded rows receive none."""
+    return grad_value * keep
+
+
 def forward(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
-            attention_logits, exact: bool = False, threads: int = 0) -> np.ndarray:
+            attention_logits, exact: bool = False, threads: int = 0,
+            padding_mask=None) -> np.ndarray:
     """Output [bs, Q, M*D] in fp64."""
     off = np.asarray(sampling_offsets)
     L, P = off.shape[3], off.shape[4]
     a = softmax_weights(attention_logits, L, P)
     loc = locations(reference_points, sampling_offsets, spatial_shapes, exact)
-    return core_forward(value, spatial_shapes, level_start_index, loc, a, exact_coords=exact,
+    v = np.asarray(value, np.float64) * keep_rows(value, padding_mask)
+    return core_forward(v, spatial_shapes, level_start_index, loc, a, exact_coords=exact,
                         threads=threads)
 
 
 def backward(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
-             attention_logits, grad_output, exact: bool = False, threads: int = 0
-             ) -> Tuple[np.ndarray, np.ndarray, np.ndarray, np.ndarray]:
-    """(grad_value, grad_sampling_offsets, grad_attention_logits, grad_reference_points), fp64."""
+             attention_logits, grad_output, exact: bool = False, threads: int = 0,
+             padding_mask=None) -> Tuple[np.ndarray, np.ndarray, np.ndarray, np.ndarray]:
+    """(grad_value, grad_sampling_offsets, grad_attention_logits, grad_reference_points), fp64.
+    grad_value is the gradient with respect to the value before the padding mask."""
     ref = np.asarray(reference_points, np.float64)
     off = np.asarray(sampling_offsets, np.float64)
     bs, Q, M, L, P, _ = off.shape
     a = softmax_weights(attention_logits, L, P)
     loc = locations(reference_points, sampling_offsets, spatial_shapes, exact)
-    gv, gl, ga = core_backward(value, spatial_shapes, level_start_index, loc, a, grad_output,
-                               exact_coords=exact, threads=threads)
+    keep = keep_rows(value, padding_mask)
+    gv, gl, ga = core_backward(np.asarray(value, np.float64) * keep, spatial_shapes,
+                               level_start_index, loc, a, grad_output, exact_coords=exact,
+                               threads=threads)
+    gv = masked_fill_grad(gv, keep)
     ga = ga.reshape(bs, Q, M, L * P)
     af = a.reshape(bs, Q, M, L * P)
     g_logits = af * (ga - (af * ga).sum(axis=-1, keepdims=True))

@@ -41,6 +41,7 @@ __all__ = [
     "f32_to_f16_bits",
     "f16_bits_to_f32",
     "make_inputs",
+    "padding_mask",
     "make_fused_inputs",
     "random_workload",
 ]
@@ -344,6 +345,29 @@ def make_fused_inputs(wl: Workload, ref_dim: int = 2, offset_sigma: float = 2.0
         else:
             out[k] = a
     return out
+
+
+def padding_mask(wl: Workload, min_ratio: float = 0.6) -> np.ndarray:
+    """Seeded key padding mask [bs, num_keys] (bool, True = padded) shaped like
+    the masks of a padded image batch: image b keeps the top-left
+    ceil(rh_b * H_l) x ceil(rw_b * W_l) pixels of every level, with (rh_b, rw_b)
+    ~ U[min_ratio, 1]^2 and image 0 unpadded (the batch is padded to it).  Drawn
+    from its own stream (seed + 70000), so the other inputs do not change."""
+    rng = np.random.default_rng(wl.seed + 70000)
+    ratios = rng.uniform(min_ratio, 1.0, (wl.bs, 2))
+    ratios[0] = 1.0
+    mask = np.zeros((wl.bs, wl.num_keys), dtype=bool)
+    start = 0
+    for H, W in wl.spatial_shapes:
+        for b in range(wl.bs):
+            vh = int(np.ceil(ratios[b, 0] * H))
+            vw = int(np.ceil(ratios[b, 1] * W))
+            m = np.zeros((H, W), dtype=bool)
+            m[vh:, :] = True
+            m[:, vw:] = True
+            mask[b, start:start + H * W] = m.reshape(-1)
+        start += H * W
+    return mask
 
 
 def random_workload(seed: int, bs: int, spatial_shapes, num_heads: int, head_dim: int,

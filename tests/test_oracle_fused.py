@@ -139,6 +139,44 @@ def test_backward_matches_central_differences(ref_dim):
     assert checked >= 10
 
 
+def _mask_problem():
+    """Hand-built case: one 8x16 level, one head and point (softmax weight 1),
+    value == c everywhere.  Query 0 sits on the centre of pixel (5, 3); query 1
+    half-way between pixels (9, 2) and (10, 2).  Batch 1 pads pixels (5, 3) and
+    (10, 2); batch 0 pads nothing."""
+    H, W, D, c = 8, 16, 4, 3.0
+    shapes = np.array([[H, W]])
+    lsi = np.array([0])
+    value = np.full((2, H * W, 1, D), c)
+    ref = np.array([[(5.5 / W, 3.5 / H), (10.0 / W, 2.5 / H)]] * 2, np.float32)[:, :, None, :]
+    off = np.zeros((2, 2, 1, 1, 1, 2), np.float32)
+    logits = np.zeros((2, 2, 1, 1), np.float32)
+    mask = np.zeros((2, H * W), bool)
+    mask[1, 3 * W + 5] = mask[1, 2 * W + 10] = True
+    g = np.random.default_rng(21).standard_normal((2, 2, D))
+    return value, shapes, lsi, ref, off, logits, mask, g, c, W
+
+
+def test_padding_mask_closed_form():
+    value, sh, lsi, ref, off, logits, mask, g, c, W = _mask_problem()
+    out = fused.forward(value, sh, lsi, ref, off, logits, padding_mask=mask)
+    want = np.array([[c, c], [0.0, 0.5 * c]])[:, :, None] * np.ones(g.shape[-1])
+    np.testing.assert_array_equal(out, want)
+    gv, goff, glog, gref = fused.backward(value, sh, lsi, ref, off, logits, g, padding_mask=mask)
+    gv_want = np.zeros_like(value)
+    gv_want[0, 3 * W + 5, 0] = g[0, 0]
+    gv_want[0, 2 * W + 9, 0] = gv_want[0, 2 * W + 10, 0] = 0.5 * g[0, 1]
+    gv_want[1, 2 * W + 9, 0] = 0.5 * g[1, 1]                  # the padded neighbour gets nothing
+    np.testing.assert_allclose(gv, gv_want, rtol=0, atol=1e-15)
+    # d out / d x_im between a value-c pixel and a padded (zero) one is -c; offsets are in pixels
+    np.testing.assert_allclose(goff[1, 1, 0, 0, 0, 0], -c * g[1, 1].sum(), rtol=1e-12)
+    np.testing.assert_allclose(goff[0, 1, 0, 0, 0, 0], 0.0, atol=1e-12)
+    # an all-false mask is no mask
+    np.testing.assert_array_equal(
+        fused.forward(value, sh, lsi, ref, off, logits, padding_mask=np.zeros_like(mask)),
+        fused.forward(value, sh, lsi, ref, off, logits))
+
+
 # ------------------------------------------------ planted mistakes must be caught
 def _mutant_locations_swapped(ref, off, shapes, exact=False):
     sh = np.asarray(shapes)[:, ::-1]                      # (H, W) rows read as (W, H)
@@ -158,7 +196,17 @@ def _mutant_softmax_wrong_axis(logits, L, P):
     return (e / e.sum(axis=2, keepdims=True)).reshape(*z.shape[:-1], L, P)   # over heads
 
 
+def _mutant_mask_batch_flipped(value, padding_mask):
+    m = None if padding_mask is None else np.asarray(padding_mask)[::-1]
+    return _ORIG_KEEP(value, m)
+
+
+def _mutant_mask_grad_kept(grad_value, keep):
+    return grad_value                                     # padded rows keep their gradient
+
+
 _ORIG_LOCATIONS = fused.locations
+_ORIG_KEEP = fused.keep_rows
 
 
 def _battery():
@@ -171,6 +219,7 @@ def _battery():
         test_four_d_references_with_matching_box_equal_the_two_d_form()
         for rd in (2, 4):
             test_backward_matches_central_differences(rd)
+        test_padding_mask_closed_form()
     except AssertionError:
         return False
     return True
@@ -180,6 +229,8 @@ def _battery():
     ("normaliser_transposed", "locations", _mutant_locations_swapped),
     ("box_half_dropped", "locations", _mutant_locations_no_half),
     ("softmax_over_heads", "softmax_weights", _mutant_softmax_wrong_axis),
+    ("mask_batch_flipped", "keep_rows", _mutant_mask_batch_flipped),
+    ("mask_gradient_kept", "masked_fill_grad", _mutant_mask_grad_kept),
 ])
 def test_fused_mutant_is_caught(monkeypatch, name, attr, mutant):
     assert _battery()

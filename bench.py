@@ -292,8 +292,10 @@ def run_native(args, wl):
 
     def run_backward(accumulate):
         if fused:     # the encoder's reference points are constants: no reference gradient
-            B.msda_backward_fused(*args_fwd, d["grad_output"], gv, gl, gw, reference_grad=False,
-                                  workspace=workspace, accumulate=accumulate, stream=stream)
+            B.msda_backward_fused(*args_fwd, d["grad_output"], grad_value=gv,
+                                  grad_sampling_offsets=gl, grad_attn_logits=gw,
+                                  reference_grad=False, workspace=workspace,
+                                  accumulate=accumulate, stream=stream)
         else:
             B.msda_backward(*args_fwd, d["grad_output"], gv, gl, gw, workspace=workspace,
                             accumulate=accumulate, stream=stream)

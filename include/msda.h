@@ -165,17 +165,24 @@ MSDA_API int msda_backward(const void* value, const void* spatial_shapes,
  *   ref_dim 4: loc = ref_xy + off / num_points * ref_wh * 0.5
  * in binary32, each operation rounded to nearest, with the reciprocals rounded
  * once: fl(ref + fl(off * fl(1/W))) and fl(ref_xy + fl(fl(off * w) *
- * fl(1/(2*num_points)))), then the same sum as msda_forward.  num_levels*num_points must not exceed
- * MSDA_MAX_FUSED_LEVEL_POINTS (else MSDA_ERR_UNSUPPORTED), ref_dim must be 2 or
- * 4.  Saves the caller's softmax and location kernels and their
- * [bs, Q, M, L, P, 3] round trip through memory.  One kernel launch.
+ * fl(1/(2*num_points)))), then the same sum as msda_forward.
+ *   key_padding_mask  [bs, num_keys] bytes (a torch.bool tensor), nonzero =
+ *                     padded key, or NULL.  The module's masked_fill of value
+ *                     (walk-through, "2.2.4", MSDeformAttn.forward) fused into
+ *                     the value load: every head's row of a padded key reads
+ *                     as zero.  Any byte alignment.
+ * num_levels*num_points must not exceed MSDA_MAX_FUSED_LEVEL_POINTS (else
+ * MSDA_ERR_UNSUPPORTED), ref_dim must be 2 or 4.  Saves the caller's softmax,
+ * location and masking kernels and their round trips through memory.  One
+ * kernel launch.
  */
 MSDA_API int msda_forward_fused(const void* value, const void* spatial_shapes,
                                 const void* level_start_index, const void* reference_points,
                                 const void* sampling_offsets, const void* attn_logits,
-                                void* output, int bs, int num_keys, int num_heads, int head_dim,
-                                int num_levels, int num_points, int num_queries, int ref_dim,
-                                int dtype, void* stream);
+                                const void* key_padding_mask, void* output, int bs,
+                                int num_keys, int num_heads, int head_dim, int num_levels,
+                                int num_points, int num_queries, int ref_dim, int dtype,
+                                void* stream);
 
 /*
  * Backward of msda_forward_fused: grad_value (as msda_backward, same
@@ -184,13 +191,16 @@ MSDA_API int msda_forward_fused(const void* value, const void* spatial_shapes,
  * per row), and, when grad_reference_points is not NULL, the gradient of the
  * reference points summed over heads and points into that fp32
  * [bs, num_queries, num_levels, ref_dim] buffer (16-byte aligned, overwritten).
- * Launches: zero-fills, one gather / scatter kernel, and for half types the
- * finalize kernel.
+ * With key_padding_mask, grad_value is the gradient with respect to the value
+ * before masking: padded rows receive none (zero, or unchanged when
+ * accumulating).  Launches: zero-fills, one gather / scatter kernel, and for
+ * half types the finalize kernel.
  */
 MSDA_API int msda_backward_fused(const void* value, const void* spatial_shapes,
                                  const void* level_start_index, const void* reference_points,
                                  const void* sampling_offsets, const void* attn_logits,
-                                 const void* grad_output, void* grad_value,
+                                 const void* key_padding_mask, const void* grad_output,
+                                 void* grad_value,
                                  void* grad_sampling_offsets, void* grad_attn_logits,
                                  float* grad_reference_points, void* workspace,
                                  size_t workspace_bytes, int bs, int num_keys, int num_heads,

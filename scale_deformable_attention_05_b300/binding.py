@@ -73,9 +73,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msda_version.restype = _int
     lib.msda_backward_noalloc.argtypes = [_vp] * 9 + _DIMS + [_int, ctypes.c_uint, _vp]
     lib.msda_backward_noalloc.restype = _int
-    lib.msda_forward_fused.argtypes = [_vp] * 7 + _DIMS + [_int, _int, _vp]
+    lib.msda_forward_fused.argtypes = [_vp] * 8 + _DIMS + [_int, _int, _vp]
     lib.msda_forward_fused.restype = _int
-    lib.msda_backward_fused.argtypes = ([_vp] * 12 + [ctypes.c_size_t] + _DIMS +
+    lib.msda_backward_fused.argtypes = ([_vp] * 13 + [ctypes.c_size_t] + _DIMS +
                                         [_int, _int, ctypes.c_uint, _vp])
     lib.msda_backward_fused.restype = _int
     return lib
@@ -223,10 +223,23 @@ def _fused_dims(value, spatial_shapes, reference_points, sampling_offsets, attn_
     return bs, K, M, D, L, P, Q, ref_dim
 
 
+def _mask(key_padding_mask: Optional[torch.Tensor], bs: int, K: int) -> Optional[torch.Tensor]:
+    """The [bs, K] key padding mask as one byte per key (True / nonzero = padded)."""
+    if key_padding_mask is None:
+        return None
+    if tuple(key_padding_mask.shape) != (bs, K):
+        raise ValueError(f"key_padding_mask must be [bs, num_keys] = {(bs, K)}")
+    if key_padding_mask.dtype not in (torch.bool, torch.uint8):
+        raise TypeError("key_padding_mask must be torch.bool or torch.uint8")
+    return key_padding_mask.contiguous()
+
+
 def msda_forward_fused(value, spatial_shapes, level_start_index, reference_points,
-                       sampling_offsets, attn_logits, output=None, stream=None) -> torch.Tensor:
-    """output [bs, Q, M*D]: softmax of the logits and locations from the reference
-    points and offsets, then the operator, in one kernel (see include/msda.h)."""
+                       sampling_offsets, attn_logits, key_padding_mask=None, output=None,
+                       stream=None) -> torch.Tensor:
+    """output [bs, Q, M*D]: softmax of the logits, locations from the reference
+    points and offsets, and the optional key padding mask applied to value, then
+    the operator, in one kernel (see include/msda.h)."""
     bs, K, M, D, L, P, Q, ref_dim = _fused_dims(value, spatial_shapes, reference_points,
                                                 sampling_offsets, attn_logits)
     code = _dtype_code(value, spatial_shapes)
@@ -234,18 +247,20 @@ def msda_forward_fused(value, spatial_shapes, level_start_index, reference_point
         output = torch.empty((bs, Q, M * D), dtype=value.dtype, device=value.device)
     _check("msda_forward_fused", _LIB.msda_forward_fused(
         _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index, spatial_shapes)),
-        _ptr(reference_points), _ptr(sampling_offsets), _ptr(attn_logits), _ptr(output),
+        _ptr(reference_points), _ptr(sampling_offsets), _ptr(attn_logits),
+        _ptr(_mask(key_padding_mask, bs, K)), _ptr(output),
         bs, K, M, D, L, P, Q, ref_dim, code, _stream(stream)))
     return output
 
 
 def msda_backward_fused(value, spatial_shapes, level_start_index, reference_points,
-                        sampling_offsets, attn_logits, grad_output, grad_value=None,
-                        grad_sampling_offsets=None, grad_attn_logits=None,
+                        sampling_offsets, attn_logits, grad_output, key_padding_mask=None,
+                        grad_value=None, grad_sampling_offsets=None, grad_attn_logits=None,
                         reference_grad: bool = True, workspace: Optional[torch.Tensor] = None,
                         accumulate: bool = False, stream=None):
     """(grad_value, grad_sampling_offsets, grad_attn_logits, grad_reference_points or None);
-    the reference-point gradient is an fp32 tensor [bs, Q, L, ref_dim]."""
+    the reference-point gradient is an fp32 tensor [bs, Q, L, ref_dim].  With a key
+    padding mask, grad_value is taken with respect to the value before masking."""
     bs, K, M, D, L, P, Q, ref_dim = _fused_dims(value, spatial_shapes, reference_points,
                                                 sampling_offsets, attn_logits)
     code = _dtype_code(value, spatial_shapes)
@@ -264,7 +279,8 @@ def msda_backward_fused(value, spatial_shapes, level_start_index, reference_poin
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("msda_backward_fused", _LIB.msda_backward_fused(
         _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index, spatial_shapes)),
-        _ptr(reference_points), _ptr(sampling_offsets), _ptr(attn_logits), _ptr(grad_output),
+        _ptr(reference_points), _ptr(sampling_offsets), _ptr(attn_logits),
+        _ptr(_mask(key_padding_mask, bs, K)), _ptr(grad_output),
         _ptr(grad_value), _ptr(grad_sampling_offsets), _ptr(grad_attn_logits), _ptr(grad_ref),
         _ptr(workspace) if workspace is not None else None, ws_bytes,
         bs, K, M, D, L, P, Q, ref_dim, code, MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0,
@@ -324,35 +340,37 @@ class MSDeformAttnFunction(torch.autograd.Function):
 
 class MSDeformAttnFusedFunction(torch.autograd.Function):
     """Autograd wrapper of the fused entry points: (value, spatial_shapes,
-    level_start_index, reference_points, sampling_offsets, attn_logits) ->
-    output; backward returns gradients for value, reference_points (when it
-    requires grad), sampling_offsets and attn_logits."""
+    level_start_index, reference_points, sampling_offsets, attn_logits,
+    key_padding_mask or None) -> output; backward returns gradients for value
+    (before masking), reference_points (when it requires grad),
+    sampling_offsets and attn_logits."""
 
     @staticmethod
     def forward(ctx, value, spatial_shapes, level_start_index, reference_points,
-                sampling_offsets, attn_logits):
+                sampling_offsets, attn_logits, key_padding_mask=None):
         value, reference_points = value.contiguous(), reference_points.contiguous()
         sampling_offsets, attn_logits = sampling_offsets.contiguous(), attn_logits.contiguous()
         out = msda_forward_fused(value, spatial_shapes, level_start_index, reference_points,
-                                 sampling_offsets, attn_logits)
+                                 sampling_offsets, attn_logits, key_padding_mask)
         ctx.save_for_backward(value, spatial_shapes, level_start_index, reference_points,
-                              sampling_offsets, attn_logits)
+                              sampling_offsets, attn_logits, key_padding_mask)
         return out
 
     @staticmethod
     def backward(ctx, grad_output):
-        value, shapes, lsi, ref, off, logits = ctx.saved_tensors
+        value, shapes, lsi, ref, off, logits, mask = ctx.saved_tensors
         need_ref = ctx.needs_input_grad[3]
         gv, goff, glog, gref = msda_backward_fused(value, shapes, lsi, ref, off, logits,
-                                                   grad_output.contiguous(),
+                                                   grad_output.contiguous(), mask,
                                                    reference_grad=need_ref)
-        return gv, None, None, (gref.to(ref.dtype) if need_ref else None), goff, glog
+        return gv, None, None, (gref.to(ref.dtype) if need_ref else None), goff, glog, None
 
 
 def ms_deform_attn_fused(value, spatial_shapes, level_start_index, reference_points,
-                         sampling_offsets, attn_logits):
+                         sampling_offsets, attn_logits, key_padding_mask=None):
     return MSDeformAttnFusedFunction.apply(value, spatial_shapes, level_start_index,
-                                           reference_points, sampling_offsets, attn_logits)
+                                           reference_points, sampling_offsets, attn_logits,
+                                           key_padding_mask)
 
 
 def ms_deform_attn(value, spatial_shapes, level_start_index, sampling_loc, attn_weight):

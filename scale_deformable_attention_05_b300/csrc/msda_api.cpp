@@ -108,7 +108,8 @@ namespace {
 // sampling_loc / attn_weight are offsets and logits, ref the reference points).
 int forward_impl(const void* value, const void* spatial_shapes, const void* level_start_index,
                  const void* sampling_loc, const void* attn_weight, const void* ref,
-                 int ref_dim, void* output, const Dims& d, int dtype, void* stream) {
+                 int ref_dim, const void* mask, void* output, const Dims& d, int dtype,
+                 void* stream) {
     MSDA_TRY(check_dims(d, dtype));
     if (ref_dim != 0) MSDA_TRY(check_fused(d, ref_dim));
     MSDA_TRY(check_ptr(output, d.out_elems()));
@@ -129,6 +130,7 @@ int forward_impl(const void* value, const void* spatial_shapes, const void* leve
                      index32(dtype)};
     pb.ref = ref;
     pb.ref_dim = ref_dim;
+    pb.mask = static_cast<const unsigned char*>(mask);
     return cuda_status(msda::launch_forward(pb, output, value_type(dtype), st));
 }
 
@@ -136,7 +138,8 @@ int forward_impl(const void* value, const void* spatial_shapes, const void* leve
 // grad_ref (fused only, fp32, may be null) is zero-filled and accumulated.
 int backward_impl(const void* value, const void* spatial_shapes, const void* level_start_index,
                   const void* sampling_loc, const void* attn_weight, const void* ref, int ref_dim,
-                  const void* grad_output, void* grad_value, void* grad_sampling_loc,
+                  const void* mask, const void* grad_output, void* grad_value,
+                  void* grad_sampling_loc,
                   void* grad_attn_weight, float* grad_ref, void* workspace,
                   size_t workspace_bytes, const Dims& d, int dtype, unsigned flags,
                   void* stream) {
@@ -181,6 +184,7 @@ int backward_impl(const void* value, const void* spatial_shapes, const void* lev
                      index32(dtype)};
     pb.ref = ref;
     pb.ref_dim = ref_dim;
+    pb.mask = static_cast<const unsigned char*>(mask);
     const int vt = value_type(dtype);
     float* gv32;
     if (vt == MSDA_F32) {
@@ -209,18 +213,19 @@ int msda_forward(const void* value, const void* spatial_shapes,
                  void* stream) {
     const Dims d{bs, num_keys, num_heads, head_dim, num_levels, num_points, num_queries};
     return forward_impl(value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
-                        nullptr, 0, output, d, dtype, stream);
+                        nullptr, 0, nullptr, output, d, dtype, stream);
 }
 
 int msda_forward_fused(const void* value, const void* spatial_shapes,
                        const void* level_start_index, const void* reference_points,
-                       const void* sampling_offsets, const void* attn_logits, void* output,
-                       int bs, int num_keys, int num_heads, int head_dim, int num_levels,
-                       int num_points, int num_queries, int ref_dim, int dtype, void* stream) {
+                       const void* sampling_offsets, const void* attn_logits,
+                       const void* key_padding_mask, void* output, int bs, int num_keys,
+                       int num_heads, int head_dim, int num_levels, int num_points,
+                       int num_queries, int ref_dim, int dtype, void* stream) {
     const Dims d{bs, num_keys, num_heads, head_dim, num_levels, num_points, num_queries};
     if (ref_dim != 2 && ref_dim != 4) return MSDA_ERR_UNSUPPORTED;
     return forward_impl(value, spatial_shapes, level_start_index, sampling_offsets, attn_logits,
-                        reference_points, ref_dim, output, d, dtype, stream);
+                        reference_points, ref_dim, key_padding_mask, output, d, dtype, stream);
 }
 
 size_t msda_backward_workspace_bytes(int bs, int num_keys, int num_heads, int head_dim,
@@ -239,7 +244,7 @@ int msda_backward(const void* value, const void* spatial_shapes,
                   void* stream) {
     const Dims d{bs, num_keys, num_heads, head_dim, num_levels, num_points, num_queries};
     return backward_impl(value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
-                         nullptr, 0, grad_output, grad_value, grad_sampling_loc,
+                         nullptr, 0, nullptr, grad_output, grad_value, grad_sampling_loc,
                          grad_attn_weight, nullptr, workspace, workspace_bytes, d, dtype, flags,
                          stream);
 }
@@ -247,7 +252,8 @@ int msda_backward(const void* value, const void* spatial_shapes,
 int msda_backward_fused(const void* value, const void* spatial_shapes,
                         const void* level_start_index, const void* reference_points,
                         const void* sampling_offsets, const void* attn_logits,
-                        const void* grad_output, void* grad_value, void* grad_sampling_offsets,
+                        const void* key_padding_mask, const void* grad_output, void* grad_value,
+                        void* grad_sampling_offsets,
                         void* grad_attn_logits, float* grad_reference_points, void* workspace,
                         size_t workspace_bytes, int bs, int num_keys, int num_heads,
                         int head_dim, int num_levels, int num_points, int num_queries,
@@ -255,7 +261,8 @@ int msda_backward_fused(const void* value, const void* spatial_shapes,
     const Dims d{bs, num_keys, num_heads, head_dim, num_levels, num_points, num_queries};
     if (ref_dim != 2 && ref_dim != 4) return MSDA_ERR_UNSUPPORTED;
     return backward_impl(value, spatial_shapes, level_start_index, sampling_offsets,
-                         attn_logits, reference_points, ref_dim, grad_output, grad_value,
+                         attn_logits, reference_points, ref_dim, key_padding_mask, grad_output,
+                         grad_value,
                          grad_sampling_offsets, grad_attn_logits, grad_reference_points,
                          workspace, workspace_bytes, d, dtype, flags, stream);
 }

@@ -65,6 +65,7 @@ __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* 
                                                  float4* woffwh, const SampleFetch& f,
                                                  const PrepFetch& pf,
                                                  const float2* s_inv, float inv_2p,
+                                                 const unsigned char* __restrict__ mrow,
                                                  const LevelInfo* s_levels,
                                                  const unsigned char* s_level_of, int r0,
                                                  int lane, int dedup) {
@@ -92,8 +93,10 @@ __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* 
                 const float2 inv = s_inv[l];
                 xy = prep_location<kRef>(pf.rxy[h], pf.rwh[h], xy, inv.x, inv.y, inv_2p);
             }
-            const Footprint fp = make_footprint(fmaf(xy.x, (float)lv.W, -0.5f),
-                                                fmaf(xy.y, (float)lv.H, -0.5f), lv);
+            Footprint fp = make_footprint(fmaf(xy.x, (float)lv.W, -0.5f),
+                                          fmaf(xy.y, (float)lv.H, -0.5f), lv);
+            if constexpr (kRef != 0)
+                if (mrow != nullptr) mask_corners(fp, mrow);
             key = make_int4(fp.key[0], fp.key[1], fp.key[2], fp.key[3]);
             aux = make_float4(fp.live || kRef != 0 ? a : 0.f, fp.fx, fp.fy, __int_as_float(l));
             cc = class_corners(fp, a);
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                     T* __restrict__ grad_attn, int num_keys, int num_heads, int head_dim,
                     int num_levels, int num_points, int num_queries, int num_qtiles,
                     int num_tiles, int tiles_per_cta, const T* __restrict__ ref,
-                    float* __restrict__ grad_ref) {
+                    const unsigned char* __restrict__ mask, float* __restrict__ grad_ref) {
     constexpr bool kPrep = kRef != 0;
     using Geom = TileGeom<kLanes>;
     constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
@@ -231,8 +234,10 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
         // ---- 1. footprints of this round (inputs fetched, references prefetched, a round ahead)
         if constexpr (kPrep) fetch_refs<T, kRef>(pf, f, ref, tc, num_queries, num_levels, pl);
         if constexpr (kPrep) softmax_rows<kSPG>(f);
-        backward_records<kSPG, kStride, kRef>(wk, waw, wax, woffwh, f, pf, s_inv,
-                                               inv_2p, s_levels, s_level_of, it.r0, lane, dedup);
+        backward_records<kSPG, kStride, kRef>(
+            wk, waw, wax, woffwh, f, pf, s_inv, inv_2p,
+            mask ? mask + (int64_t)tc.b * num_keys : nullptr, s_levels, s_level_of, it.r0, lane,
+            dedup);
         __syncwarp();
         const TileCoord cur = tc;
         const int r0 = it.r0;

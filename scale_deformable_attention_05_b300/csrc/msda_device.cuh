@@ -377,6 +377,16 @@ __device__ __forceinline__ Footprint make_footprint(float x, float y, const Leve
     return f;
 }
 
+// Key padding mask of the fused entry points (the module's masked_fill of
+// value): a corner on a padded key reads as zero, which is what an off-map
+// corner does, so it is dropped the same way.  mrow: the tile's batch row of
+// the [bs, K] mask.
+__device__ __forceinline__ void mask_corners(Footprint& fp, const unsigned char* __restrict__ mrow) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        if (fp.key[c] >= 0 && __ldg(mrow + fp.key[c]) != 0) fp.key[c] = -1;
+}
+
 // Corners of a footprint reordered by pixel parity class t = (x & 1) + 2 (y & 1).
 // Each sample has exactly one corner in each class, so two samples can share
 // a pixel only within the same class.  kw[t] is corner weight * a (0 when off

@@ -41,6 +41,7 @@ template <int kSPG, int kStride, int kRef>
 __device__ __forceinline__ void forward_records(int4* wk, float4* ww, const SampleFetch& f,
                                                 const PrepFetch& pf,
                                                 const float2* s_inv, float inv_2p,
+                                                const unsigned char* __restrict__ mrow,
                                                 const LevelInfo* s_levels,
                                                 const unsigned char* s_level_of, int r0,
                                                 int lane) {
@@ -58,8 +59,10 @@ __device__ __forceinline__ void forward_records(int4* wk, float4* ww, const Samp
                 const float2 inv = s_inv[s_level_of[r0 + sj]];
                 xy = prep_location<kRef>(pf.rxy[h], pf.rwh[h], xy, inv.x, inv.y, inv_2p);
             }
-            const Footprint fp = make_footprint(fmaf(xy.x, (float)lv.W, -0.5f),
-                                                fmaf(xy.y, (float)lv.H, -0.5f), lv);
+            Footprint fp = make_footprint(fmaf(xy.x, (float)lv.W, -0.5f),
+                                          fmaf(xy.y, (float)lv.H, -0.5f), lv);
+            if constexpr (kRef != 0)
+                if (mrow != nullptr) mask_corners(fp, mrow);
             key = make_int4(fp.key[0], fp.key[1], fp.key[2], fp.key[3]);
             w = make_float4(fp.key[0] >= 0 ? a * fp.w[0] : 0.f, fp.key[1] >= 0 ? a * fp.w[1] : 0.f,
                             fp.key[2] >= 0 ? a * fp.w[2] : 0.f, fp.key[3] >= 0 ? a * fp.w[3] : 0.f);
@@ -99,7 +102,8 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
                    const void* __restrict__ level_start_index, int idx32, const T* __restrict__ loc,
                    const T* __restrict__ attn, T* __restrict__ out, int num_keys, int num_heads,
                    int head_dim, int num_levels, int num_points, int num_queries,
-                   int num_qtiles, int num_tiles, int tiles_per_cta, const T* __restrict__ ref) {
+                   int num_qtiles, int num_tiles, int tiles_per_cta, const T* __restrict__ ref,
+                   const unsigned char* __restrict__ mask) {
     constexpr bool kPrep = kRef != 0;
     using Geom = TileGeom<kLanes>;
     using VIO = VecIO<T, kVB>;
@@ -150,8 +154,9 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
         // ---- 1. footprints of this round (inputs fetched, references prefetched, a round ahead)
         if constexpr (kPrep) fetch_refs<T, kRef>(pf, f, ref, tc, num_queries, num_levels, pl);
         if constexpr (kPrep) softmax_rows<kSPG>(f);
-        forward_records<kSPG, kStride, kRef>(wk, ww, f, pf, s_inv, inv_2p, s_levels,
-                                              s_level_of, it.r0, lane);
+        forward_records<kSPG, kStride, kRef>(
+            wk, ww, f, pf, s_inv, inv_2p, mask ? mask + (int64_t)tc.b * num_keys : nullptr,
+            s_levels, s_level_of, it.r0, lane);
         __syncwarp();
         const TileCoord cur = tc;
         const int r0 = it.r0;

@@ -146,7 +146,7 @@ cudaError_t launch_forward_t(const Problem& pb, void* out, cudaStream_t st) {
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<T*>(out), pb.K, pb.M, pb.D, pb.L, pb.P, pb.Q,
-        tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta, static_cast<const T*>(pb.ref));
+        tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta, static_cast<const T*>(pb.ref), pb.mask);
     return cudaGetLastError();
 }
 
@@ -163,7 +163,7 @@ cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
         static_cast<T*>(grad_loc), static_cast<T*>(grad_attn), pb.K, pb.M, pb.D, pb.L, pb.P,
         pb.Q, tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta, static_cast<const T*>(pb.ref),
-        grad_ref);
+        pb.mask, grad_ref);
     return cudaGetLastError();
 }
 

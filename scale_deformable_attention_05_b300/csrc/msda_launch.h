@@ -20,6 +20,8 @@ struct Problem {
     // logits, ref the reference points [bs, Q, L, ref_dim]; ref_dim 0 otherwise.
     const void* ref = nullptr;
     int ref_dim = 0;
+    // Fused entry points: optional key padding mask [bs, K], nonzero = padded.
+    const unsigned char* mask = nullptr;
 };
 
 // Element type codes (the low byte of the ABI's dtype argument).

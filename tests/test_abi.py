@@ -133,14 +133,15 @@ def test_backward_rejects_on_host(kw, status):
 def test_fused_entry_points_reject_on_host():
     d = DIMS
     fwd = lambda ref_dim=2, L=1, P=8, ref=A: L_.msda_forward_fused(
-        A, A, A, ref, A, A, A, d["bs"], d["K"], d["M"], d["D"], L, P, d["Q"], ref_dim, 0, None)
+        A, A, A, ref, A, A, None, A, d["bs"], d["K"], d["M"], d["D"], L, P, d["Q"], ref_dim, 0,
+        None)
     L_ = L
     assert fwd(ref_dim=3) == 3                 # references are (x, y) or (x, y, w, h)
     assert fwd(L=5, P=16) == 3                 # L*P above MSDA_MAX_FUSED_LEVEL_POINTS
     assert fwd(ref=None) == 1
     assert fwd(ref=A + 4) == 4
     bwd = lambda ref_dim=2, gref=None, dtype=0: L.msda_backward_fused(
-        A, A, A, A, A, A, A, A, A, A, gref, None, 0, d["bs"], d["K"], d["M"], d["D"], 1, 8,
+        A, A, A, A, A, A, None, A, A, A, A, gref, None, 0, d["bs"], d["K"], d["M"], d["D"], 1, 8,
         d["Q"], ref_dim, dtype, 0, None)
     assert bwd(ref_dim=1) == 3
     assert bwd(gref=A + 8) == 4                # fp32 reference gradient must be 16-byte aligned

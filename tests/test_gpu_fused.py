@@ -29,22 +29,33 @@ def _dev(inp, wl, name):
     return torch.from_numpy(np.ascontiguousarray(inp[name])).cuda()
 
 
-def _run_and_check(B, wl, ref_dim, sigma=2.0):
+def _mask_for(wl, kind):
+    if kind is None:
+        return None
+    if kind == "detr":
+        return gen.padding_mask(wl)                     # padded right / bottom per image
+    rng = np.random.default_rng(wl.seed + 90000)
+    return rng.random((wl.bs, wl.num_keys)) < 0.3      # scattered padded keys
+
+
+def _run_and_check(B, wl, ref_dim, sigma=2.0, mask_kind=None):
     inp = gen.make_fused_inputs(wl, ref_dim, offset_sigma=sigma)
+    mask = _mask_for(wl, mask_kind)
     names = ("value", "reference_points", "sampling_offsets", "attention_logits", "grad_output")
     d = {k: _dev(inp, wl, k) for k in names}
     sh = torch.from_numpy(inp["spatial_shapes"]).cuda()
     lsi = torch.from_numpy(inp["level_start_index"]).cuda()
+    dmask = None if mask is None else torch.from_numpy(mask).cuda()
     args = (d["value"], sh, lsi, d["reference_points"], d["sampling_offsets"],
             d["attention_logits"])
-    out = B.msda_forward_fused(*args)
-    gv, goff, glog, gref = B.msda_backward_fused(*args, d["grad_output"])
+    out = B.msda_forward_fused(*args, dmask)
+    gv, goff, glog, gref = B.msda_backward_fused(*args, d["grad_output"], dmask)
     torch.cuda.synchronize()
     assert B.msda_last_device_error() == 0
     oargs = (inp["value"], inp["spatial_shapes"], inp["level_start_index"],
              inp["reference_points"], inp["sampling_offsets"], inp["attention_logits"])
-    assert_out_close(host(out), ofused.forward(*oargs), wl.dtype)
-    rv, roff, rlog, rref = ofused.backward(*oargs, inp["grad_output"])
+    assert_out_close(host(out), ofused.forward(*oargs, padding_mask=mask), wl.dtype)
+    rv, roff, rlog, rref = ofused.backward(*oargs, inp["grad_output"], padding_mask=mask)
     assert_grad_close(host(gv), rv, wl.dtype, "grad_value")
     assert_grad_close(host(goff), roff, wl.dtype, "grad_sampling_offsets")
     assert_grad_close(host(glog), rlog, wl.dtype, "grad_attn_logits")
@@ -81,6 +92,50 @@ def test_fused_decoder_shape(B, ref_dim):
 def test_fused_encoder_shape(B):
     wl = gen.WORKLOADS["encoder"].with_(bs=1, seed=1007)
     _run_and_check(B, wl, 2, sigma=1.5)
+
+
+MASK_CASES = [
+    ("pyramid-scattered", 71, 2, ((9, 7), (5, 4), (3, 2), (2, 1)), 3, 32, 4, 17, "f32", 2,
+     "random"),
+    ("boxes-detr", 72, 3, ((12, 10), (6, 5), (3, 3)), 2, 32, 4, 15, "f32", 4, "detr"),
+    ("bf16-detr", 73, 2, ((9, 7), (5, 4)), 2, 32, 8, 11, "bf16", 2, "detr"),
+    ("wide-head-scattered", 74, 2, ((16, 12), (8, 6)), 2, 256, 16, 7, "f32", 2, "random"),
+]
+
+
+@pytest.mark.parametrize("case", MASK_CASES, ids=lambda c: c[0])
+def test_fused_padding_mask(B, case):
+    _, seed, bs, shapes, M, D, P, Q, dtype, ref_dim, kind = case
+    wl = gen.random_workload(seed, bs, shapes, M, D, P, Q, dtype=dtype)
+    _run_and_check(B, wl, ref_dim, mask_kind=kind)
+
+
+def test_fused_encoder_shape_padded_batch(B):
+    """bs=2 encoder pyramid, image 1 padded (DETR-style valid region)."""
+    wl = gen.WORKLOADS["encoder"].with_(seed=1008)
+    _run_and_check(B, wl, 2, sigma=1.5, mask_kind="detr")
+
+
+def test_fused_padding_mask_accumulate_leaves_padded_rows(B):
+    wl = gen.random_workload(75, 2, ((9, 7), (5, 4)), 2, 32, 4, 13)
+    inp = gen.make_fused_inputs(wl, 2)
+    mask = _mask_for(wl, "random")
+    t = lambda k: torch.from_numpy(np.ascontiguousarray(inp[k])).cuda()
+    sh = torch.from_numpy(inp["spatial_shapes"]).cuda()
+    lsi = torch.from_numpy(inp["level_start_index"]).cuda()
+    args = (t("value"), sh, lsi, t("reference_points"), t("sampling_offsets"),
+            t("attention_logits"), t("grad_output"), torch.from_numpy(mask).cuda())
+    base = torch.randn(t("value").shape, generator=torch.Generator().manual_seed(5)).cuda()
+    gv = base.clone()
+    B.msda_backward_fused(*args, grad_value=gv, accumulate=True)
+    torch.cuda.synchronize()
+    gv, base = host(gv), host(base)
+    np.testing.assert_array_equal(gv[mask], base[mask])         # padded rows untouched
+    rv = ofused.backward(*[inp[k] for k in ("value", "spatial_shapes", "level_start_index",
+                                            "reference_points", "sampling_offsets",
+                                            "attention_logits", "grad_output")],
+                         padding_mask=mask)[0]
+    assert_grad_close(gv - base, rv, "f32", "grad_value")
 
 
 def test_fused_autograd_wrapper(B):

@@ -217,6 +217,8 @@ def _config(wl, args):
             "entry_points": ("msda_forward_fused / msda_backward_fused (2-d reference points, "
                              "offsets, logits)" if getattr(args, "path", "plain") == "fused"
                              else "msda_forward / msda_backward"),
+            "padding_mask": ("per-image top-left valid region, U[0.6, 1] of each side, image 0 "
+                             "unpadded" if getattr(args, "padding_mask", False) else None),
             "l2": "flushed before every step (write of 2x L2 size, outside the timed events)",
             "parallelism": f"replicas x{args.gpus} (each rank its own batch)"}
 
@@ -268,7 +270,10 @@ def run_native(args, wl):
         return torch.from_numpy(np.ascontiguousarray(inp[name]))
 
     host = {k: t(k).pin_memory() for k in names}
+    if fused and args.padding_mask:
+        host["key_padding_mask"] = torch.from_numpy(gen.padding_mask(wl_r)).pin_memory()
     d = {k: v.to(dev) for k, v in host.items()}
+    mask = d.get("key_padding_mask")
     shapes = torch.from_numpy(inp["spatial_shapes"]).to(dev)
     lsi = torch.from_numpy(inp["level_start_index"]).to(dev)
     out = torch.empty((wl.bs, wl.num_queries, wl.num_heads * wl.head_dim), dtype=d["value"].dtype,
@@ -286,14 +291,14 @@ def run_native(args, wl):
 
     def run_forward():
         if fused:
-            B.msda_forward_fused(*args_fwd, output=out, stream=stream)
+            B.msda_forward_fused(*args_fwd, key_padding_mask=mask, output=out, stream=stream)
         else:
             B.msda_forward(*args_fwd, output=out, stream=stream)
 
     def run_backward(accumulate):
         if fused:     # the encoder's reference points are constants: no reference gradient
-            B.msda_backward_fused(*args_fwd, d["grad_output"], grad_value=gv,
-                                  grad_sampling_offsets=gl, grad_attn_logits=gw,
+            B.msda_backward_fused(*args_fwd, d["grad_output"], key_padding_mask=mask,
+                                  grad_value=gv, grad_sampling_offsets=gl, grad_attn_logits=gw,
                                   reference_grad=False, workspace=workspace,
                                   accumulate=accumulate, stream=stream)
         else:
@@ -396,6 +401,8 @@ def run_native(args, wl):
         # reference points [bs, Q, L, 2] replace nothing; offsets and logits have the
         # sizes of locations and weights
         ref_bytes = wl.bs * wl.num_queries * wl.num_levels * 2 * wl.elem_bytes
+        if mask is not None:
+            ref_bytes += wl.bs * wl.num_keys        # one mask byte per key
         fb = wl.compulsory_bytes(backward=False) + ref_bytes
         bb = wl.compulsory_bytes(backward=True) + ref_bytes
     else:
@@ -421,7 +428,7 @@ def run_native(args, wl):
                 "peak": hbm_gbs, "unit": "GB/s", "frac": passes[dom]["gbs"] / hbm_gbs,
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": passes[dom]["compulsory_bytes"],
-                "traffic": _profiled_traffic(wl.name, kname)}
+                "traffic": _profiled_traffic(wl.name, kname + ("_fused" if fused else ""))}
 
     line = {
         "metric": METRIC, "value": job_rate(wl.points, ws, ms_step), "unit": "points/s",
@@ -449,6 +456,8 @@ def main():
     ap.add_argument("--path", default="plain", choices=["plain", "fused"],
                     help="fused: msda_forward_fused / msda_backward_fused from reference "
                          "points, offsets and logits")
+    ap.add_argument("--padding-mask", action="store_true",
+                    help="with --path fused: pass a key padding mask (padded image batch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()

@@ -30,6 +30,7 @@ MSDA_BF16 = 1
 MSDA_F16 = 2
 MSDA_INDEX_INT32 = 0x100
 MSDA_GRAD_VALUE_ACCUMULATE = 1
+MSDA_MAX_FUSED_LEVEL_POINTS = 64
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsda.so")
 EXPORTED_SYMBOLS = (
@@ -140,6 +141,20 @@ def _dims(value: torch.Tensor, spatial_shapes: torch.Tensor, sampling_loc: torch
     return int(bs), int(K), int(M), int(D), int(L), int(P), int(Q)
 
 
+def _expect(t: Optional[torch.Tensor], shape, like: torch.Tensor, name: str) -> None:
+    """t (if given) has this shape and like's dtype and device: the kernels read
+    every float tensor as the value's element type, so a mismatch is refused
+    here instead of being read with the wrong width."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != like.dtype:
+        raise TypeError(f"{name} must have the value's dtype {like.dtype}, got {t.dtype}")
+    if t.device != like.device:
+        raise ValueError(f"{name} is on {t.device}, value on {like.device}")
+
+
 def _index(t: torch.Tensor, like: Optional[torch.Tensor] = None) -> torch.Tensor:
     if t.dtype not in (torch.int64, torch.int32):
         raise TypeError("spatial_shapes and level_start_index must be int64 or int32")
@@ -155,6 +170,9 @@ def msda_forward(value: torch.Tensor, spatial_shapes: torch.Tensor,
     """output [bs, Q, M*D] = MSDeformAttn forward (see include/msda.h)."""
     bs, K, M, D, L, P, Q = _dims(value, spatial_shapes, sampling_loc)
     code = _dtype_code(value, spatial_shapes)
+    _expect(sampling_loc, (bs, Q, M, L, P, 2), value, "sampling_loc")
+    _expect(attn_weight, (bs, Q, M, L, P), value, "attn_weight")
+    _expect(output, (bs, Q, M * D), value, "output")
     if output is None:
         output = torch.empty((bs, Q, M * D), dtype=value.dtype, device=value.device)
     _check("msda_forward", _LIB.msda_forward(
@@ -169,6 +187,16 @@ def msda_backward_workspace_bytes(bs: int, num_keys: int, num_heads: int, head_d
     return int(_LIB.msda_backward_workspace_bytes(bs, num_keys, num_heads, head_dim, dtype))
 
 
+def _check_grads(value, loc, attn, grad_output, grad_value, grad_loc, grad_attn, attn_shape,
+                 out_shape):
+    _expect(loc, tuple(attn_shape) + (2,), value, "sampling locations / offsets")
+    _expect(attn, attn_shape, value, "attention weights / logits")
+    _expect(grad_output, out_shape, value, "grad_output")
+    _expect(grad_value, value.shape, value, "grad_value")
+    _expect(grad_loc, tuple(attn_shape) + (2,), value, "grad of locations / offsets")
+    _expect(grad_attn, attn_shape, value, "grad of weights / logits")
+
+
 def msda_backward(value, spatial_shapes, level_start_index, sampling_loc, attn_weight,
                   grad_output, grad_value=None, grad_sampling_loc=None, grad_attn_weight=None,
                   workspace: Optional[torch.Tensor] = None, accumulate: bool = False,
@@ -176,7 +204,9 @@ def msda_backward(value, spatial_shapes, level_start_index, sampling_loc, attn_w
     """(grad_value, grad_sampling_loc, grad_attn_weight) of MSDeformAttn (see include/msda.h)."""
     bs, K, M, D, L, P, Q = _dims(value, spatial_shapes, sampling_loc)
     code = _dtype_code(value, spatial_shapes)
-    dev, dt = value.device, value.dtype
+    dev = value.device
+    _check_grads(value, sampling_loc, attn_weight, grad_output, grad_value, grad_sampling_loc,
+                 grad_attn_weight, (bs, Q, M, L, P), (bs, Q, M * D))
     if grad_value is None:
         grad_value = torch.empty_like(value)
     if grad_sampling_loc is None:
@@ -204,6 +234,8 @@ def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_loc
     fixed scratch array instead of a workspace (see msda_backward_noalloc in
     include/msda.h); the library allocates nothing."""
     bs, K, M, D, L, P, Q = _dims(value, spatial_shapes, sampling_loc)
+    _check_grads(value, sampling_loc, attn_weight, grad_output, grad_value, grad_sampling_loc,
+                 grad_attn_weight, (bs, Q, M, L, P), (bs, Q, M * D))
     _check("msda_backward_noalloc", _LIB.msda_backward_noalloc(
         _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index, spatial_shapes)),
         _ptr(sampling_loc), _ptr(attn_weight), _ptr(grad_output), _ptr(grad_value),
@@ -218,8 +250,9 @@ def _fused_dims(value, spatial_shapes, reference_points, sampling_offsets, attn_
     if reference_points.dim() != 4 or tuple(reference_points.shape[:3]) != (bs, Q, L):
         raise ValueError("reference_points must be [bs, Q, L, 2 or 4]")
     ref_dim = int(reference_points.shape[3])
-    if tuple(attn_logits.shape) != (bs, Q, M, L * P):
-        raise ValueError("attn_logits must be [bs, Q, M, L*P]")
+    _expect(reference_points, (bs, Q, L, ref_dim), value, "reference_points")
+    _expect(sampling_offsets, (bs, Q, M, L, P, 2), value, "sampling_offsets")
+    _expect(attn_logits, (bs, Q, M, L * P), value, "attn_logits")
     return bs, K, M, D, L, P, Q, ref_dim
 
 
@@ -231,6 +264,8 @@ def _mask(key_padding_mask: Optional[torch.Tensor], bs: int, K: int) -> Optional
         raise ValueError(f"key_padding_mask must be [bs, num_keys] = {(bs, K)}")
     if key_padding_mask.dtype not in (torch.bool, torch.uint8):
         raise TypeError("key_padding_mask must be torch.bool or torch.uint8")
+    if key_padding_mask.device.type != "cuda":
+        raise ValueError("key_padding_mask must be on the CUDA device")
     return key_padding_mask.contiguous()
 
 
@@ -243,12 +278,14 @@ def msda_forward_fused(value, spatial_shapes, level_start_index, reference_point
     bs, K, M, D, L, P, Q, ref_dim = _fused_dims(value, spatial_shapes, reference_points,
                                                 sampling_offsets, attn_logits)
     code = _dtype_code(value, spatial_shapes)
+    _expect(output, (bs, Q, M * D), value, "output")
+    mask = _mask(key_padding_mask, bs, K)
     if output is None:
         output = torch.empty((bs, Q, M * D), dtype=value.dtype, device=value.device)
     _check("msda_forward_fused", _LIB.msda_forward_fused(
         _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index, spatial_shapes)),
-        _ptr(reference_points), _ptr(sampling_offsets), _ptr(attn_logits),
-        _ptr(_mask(key_padding_mask, bs, K)), _ptr(output),
+        _ptr(reference_points), _ptr(sampling_offsets), _ptr(attn_logits), _ptr(mask),
+        _ptr(output),
         bs, K, M, D, L, P, Q, ref_dim, code, _stream(stream)))
     return output
 
@@ -265,6 +302,11 @@ def msda_backward_fused(value, spatial_shapes, level_start_index, reference_poin
                                                 sampling_offsets, attn_logits)
     code = _dtype_code(value, spatial_shapes)
     dev = value.device
+    _expect(grad_output, (bs, Q, M * D), value, "grad_output")
+    _expect(grad_value, value.shape, value, "grad_value")
+    _expect(grad_sampling_offsets, sampling_offsets.shape, value, "grad_sampling_offsets")
+    _expect(grad_attn_logits, attn_logits.shape, value, "grad_attn_logits")
+    mask = _mask(key_padding_mask, bs, K)
     if grad_value is None:
         grad_value = torch.empty_like(value)
     if grad_sampling_offsets is None:
@@ -279,8 +321,8 @@ def msda_backward_fused(value, spatial_shapes, level_start_index, reference_poin
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("msda_backward_fused", _LIB.msda_backward_fused(
         _ptr(value), _ptr(_index(spatial_shapes)), _ptr(_index(level_start_index, spatial_shapes)),
-        _ptr(reference_points), _ptr(sampling_offsets), _ptr(attn_logits),
-        _ptr(_mask(key_padding_mask, bs, K)), _ptr(grad_output),
+        _ptr(reference_points), _ptr(sampling_offsets), _ptr(attn_logits), _ptr(mask),
+        _ptr(grad_output),
         _ptr(grad_value), _ptr(grad_sampling_offsets), _ptr(grad_attn_logits), _ptr(grad_ref),
         _ptr(workspace) if workspace is not None else None, ws_bytes,
         bs, K, M, D, L, P, Q, ref_dim, code, MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0,

@@ -1,0 +1,90 @@
+"""MSDeformAttn layer: the projections around the fused CUDA operator.
+
+The layer of the Deformable DETR walk-through ("2.2.4 源码分析",
+MSDeformAttn): four linear maps of width d_model and the sampling between
+them,
+
+    value   = value_proj(input_flatten)               [N, Len_in, M, D]
+    offsets = sampling_offsets(query)                 [N, Len_q, M, L, P, 2]
+    logits  = attention_weights(query)                [N, Len_q, M, L*P]
+    out     = output_proj(msda(value masked by input_padding_mask,
+                               softmax(logits), reference_points + offsets))
+
+The four projections are plain dense GEMMs (``torch.nn.Linear``, cuBLAS);
+everything between them -- masking, softmax, locations from 2-d or 4-d
+reference points, bilinear sampling and their backward -- is one launch of
+the fused entry points of ``libmsda.so`` each way.  The tensors the GEMMs
+produce are already in the operator's layouts, so nothing is copied or
+transposed between them.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import torch
+from torch import nn
+
+from . import binding as B
+
+
+class MSDeformAttn(nn.Module):
+    """Multi-scale deformable attention with d_model channels split into
+    n_heads heads, sampling n_points points on each of n_levels levels."""
+
+    def __init__(self, d_model: int = 256, n_levels: int = 4, n_heads: int = 8,
+                 n_points: int = 4):
+        super().__init__()
+        if d_model % n_heads != 0:
+            raise ValueError(f"d_model {d_model} is not a multiple of n_heads {n_heads}")
+        head_dim = d_model // n_heads
+        if head_dim % 8 != 0:
+            raise ValueError(f"head_dim {head_dim} must be a multiple of 8 (16-byte rows)")
+        if n_levels * n_points > B.MSDA_MAX_FUSED_LEVEL_POINTS:
+            raise ValueError(f"n_levels * n_points must be <= {B.MSDA_MAX_FUSED_LEVEL_POINTS}")
+        self.d_model, self.n_levels, self.n_heads, self.n_points = d_model, n_levels, n_heads, n_points
+        self.sampling_offsets = nn.Linear(d_model, n_heads * n_levels * n_points * 2)
+        self.attention_weights = nn.Linear(d_model, n_heads * n_levels * n_points)
+        self.value_proj = nn.Linear(d_model, d_model)
+        self.output_proj = nn.Linear(d_model, d_model)
+        self.reset_parameters()
+
+    @torch.no_grad()
+    def reset_parameters(self) -> None:
+        """The walk-through's initial state: offset and attention weights zero,
+        so every query starts from fixed offsets and uniform attention.  Head h
+        looks along the direction at angle 2*pi*h/n_heads, scaled so its larger
+        component is 1; point p sits p+1 steps out along it, on every level.
+        Value and output projections: Xavier-uniform weights, zero bias."""
+        nn.init.zeros_(self.sampling_offsets.weight)
+        theta = torch.arange(self.n_heads, dtype=torch.float64) * (2.0 * math.pi / self.n_heads)
+        direction = torch.stack([theta.cos(), theta.sin()], -1)
+        direction = direction / direction.abs().max(-1, keepdim=True).values
+        steps = torch.arange(1, self.n_points + 1, dtype=torch.float64)
+        bias = direction[:, None, None, :] * steps[None, None, :, None]          # [M, 1, P, 2]
+        bias = bias.expand(self.n_heads, self.n_levels, self.n_points, 2)
+        self.sampling_offsets.bias.copy_(bias.reshape(-1))
+        nn.init.zeros_(self.attention_weights.weight)
+        nn.init.zeros_(self.attention_weights.bias)
+        nn.init.xavier_uniform_(self.value_proj.weight)
+        nn.init.zeros_(self.value_proj.bias)
+        nn.init.xavier_uniform_(self.output_proj.weight)
+        nn.init.zeros_(self.output_proj.bias)
+
+    def forward(self, query: torch.Tensor, reference_points: torch.Tensor,
+                input_flatten: torch.Tensor, input_spatial_shapes: torch.Tensor,
+                input_level_start_index: torch.Tensor,
+                input_padding_mask: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """query [N, Len_q, d_model]; reference_points [N, Len_q, n_levels, 2]
+        (normalised x, y) or [..., 4] (boxes x, y, w, h); input_flatten
+        [N, Len_in, d_model] with Len_in = sum of H*W; input_padding_mask
+        [N, Len_in] bool (True = padded) or None.  Returns [N, Len_q, d_model]."""
+        N, Len_q, _ = query.shape
+        Len_in = input_flatten.shape[1]
+        M, L, P = self.n_heads, self.n_levels, self.n_points
+        value = self.value_proj(input_flatten).view(N, Len_in, M, self.d_model // M)
+        offsets = self.sampling_offsets(query).view(N, Len_q, M, L, P, 2)
+        logits = self.attention_weights(query).view(N, Len_q, M, L * P)
+        out = B.ms_deform_attn_fused(value, input_spatial_shapes, input_level_start_index,
+                                     reference_points, offsets, logits, input_padding_mask)
+        return self.output_proj(out)

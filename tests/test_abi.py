@@ -171,6 +171,42 @@ def test_binding_rejects_cpu_tensors():
         B.msda_forward(v, shapes, lsi, loc, w)
 
 
+def test_binding_rejects_mismatched_dtypes_and_shapes():
+    """Every float tensor is read with the value's element type: the binding
+    refuses mismatches before the library sees a pointer."""
+    import torch
+    v = torch.zeros(1, 4, 1, 8)
+    loc = torch.zeros(1, 2, 1, 1, 1, 2)
+    w = torch.zeros(1, 2, 1, 1, 1)
+    shapes = torch.tensor([[2, 2]])
+    lsi = torch.tensor([0])
+    with pytest.raises(TypeError, match="dtype"):
+        B.msda_forward(v, shapes, lsi, loc.bfloat16(), w)
+    with pytest.raises(TypeError, match="dtype"):
+        B.msda_forward(v, shapes, lsi, loc, w.half())
+    with pytest.raises(ValueError, match="shape"):
+        B.msda_forward(v, shapes, lsi, loc, torch.zeros(1, 2, 1, 1, 2))
+    with pytest.raises(ValueError, match="shape"):
+        B.msda_backward(v, shapes, lsi, loc, w, torch.zeros(1, 2, 4))
+    ref = torch.zeros(1, 2, 1, 2)
+    lg = torch.zeros(1, 2, 1, 1)
+    with pytest.raises(TypeError, match="dtype"):
+        B.msda_forward_fused(v, shapes, lsi, ref.double(), loc, lg)
+    with pytest.raises(ValueError, match="key_padding_mask"):
+        B.msda_forward_fused(v, shapes, lsi, ref, loc, lg, torch.zeros(1, 3, dtype=torch.bool))
+    with pytest.raises(TypeError, match="key_padding_mask"):
+        B.msda_forward_fused(v, shapes, lsi, ref, loc, lg, torch.zeros(1, 4))
+
+
+def test_python_constants_match_header():
+    text = open(HEADER).read()
+    for name in ("MSDA_F32", "MSDA_BF16", "MSDA_F16", "MSDA_INDEX_INT32",
+                 "MSDA_MAX_FUSED_LEVEL_POINTS", "MSDA_GRAD_VALUE_ACCUMULATE"):
+        m = re.search(name + r"\s*=?\s*(0x[0-9a-fA-F]+|\d+)", text)
+        assert m, name
+        assert int(m.group(1), 0) == getattr(B, name), name
+
+
 def test_product_path_does_not_import_oracle():
     pkg = os.path.join(ROOT, "scale_deformable_attention_05_b300")
     for dirpath, _, files in os.walk(pkg):
@@ -179,3 +215,25 @@ def test_product_path_does_not_import_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "msda_oracle" not in text and "liboracle" not in text, f
+
+
+def test_module_initial_state():
+    """MSDeformAttn starts with zero offset / attention weights and the offset
+    bias on the ring of head directions, point p at p + 1 steps (checked against
+    the directions written out by hand for 8 heads)."""
+    import torch
+    from scale_deformable_attention_05_b300.module import MSDeformAttn
+    layer = MSDeformAttn(64, n_levels=2, n_heads=8, n_points=3)
+    assert not layer.sampling_offsets.weight.any()
+    assert not layer.attention_weights.weight.any() and not layer.attention_weights.bias.any()
+    assert not layer.value_proj.bias.any() and not layer.output_proj.bias.any()
+    b = layer.sampling_offsets.bias.detach().double().reshape(8, 2, 3, 2)
+    ring = torch.tensor([[1, 0], [1, 1], [0, 1], [-1, 1], [-1, 0], [-1, -1], [0, -1], [1, -1]],
+                        dtype=torch.float64)
+    for p in range(3):
+        for lvl in range(2):
+            torch.testing.assert_close(b[:, lvl, p], ring * (p + 1), rtol=0, atol=1e-6)
+    with pytest.raises(ValueError):
+        MSDeformAttn(60, n_heads=8)                 # d_model not a multiple of n_heads
+    with pytest.raises(ValueError):
+        MSDeformAttn(64, n_levels=5, n_heads=8, n_points=16)   # L*P above the fused limit

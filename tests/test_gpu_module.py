@@ -1,0 +1,101 @@
+"""The MSDeformAttn layer (projections + fused operator) against an fp64
+composition of the same steps: numpy matmuls for the four projections around
+the fused oracle (oracle/fused.py), forward and every gradient.
+
+The sampling-offset projection has zero weight (the layer's initial state), so
+the offsets are its bias exactly on both sides and both select the same
+pixels; the other projections are seeded random.  Tolerance: the fp32 grad
+rule, max|err| <= 1e-4 * max|ref|, for the output too -- it passes through
+three fp32 GEMMs of depth d_model before and after the operator."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import fused as ofused
+from scale_deformable_attention_05_b300 import inputs as gen
+from tests.gpu_helpers import assert_grad_close, host
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+
+def _oracle(params, q, x, ref, shapes, lsi, mask, g, M, L, P):
+    """fp64 forward and gradients of output_proj(msda(value_proj(x), ...))."""
+    Wv, bv, Wo, bo, Wa, ba, Wout, bout = (params[k] for k in (
+        "value_proj.weight", "value_proj.bias", "sampling_offsets.weight", "sampling_offsets.bias",
+        "attention_weights.weight", "attention_weights.bias", "output_proj.weight",
+        "output_proj.bias"))
+    N, Q, C = q.shape
+    K = x.shape[1]
+    value = (x @ Wv.T + bv).reshape(N, K, M, C // M)
+    off = (q @ Wo.T + bo).reshape(N, Q, M, L, P, 2)
+    logits = (q @ Wa.T + ba).reshape(N, Q, M, L * P)
+    y = ofused.forward(value, shapes, lsi, ref, off.astype(np.float32), logits,
+                       padding_mask=mask)
+    out = y @ Wout.T + bout
+    gy = g @ Wout
+    gv, goff, glog, gref = ofused.backward(value, shapes, lsi, ref, off.astype(np.float32),
+                                           logits, gy, padding_mask=mask)
+    gv, goff, glog = gv.reshape(N, K, C), goff.reshape(N, Q, -1), glog.reshape(N, Q, -1)
+    flat = lambda a: a.reshape(-1, a.shape[-1])
+    grads = {
+        "output_proj.weight": flat(g).T @ flat(y), "output_proj.bias": flat(g).sum(0),
+        "value_proj.weight": flat(gv).T @ flat(x), "value_proj.bias": flat(gv).sum(0),
+        "sampling_offsets.weight": flat(goff).T @ flat(q), "sampling_offsets.bias": flat(goff).sum(0),
+        "attention_weights.weight": flat(glog).T @ flat(q),
+        "attention_weights.bias": flat(glog).sum(0),
+        "query": goff @ Wo + glog @ Wa, "input_flatten": gv @ Wv, "reference_points": gref,
+    }
+    return out, grads
+
+
+@pytest.mark.parametrize("ref_dim,masked", [(2, True), (4, False)])
+def test_module_matches_fp64_composition(ref_dim, masked):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from scale_deformable_attention_05_b300.module import MSDeformAttn
+    torch.backends.cuda.matmul.allow_tf32 = False
+    shapes = ((10, 12), (5, 6), (3, 3))
+    C, M, L, P, N, Q = 64, 4, len(shapes), 4, 2, 9
+    wl = gen.random_workload(81 + ref_dim, N, shapes, M, C // M, P, Q)
+    K = wl.num_keys
+    rng = np.random.default_rng(wl.seed)
+    layer = MSDeformAttn(C, L, M, P).cuda()
+    params = {}
+    with torch.no_grad():
+        for name, p in layer.named_parameters():
+            if name == "sampling_offsets.weight":
+                a = np.zeros(tuple(p.shape))
+            elif name == "sampling_offsets.bias":
+                a = rng.normal(0.0, 2.0, tuple(p.shape))
+            else:
+                a = rng.normal(0.0, 1.0 / np.sqrt(C), tuple(p.shape))
+            a = a.astype(np.float32)
+            p.copy_(torch.from_numpy(a))
+            params[name] = a.astype(np.float64)
+    q = rng.standard_normal((N, Q, C)).astype(np.float32)
+    x = rng.standard_normal((N, K, C)).astype(np.float32)
+    ref = rng.uniform(0.1, 0.9, (N, Q, L, 2))
+    if ref_dim == 4:
+        ref = np.concatenate([ref, rng.uniform(0.1, 0.5, (N, Q, L, 2))], -1)
+    ref = ref.astype(np.float32)
+    g = rng.standard_normal((N, Q, C)).astype(np.float32)
+    mask = gen.padding_mask(wl, min_ratio=0.5) if masked else None
+    sh = torch.tensor(shapes, dtype=torch.int64, device="cuda")
+    lsi = torch.from_numpy(gen.level_start_index(shapes)).cuda()
+    tq, tx, tref = (torch.tensor(a, device="cuda", requires_grad=True) for a in (q, x, ref))
+    tmask = None if mask is None else torch.from_numpy(mask).cuda()
+    out = layer(tq, tref, tx, sh, lsi, tmask)
+    out.backward(torch.from_numpy(g).cuda())
+    torch.cuda.synchronize()
+    want, grads = _oracle(params, q.astype(np.float64), x.astype(np.float64), ref,
+                          np.array(shapes), gen.level_start_index(shapes), mask,
+                          g.astype(np.float64), M, L, P)
+    assert_grad_close(host(out), want, "f32", "output")
+    got = {n: p.grad for n, p in layer.named_parameters()}
+    got.update(query=tq.grad, input_flatten=tx.grad, reference_points=tref.grad)
+    for name, ref_grad in grads.items():
+        assert_grad_close(host(got[name]), ref_grad, "f32", name)
+    if mask is not None:                       # padded keys pass no gradient to the input
+        assert not host(tx.grad)[mask].any()

@@ -153,3 +153,77 @@ def test_fused_autograd_wrapper(B):
     rv, roff, rlog, rref = ofused.backward(*oargs, inp["grad_output"])
     for got, want in ((v.grad, rv), (off.grad, roff), (lg.grad, rlog), (ref.grad, rref)):
         assert_grad_close(host(got), want, "f32")
+
+
+def _fused_tensors(wl, ref_dim=2, mask=None, index=torch.int64):
+    inp = gen.make_fused_inputs(wl, ref_dim)
+    t = lambda k: torch.from_numpy(np.ascontiguousarray(inp[k])).cuda()
+    sh = torch.from_numpy(inp["spatial_shapes"]).to(index).cuda()
+    lsi = torch.from_numpy(inp["level_start_index"]).to(index).cuda()
+    args = (t("value"), sh, lsi, t("reference_points"), t("sampling_offsets"),
+            t("attention_logits"))
+    dmask = None if mask is None else torch.from_numpy(mask).cuda()
+    return inp, args, t("grad_output"), dmask
+
+
+def test_fused_int32_index_tensors_match_int64(B):
+    wl = gen.random_workload(76, 2, ((9, 7), (5, 4), (3, 2)), 2, 32, 4, 13)
+    mask = _mask_for(wl, "random")
+    res = []
+    for index in (torch.int64, torch.int32):
+        _, args, g, dmask = _fused_tensors(wl, 4, mask, index)
+        out = B.msda_forward_fused(*args, dmask)
+        grads = B.msda_backward_fused(*args, g, dmask)
+        torch.cuda.synchronize()
+        res.append([host(out)] + [host(x) for x in grads])
+    (o64, gv64, goff64, glog64, gref64), (o32, gv32, goff32, glog32, gref32) = res
+    # per-sample results are computed identically; grad_value and the reference
+    # gradient are sums by atomics, whose order may differ between launches
+    np.testing.assert_array_equal(o32, o64)
+    np.testing.assert_array_equal(goff32, goff64)
+    np.testing.assert_array_equal(glog32, glog64)
+    assert_grad_close(gv32, gv64, "f32", "grad_value")
+    assert_grad_close(gref32, gref64, "f32", "grad_reference_points")
+
+
+def test_fused_every_key_padded_gives_zeros(B):
+    wl = gen.random_workload(77, 2, ((9, 7), (5, 4)), 2, 32, 4, 9)
+    mask = np.ones((wl.bs, wl.num_keys), dtype=bool)
+    _, args, g, dmask = _fused_tensors(wl, 2, mask)
+    gv0 = torch.full_like(args[0], 3.0)
+    out = B.msda_forward_fused(*args, dmask)
+    gv, goff, glog, gref = B.msda_backward_fused(*args, g, dmask, grad_value=gv0,
+                                                 accumulate=True)
+    torch.cuda.synchronize()
+    assert not host(out).any()
+    assert (host(gv) == 3.0).all()                     # nothing added to padded rows
+    assert not host(goff).any() and not host(glog).any() and not host(gref).any()
+
+
+def test_fused_offsets_off_the_map_give_zeros(B):
+    wl = gen.random_workload(78, 1, ((9, 7), (5, 4)), 2, 16, 4, 6)
+    _, args, g, _ = _fused_tensors(wl, 2)
+    off = torch.full_like(args[4], 1.0e4)               # every sample far outside every level
+    args = args[:4] + (off,) + args[5:]
+    out = B.msda_forward_fused(*args)
+    gv, goff, glog, gref = B.msda_backward_fused(*args, g)
+    torch.cuda.synchronize()
+    for x in (out, gv, goff, glog, gref):
+        assert not host(x).any()
+
+
+def test_fused_no_queries(B):
+    wl = gen.random_workload(79, 2, ((9, 7), (5, 4)), 2, 32, 4, 5)
+    _, args, g, _ = _fused_tensors(wl, 2)
+    cut = lambda x: x[:, :0].contiguous()
+    args0 = args[:3] + tuple(cut(x) for x in args[3:])
+    out = B.msda_forward_fused(*args0)
+    gv, goff, glog, gref = B.msda_backward_fused(*args0, cut(g))
+    torch.cuda.synchronize()
+    assert out.shape == (wl.bs, 0, wl.num_heads * wl.head_dim)
+    assert not host(gv).any() and goff.numel() == 0 and glog.numel() == 0 and gref.numel() == 0
+
+
+def test_fused_f16_with_mask(B):
+    wl = gen.random_workload(80, 2, ((9, 7), (5, 4)), 2, 64, 4, 11, dtype="f16")
+    _run_and_check(B, wl, 4, mask_kind="detr")

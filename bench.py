@@ -447,7 +447,8 @@ def run_native(args, wl):
                 "peak": hbm_gbs, "unit": "GB/s", "frac": passes[dom]["gbs"] / hbm_gbs,
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": passes[dom]["compulsory_bytes"],
-                "traffic": _profiled_traffic(wl.name, kname + ("_fused" if fused else ""))}
+                "traffic": (None if mask is not None else   # the committed captures run unmasked
+                            _profiled_traffic(wl.name, kname + ("_fused" if fused else "")))}
 
     line = {
         "metric": METRIC, "value": job_rate(wl.points, ws, ms_step), "unit": "points/s",

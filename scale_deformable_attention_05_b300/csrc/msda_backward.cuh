@@ -134,8 +134,8 @@ __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* 
 }
 
 // grad_output row of query q (zeros past the last query or channel).
-template <typename T, int kLanes, int kVPL>
-__device__ __forceinline__ void load_grad_row(float (&gr)[kVPL][IO<T>::kVec],
+template <typename T, int kLanes, int kVPL, int kVB>
+__device__ __forceinline__ void load_grad_row(float (&gr)[kVPL][VecIO<T, kVB>::kVec],
                                               const T* __restrict__ grad_out,
                                               const TileCoord& tc, int g, int li, int nvec,
                                               int num_queries, int num_heads, int head_dim) {
@@ -145,9 +145,10 @@ __device__ __forceinline__ void load_grad_row(float (&gr)[kVPL][IO<T>::kVec],
     for (int k = 0; k < kVPL; ++k) {
         const int vi = li + k * kLanes;
 #pragma unroll
-        for (int e = 0; e < IO<T>::kVec; ++e) gr[k][e] = 0.f;
+        for (int e = 0; e < VecIO<T, kVB>::kVec; ++e) gr[k][e] = 0.f;
         if (q < num_queries && vi < nvec)
-            IO<T>::load_vec_stream(grad_out + row * head_dim + vi * IO<T>::kVec, gr[k]);
+            VecIO<T, kVB>::load_stream(grad_out + row * head_dim + vi * VecIO<T, kVB>::kVec,
+                                       gr[k]);
     }
 }
 
@@ -157,7 +158,12 @@ __device__ __forceinline__ void load_grad_row(float (&gr)[kVPL][IO<T>::kVec],
 // grad_attn the logit gradient (softmax Jacobian), grad_ref (fp32, may be
 // null) the reference-point gradient summed over heads and points.  Requires
 // L*P <= kSPG (every row in one round).
-template <typename T, int kLanes, int kVPL, int kRef>
+// kVB: bytes per row vector and lane: 16, or 8 for 16-bit types, so that a lane
+// holds four channels and its share of a corner's fp32 grad_value row is one
+// 16-byte red.  (With eight 16-bit channels a lane sends two 16-byte reds,
+// each covering half of every 32-byte sector of the row; the bf16 encoder
+// backward measured 1298 us that way against 1207 us with 8-byte vectors.)
+template <typename T, int kLanes, int kVPL, int kRef, int kVB>
 __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                                   MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS > 0
                                       ? MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS
@@ -172,8 +178,9 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                     const unsigned char* __restrict__ mask, float* __restrict__ grad_ref) {
     constexpr bool kPrep = kRef != 0;
     using Geom = TileGeom<kLanes>;
+    using VIO = VecIO<T, kVB>;
     constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
-    constexpr int V = IO<T>::kVec;
+    constexpr int V = VIO::kVec;
     // samples per transpose-reduce (at least kLanes / 4, so a lane keeps >= 1 value)
     constexpr int kBatch = MSDA_BWD_BATCH > kLanes / 4 ? MSDA_BWD_BATCH : kLanes / 4;
     constexpr int kHeld = 4 * kBatch / kLanes;     // dot products a lane keeps after it
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     PrepLane pl;
     if constexpr (kPrep) pl = prep_lane<kSPG>(lane, num_levels, LP, kRef, s_level_of);
     float gr[kVPL][V], gnext[kVPL][V];
-    load_grad_row<T, kLanes, kVPL>(gnext, grad_out, tc, g, li, nvec, num_queries, num_heads,
+    load_grad_row<T, kLanes, kVPL, kVB>(gnext, grad_out, tc, g, li, nvec, num_queries, num_heads,
                                    head_dim);
 
     while (true) {
@@ -257,7 +264,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
             fetch_samples<T, kSPG>(f, loc, attn, tc, it.r0, lane, LP, num_queries, num_heads);
             if constexpr (kPrep) prefetch_refs<T, kRef>(f, ref, tc, num_queries, num_levels, pl);
             if (it.r0 == 0)
-                load_grad_row<T, kLanes, kVPL>(gnext, grad_out, tc, g, li, nvec, num_queries,
+                load_grad_row<T, kLanes, kVPL, kVB>(gnext, grad_out, tc, g, li, nvec, num_queries,
                                                num_heads, head_dim);
         }
 
@@ -289,7 +296,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                         const int vi = li + k * kLanes;
 #pragma unroll
                         for (int e = 0; e < V; ++e) v[k][e] = 0.f;
-                        if (keys[c] >= 0 && vi < nvec) IO<T>::load_vec(p + vi * 16, v[k]);
+                        if (keys[c] >= 0 && vi < nvec) VIO::load(p + vi * kVB, v[k]);
                     }
                     float d = 0.f;
 #pragma unroll

@@ -102,9 +102,11 @@ struct IO<__nv_bfloat16> {
     __device__ __forceinline__ static void load_vec_stream(const T* p, float (&v)[kVec]) {
         unpack(__ldcs(reinterpret_cast<const uint4*>(p)), v);
     }
-    __device__ __forceinline__ static float2 load_xy(const T* p) {
-        const uint32_t u = __ldcs(reinterpret_cast<const unsigned int*>(p));
+    __device__ __forceinline__ static float2 pair(uint32_t u) {
         return make_float2(bf16_lo(u), bf16_hi(u));
+    }
+    __device__ __forceinline__ static float2 load_xy(const T* p) {
+        return pair(__ldcs(reinterpret_cast<const unsigned int*>(p)));
     }
     __device__ __forceinline__ static float load_one(const T* p) {
         const unsigned short u = __ldcs(reinterpret_cast<const unsigned short*>(p));
@@ -155,8 +157,9 @@ struct IO<__half> {
     __device__ __forceinline__ static void load_vec_stream(const T* p, float (&v)[kVec]) {
         unpack(__ldcs(reinterpret_cast<const uint4*>(p)), v);
     }
+    __device__ __forceinline__ static float2 pair(uint32_t u) { return half2_bits_to_float2(u); }
     __device__ __forceinline__ static float2 load_xy(const T* p) {
-        return half2_bits_to_float2(__ldcs(reinterpret_cast<const unsigned int*>(p)));
+        return pair(__ldcs(reinterpret_cast<const unsigned int*>(p)));
     }
     __device__ __forceinline__ static float load_one(const T* p) {
         const unsigned short u = __ldcs(reinterpret_cast<const unsigned short*>(p));
@@ -276,11 +279,32 @@ struct IO32<__half> {
 template <typename T, int kBytes>
 struct VecIO;
 
+// 8-byte vectors of a 16-bit type: four channels, whose fp32 gradient is one
+// 16-byte red (the backward's layout for half types, see backward_kernel).
+template <typename T>
+struct VecIO<T, 8> {
+    static_assert(sizeof(T) == 2, "8-byte vectors hold four 16-bit values");
+    static constexpr int kVec = 4;
+    __device__ __forceinline__ static void unpack(const uint2 u, float (&v)[kVec]) {
+        const float2 a = IO<T>::pair(u.x), b = IO<T>::pair(u.y);
+        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    }
+    __device__ __forceinline__ static void load(const void* p, float (&v)[kVec]) {
+        unpack(__ldg(reinterpret_cast<const uint2*>(p)), v);
+    }
+    __device__ __forceinline__ static void load_stream(const T* p, float (&v)[kVec]) {
+        unpack(__ldcs(reinterpret_cast<const uint2*>(p)), v);
+    }
+};
+
 template <typename T>
 struct VecIO<T, 16> {
     static constexpr int kVec = IO<T>::kVec;
     __device__ __forceinline__ static void load(const void* p, float (&v)[kVec]) {
         IO<T>::load_vec(p, v);
+    }
+    __device__ __forceinline__ static void load_stream(const T* p, float (&v)[kVec]) {
+        IO<T>::load_vec_stream(p, v);
     }
     __device__ __forceinline__ static void store(T* p, const float (&v)[kVec]) {
         IO<T>::store_vec(p, v);

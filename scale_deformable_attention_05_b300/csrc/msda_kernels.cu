@@ -150,11 +150,11 @@ cudaError_t launch_forward_t(const Problem& pb, void* out, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <typename T, int kLanes, int kVPL, int kRef = 0>
+template <typename T, int kLanes, int kVPL, int kRef, int kVB>
 cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv32,
                               void* grad_loc, void* grad_attn, cudaStream_t st,
                               float* grad_ref = nullptr) {
-    auto kernel = backward_kernel<T, kLanes, kVPL, kRef>;
+    auto kernel = backward_kernel<T, kLanes, kVPL, kRef, kVB>;
     constexpr int kThreads = MSDA_BWD_WARPS * 32;
     const TileGrid tg =
         tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS);
@@ -257,19 +257,39 @@ cudaError_t launch_backward_merge_t(const Problem& pb, int log2_points, const vo
     return cudaGetLastError();
 }
 
+// backward_kernel reads four channels per lane vector: 16 bytes of fp32, 8 bytes
+// of a 16-bit type, so that a lane's share of a corner's fp32 grad_value row is
+// one 16-byte red and the lane group's reds cover whole 32-byte sectors.
+template <typename T>
+constexpr int backward_vec_bytes() { return sizeof(T) == 2 ? 8 : 16; }
+
+template <typename T>
+int backward_nvec(const Problem& pb) { return pb.D * (int)sizeof(T) / backward_vec_bytes<T>(); }
+
+template <typename T, int kRef, int kMinLanes>
+cudaError_t launch_backward_layout(const Problem& pb, Layout ly, const void* g, float* gv32,
+                                   void* gl, void* ga, cudaStream_t st, float* gref) {
+    constexpr int kVB = backward_vec_bytes<T>();
+    if (ly.vpl == 1) {
+        switch (ly.lanes) {
+            case 4:
+                if constexpr (kMinLanes <= 4)
+                    return launch_backward_t<T, 4, 1, kRef, kVB>(pb, g, gv32, gl, ga, st, gref);
+                [[fallthrough]];
+            case 8: return launch_backward_t<T, 8, 1, kRef, kVB>(pb, g, gv32, gl, ga, st, gref);
+            case 16: return launch_backward_t<T, 16, 1, kRef, kVB>(pb, g, gv32, gl, ga, st, gref);
+            default: return launch_backward_t<T, 32, 1, kRef, kVB>(pb, g, gv32, gl, ga, st, gref);
+        }
+    }
+    if (ly.vpl == 2) return launch_backward_t<T, 32, 2, kRef, kVB>(pb, g, gv32, gl, ga, st, gref);
+    return launch_backward_t<T, 32, 4, kRef, kVB>(pb, g, gv32, gl, ga, st, gref);
+}
+
 template <typename T, int kRef>
 cudaError_t dispatch_backward_fused_ref(const Problem& pb, const void* g, float* gv32, void* gl,
                                         void* ga, cudaStream_t st, float* gref) {
-    const Layout ly = fused_layout(pb, pb.D / IO<T>::kVec, 8);
-    if (ly.vpl == 1) {
-        switch (ly.lanes) {
-            case 8: return launch_backward_t<T, 8, 1, kRef>(pb, g, gv32, gl, ga, st, gref);
-            case 16: return launch_backward_t<T, 16, 1, kRef>(pb, g, gv32, gl, ga, st, gref);
-            default: return launch_backward_t<T, 32, 1, kRef>(pb, g, gv32, gl, ga, st, gref);
-        }
-    }
-    if (ly.vpl == 2) return launch_backward_t<T, 32, 2, kRef>(pb, g, gv32, gl, ga, st, gref);
-    return launch_backward_t<T, 32, 4, kRef>(pb, g, gv32, gl, ga, st, gref);
+    return launch_backward_layout<T, kRef, 8>(pb, fused_layout(pb, backward_nvec<T>(pb), 8), g,
+                                              gv32, gl, ga, st, gref);
 }
 
 template <typename T>
@@ -298,16 +318,8 @@ cudaError_t dispatch_backward(const Problem& pb, const void* g, float* gv32, voi
         return launch_backward_merge_t<T, 32, 4>(pb, log2p, g, gv32, gl, ga, st);
     }
 #endif
-    if (ly.vpl == 1) {
-        switch (ly.lanes) {
-            case 4: return launch_backward_t<T, 4, 1>(pb, g, gv32, gl, ga, st);
-            case 8: return launch_backward_t<T, 8, 1>(pb, g, gv32, gl, ga, st);
-            case 16: return launch_backward_t<T, 16, 1>(pb, g, gv32, gl, ga, st);
-            default: return launch_backward_t<T, 32, 1>(pb, g, gv32, gl, ga, st);
-        }
-    }
-    if (ly.vpl == 2) return launch_backward_t<T, 32, 2>(pb, g, gv32, gl, ga, st);
-    return launch_backward_t<T, 32, 4>(pb, g, gv32, gl, ga, st);
+    return launch_backward_layout<T, 0, 4>(pb, choose_layout(backward_nvec<T>(pb)), g, gv32, gl,
+                                           ga, st, gref);
 }
 
 int grid_for(size_t n, int threads) {

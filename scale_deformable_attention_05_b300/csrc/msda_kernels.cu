@@ -82,8 +82,10 @@ Layout choose_layout(int nvec) {
     return ly;
 }
 
+// Waves of resident CTAs per launch: 0 picks them from the working set
+// (persistent_waves), a positive value fixes them.
 #ifndef MSDA_PERSISTENT_WAVES
-#define MSDA_PERSISTENT_WAVES 1
+#define MSDA_PERSISTENT_WAVES 0
 #endif
 
 int sm_count() {
@@ -91,6 +93,30 @@ int sm_count() {
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     return sms > 0 ? sms : 1;
+}
+
+int64_t l2_bytes() {
+    int dev = 0, l2 = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    return l2 > 0 ? l2 : (int64_t)126 << 20;
+}
+
+// Waves per launch from the working set: value (and, in the backward, its fp32
+// gradient) over a target share of L2, rounded up to a power of two.  The CTAs
+// resident at a time then cover that share of the (b, m)-ordered tiles, whose
+// value and grad_value slices stay in L2 against the streamed inputs and
+// outputs.  Targets from a sweep of 1..32 waves (CUDA events): the backward
+// wants ~0.6 L2 of slices live (fp32 encoder 1-2 waves, bf16 encoder 2-4,
+// D = 256 envelope 8-16: -27%), the forward ~L2 / 8 (fp32 encoder flat, bf16
+// encoder 4-16: -6%, envelope 32: -30%).
+int persistent_waves(const Problem& pb, int elem_bytes, bool backward) {
+    if (MSDA_PERSISTENT_WAVES > 0) return MSDA_PERSISTENT_WAVES;
+    const double ws = (double)pb.bs * pb.K * pb.M * pb.D * (elem_bytes + (backward ? 4 : 0));
+    const double target = (double)l2_bytes() * (backward ? 0.6 : 0.125);
+    int w = 1;
+    while (w < 64 && w * target < ws) w <<= 1;
+    return w;
 }
 
 #ifndef MSDA_SMEM_CARVEOUT
@@ -119,19 +145,16 @@ struct TileGrid {
 };
 
 // Warp tiles of `queries_per_tile` queries, ordered (b, m, query block).  The grid is
-// MSDA_PERSISTENT_WAVES waves of resident CTAs; each CTA takes a contiguous
+// `waves` waves of resident CTAs; each CTA takes a contiguous
 // range of tiles (a multiple of its warps), so consecutive tiles of one head
 // run on one SM and share its L1.
-TileGrid tile_grid(const Problem& pb, int queries_per_tile, int resident, int warps) {
+TileGrid tile_grid(const Problem& pb, int queries_per_tile, int resident, int warps, int waves) {
     TileGrid tg;
     tg.num_qtiles = (pb.Q + queries_per_tile - 1) / queries_per_tile;
     tg.num_tiles = pb.bs * pb.M * tg.num_qtiles;
-    int64_t per = warps;
-    if (MSDA_PERSISTENT_WAVES > 0) {
-        const int64_t ctas = (int64_t)sm_count() * resident * MSDA_PERSISTENT_WAVES;
-        per = (tg.num_tiles + ctas - 1) / ctas;
-        per = (per + warps - 1) / warps * warps;
-    }
+    const int64_t ctas = (int64_t)sm_count() * resident * waves;
+    int64_t per = (tg.num_tiles + ctas - 1) / ctas;
+    per = (per + warps - 1) / warps * warps;
     tg.tiles_per_cta = (int)per;
     tg.grid = (int)((tg.num_tiles + per - 1) / per);
     return tg;
@@ -142,7 +165,8 @@ cudaError_t launch_forward_t(const Problem& pb, void* out, cudaStream_t st) {
     auto kernel = forward_kernel<T, kLanes, kVPL, kVB, kRef>;
     constexpr int kThreads = MSDA_FWD_WARPS * 32;
     const TileGrid tg =
-        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_FWD_WARPS);
+        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_FWD_WARPS,
+                  persistent_waves(pb, (int)sizeof(T), false));
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<T*>(out), pb.K, pb.M, pb.D, pb.L, pb.P, pb.Q,
@@ -157,7 +181,8 @@ cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv
     auto kernel = backward_kernel<T, kLanes, kVPL, kRef, kVB>;
     constexpr int kThreads = MSDA_BWD_WARPS * 32;
     const TileGrid tg =
-        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS);
+        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS,
+                  persistent_waves(pb, (int)sizeof(T), true));
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
@@ -248,7 +273,8 @@ cudaError_t launch_backward_merge_t(const Problem& pb, int log2_points, const vo
     auto kernel = backward_merge_kernel<T, kLanes, kVPL>;
     constexpr int kThreads = MSDA_BWD_WARPS * 32;
     const TileGrid tg =
-        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS);
+        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS,
+                  persistent_waves(pb, (int)sizeof(T), true));
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,

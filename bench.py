@@ -246,6 +246,34 @@ def job_rate(units_per_rank, world_size, ms):
     return units_per_rank * world_size / (ms / 1e3)
 
 
+class _CapturedPass:
+    """One pass captured as a CUDA graph with the runtime API (stream capture on
+    the bench's side stream) and launched with cudaGraphLaunch: only the
+    library's kernels are in the graph, and a replay enqueues nothing else."""
+
+    def __init__(self, fn, stream):
+        from cuda.bindings import runtime as cudart
+        self.cudart, self.handle = cudart, cudart.cudaStream_t(stream.cuda_stream)
+        mode = cudart.cudaStreamCaptureMode.cudaStreamCaptureModeThreadLocal
+        self._ok(cudart.cudaStreamBeginCapture(self.handle, mode))
+        try:
+            fn()
+        finally:
+            err, graph = cudart.cudaStreamEndCapture(self.handle)
+        self._ok((err,))
+        err, self.exe = cudart.cudaGraphInstantiate(graph, 0)
+        self._ok((err,))
+        self._ok(cudart.cudaGraphDestroy(graph))
+
+    def _ok(self, res):
+        err = res[0]
+        if err != self.cudart.cudaError_t.cudaSuccess:
+            raise RuntimeError(f"CUDA graph capture: {err}")
+
+    def __call__(self):
+        self._ok(self.cudart.cudaGraphLaunch(self.exe, self.handle))
+
+
 # -------------------------------------------------------------- native arm
 def run_native(args, wl):
     import torch
@@ -332,15 +360,9 @@ def run_native(args, wl):
     torch.cuda.synchronize()
     if not args.no_graph:
         # Each pass captured once as a CUDA graph and replayed: the timed region
-        # then holds the kernels alone, not the Python marshalling between them
-        # (which exceeds the kernel time of the small workloads).
-        graphs = []
-        for fn in passes_fn:
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=stream):
-                fn()
-            graphs.append(gr)
-        passes_fn = [gr.replay for gr in graphs]
+        # then holds the library's kernels alone, not the Python marshalling
+        # between them (which exceeds the kernel time of the small workloads).
+        passes_fn = [_CapturedPass(fn, stream) for fn in passes_fn]
         for _ in range(2):
             flush.zero_()
             step()

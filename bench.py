@@ -164,10 +164,22 @@ def cpu_baseline(wl, inp, budget_s=12.0, min_reps=1):
         el = time.perf_counter() - t0
         if reps >= min_reps and (el >= budget_s or el / reps * (reps + 1) > 2.5 * budget_s):
             break
+    # the same oracle on one core, on the first queries only (a few seconds):
+    # at least 200k samples so the per-call setup does not dominate
+    per_q = wl.bs * wl.num_heads * wl.num_levels * wl.num_points
+    q1 = min(wl.num_queries, max(wl.num_queries // 16, -(-200_000 // per_q)))
+    sample1 = _sample_inputs(inp, wl, q1)
+    t1 = time.perf_counter()
+    _oracle_step(sample1, wl, threads=1)
+    el1 = time.perf_counter() - t1
+    pts1 = wl.bs * q1 * wl.num_heads * wl.num_levels * wl.num_points
     return {"value": wl.points * reps / el, "unit": "points/s", "cores": threads,
             "kind": "oracle",
             "sample": f"{reps} full forward+backward pass(es) of the '{wl.name}' workload "
-                      f"({wl.points} samples each), fp64 C oracle, {el:.1f} s"}
+                      f"({wl.points} samples each), fp64 C oracle, {el:.1f} s",
+            "single_core": {"value": pts1 / el1, "unit": "points/s", "cores": 1,
+                            "sample": f"first {q1} of {wl.num_queries} queries ({pts1} samples), "
+                                      f"forward + backward, {el1:.1f} s"}}
 
 
 def run_reference(args, wl):
@@ -451,12 +463,14 @@ def run_native(args, wl):
         bb = wl.compulsory_bytes(backward=True)
     passes = {
         "forward": {"kernel": "forward_kernel", "ms": mean(fwd_ms), "min_ms": min(fwd_ms),
+                    "median_ms": statistics.median(fwd_ms),
                     "points_per_s": wl.points / (mean(fwd_ms) / 1e3),
                     "compulsory_bytes": fb, "gbs": fb / (mean(fwd_ms) / 1e3) / 1e9},
         "zero_fill": {"kernel": "zero_fill_kernel", "ms": mean(zero_ms)},
         "backward": {"kernel": "backward_kernel" + ("" if wl.dtype == "f32" else
                                                     " (+zero/finalize)"),
                      "ms": mean(bwd_ms), "min_ms": min(bwd_ms),
+                     "median_ms": statistics.median(bwd_ms),
                      "points_per_s": wl.points / (mean(bwd_ms) / 1e3),
                      "compulsory_bytes": bb, "gbs": bb / (mean(bwd_ms) / 1e3) / 1e9},
     }

@@ -258,6 +258,77 @@ def job_rate(units_per_rank, world_size, ms):
     return units_per_rank * world_size / (ms / 1e3)
 
 
+def _e2e_pipelined(B, args, wl, fused, names, host, d, shapes, lsi, results, workspace, stream,
+                   dev, dist, world):
+    """The step end to end through the public API with host buffers: every step
+    copies its inputs from pinned host memory to the device, runs the forward and
+    the backward, and copies the output and the three gradients back.  Two
+    buffer sets make it a two-deep pipeline on three streams (host -> device,
+    compute, device -> host): step i+1's uploads and step i's downloads move in
+    opposite directions of the link while step i computes."""
+    import torch
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(x.numel() * x.element_size() for x in results)
+    sets = []
+    for i in range(2):
+        din = d if i == 0 else {k: torch.empty_like(v) for k, v in d.items()}
+        dres = results if i == 0 else tuple(torch.empty_like(x) for x in results)
+        hres = tuple(torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in dres)
+        sets.append((din, dres, hres))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in, ev_done, ev_copied = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+    def compute(din, dres):
+        o, g_v, g_l, g_w = dres
+        mask = din.get("key_padding_mask")
+        a = (din["value"], shapes, lsi) + tuple(din[k] for k in names[1:-1])
+        if fused:
+            B.msda_forward_fused(*a, key_padding_mask=mask, output=o, stream=stream)
+            B.msda_backward_fused(*a, din["grad_output"], key_padding_mask=mask, grad_value=g_v,
+                                  grad_sampling_offsets=g_l, grad_attn_logits=g_w,
+                                  reference_grad=False, workspace=workspace, stream=stream)
+        else:
+            B.msda_forward(*a, output=o, stream=stream)
+            B.msda_backward(*a, din["grad_output"], g_v, g_l, g_w, workspace=workspace,
+                            stream=stream)
+
+    def e2e_step(i):
+        b = i % 2
+        din, dres, hres = sets[b]
+        s_in.wait_event(ev_done[b])            # set b's inputs are free again
+        with torch.cuda.stream(s_in):
+            for k in host:
+                din[k].copy_(host[k], non_blocking=True)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_copied[b])        # set b's results have been read back
+        compute(din, dres)
+        ev_done[b].record(stream)
+        s_out.wait_event(ev_done[b])
+        with torch.cuda.stream(s_out):
+            for h, x in zip(hres, dres):
+                h.copy_(x, non_blocking=True)
+        ev_copied[b].record(s_out)
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(4, min(args.steps, 10))
+    e0.record(s_in)
+    for i in range(n_e2e):
+        e2e_step(i)
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, dev)
+    return {"value": job_rate(wl.points, world, e2e_ms), "unit": "points/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "path": "per step: pinned host -> device copies of the inputs, msda_forward%s and "
+                    "msda_backward%s through the Python API, device -> pinned host copies of the "
+                    "output and the three gradients; two buffer sets, uploads / compute / "
+                    "downloads on three streams" % (("_fused",) * 2 if fused else ("", ""))}
+
+
 class _CapturedPass:
     """One pass captured as a CUDA graph with the runtime API (stream capture on
     the bench's side stream) and launched with cudaGraphLaunch: only the
@@ -410,39 +481,8 @@ def run_native(args, wl):
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h_gv = torch.empty(gv.shape, dtype=gv.dtype).pin_memory()
-        h_gl = torch.empty(gl.shape, dtype=gl.dtype).pin_memory()
-        h_gw = torch.empty(gw.shape, dtype=gw.dtype).pin_memory()
-        h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = sum(x.numel() * x.element_size() for x in (h_out, h_gv, h_gl, h_gw))
-
-        def e2e_step():
-            for k in host:
-                d[k].copy_(host[k], non_blocking=True)
-            run_forward()
-            run_backward(accumulate=False)
-            h_out.copy_(out, non_blocking=True)
-            h_gv.copy_(gv, non_blocking=True)
-            h_gl.copy_(gl, non_blocking=True)
-            h_gw.copy_(gw, non_blocking=True)
-
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_e2e = max(3, min(args.steps, 10))
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, dev)
-        e2e = {"value": job_rate(wl.points, ws, e2e_ms), "unit": "points/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "path": "pinned host -> device copies, msda_forward%s, msda_backward%s, "
-                       "device -> pinned host copies of output and the three gradients"
-                       % (("_fused",) * 2 if fused else ("", ""))}
+        e2e = _e2e_pipelined(B, args, wl, fused, names, host, d, shapes, lsi, (out, gv, gl, gw),
+                             workspace, stream, dev, dist, ws)
 
     if rank != 0:
         if dist:

@@ -68,9 +68,10 @@ struct Layout {
     int lanes, vpl;
 };
 
-// Lanes per lane group and 16-byte vectors per lane for a head of `nvec`
-// vectors: one vector per lane up to 32 vectors (at least 4 lanes, so a
-// warp tile holds at most 8 queries), then 2 or 4 vectors on 32 lanes.
+// Lanes per lane group and row vectors per lane for a head of `nvec` vectors
+// (of whatever width the kernel reads): one vector per lane up to 32 vectors
+// (at least 4 lanes, so a warp tile holds at most 8 queries), then 2 or 4
+// vectors on 32 lanes.
 Layout choose_layout(int nvec) {
     Layout ly{4, 1};
     if (nvec <= 32) {

@@ -29,7 +29,7 @@ constexpr int kF32 = 0, kBF16 = 1, kF16 = 2;
 
 cudaError_t launch_forward(const Problem& pb, void* out, int dtype, cudaStream_t st);
 // gv32: fp32 grad_value accumulator (the caller's fp32 grad_value, or the
-// bf16 path's workspace), already zeroed or holding the sum to add to.
+// 16-bit paths' workspace), already zeroed or holding the sum to add to.
 // grad_ref: fused mode's fp32 reference-point gradient (already zeroed), or null.
 cudaError_t launch_backward(const Problem& pb, const void* grad_out, float* gv32, void* grad_loc,
                             void* grad_attn, int dtype, cudaStream_t st,

@@ -182,6 +182,26 @@ def cpu_baseline(wl, inp, budget_s=12.0, min_reps=1):
                                       f"forward + backward, {el1:.1f} s"}}
 
 
+def touched_roofline(wl, inp, passes, hbm_gbs):
+    """Secondary roofline: the value (and grad_value) bytes counted over the
+    distinct (b, key, m) rows the workload's samples touch with a non-zero
+    weight, as counted by the oracle, instead of the whole tensor.  Matters
+    where few rows are read (the decoder's 300 queries)."""
+    import oracle
+    rows = oracle.touched_rows(inp["spatial_shapes"], inp["level_start_index"],
+                               inp["sampling_locations"], inp["attention_weights"],
+                               wl.bs, wl.num_keys, wl.num_heads)
+    row_bytes = wl.head_dim * wl.elem_bytes
+    value = wl.bs * wl.num_keys * wl.num_heads * row_bytes
+    out = {"label": "secondary: value and grad_value bytes over touched rows only",
+           "touched_rows": rows, "of_rows": wl.bs * wl.num_keys * wl.num_heads}
+    for name, n_value in (("forward", 1), ("backward", 2)):
+        b = passes[name]["compulsory_bytes"] - n_value * (value - rows * row_bytes)
+        gbs = b / (passes[name]["ms"] / 1e3) / 1e9
+        out[name] = {"bytes": b, "gbs": gbs, "frac": gbs / hbm_gbs}
+    return out
+
+
 def run_reference(args, wl):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -535,7 +555,10 @@ def run_native(args, wl):
         "wall_s_timed_region_incl_flush": wall, "clocks": clocks, "e2e": e2e,
     }
     if not args.no_cpu_baseline and ws == 1:
-        line["cpu_baseline"] = cpu_baseline(wl, gen.make_inputs(wl))
+        inp0 = gen.make_inputs(wl)
+        line["cpu_baseline"] = cpu_baseline(wl, inp0)
+        if not fused:
+            line["roofline_touched"] = touched_roofline(wl, inp0, passes, hbm_gbs)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -182,6 +182,94 @@ def cpu_baseline(wl, inp, budget_s=12.0, min_reps=1):
                                       f"forward + backward, {el1:.1f} s"}}
 
 
+def run_layer(args, wl):
+    """The MSDeformAttn layer (module.MSDeformAttn: four cuBLAS projections around
+    the fused entry points) forward + backward through autograd on the workload's
+    shape: seeded random query / input features, the workload's fused reference
+    points, the layer's initial parameters.  Each step is timed with CUDA events
+    as the layer runs (Python and autograd included); L2 flushed before each."""
+    import torch
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    from scale_deformable_attention_05_b300.module import MSDeformAttn
+    if wl.dtype != "f32":
+        raise SystemExit("--path layer runs fp32 workloads")
+    torch.backends.cuda.matmul.allow_tf32 = False
+    dev = torch.device("cuda", local)
+    wl_r = rank_workload(wl, rank)
+    C = wl.num_heads * wl.head_dim
+    torch.manual_seed(wl_r.seed)
+    layer = MSDeformAttn(C, wl.num_levels, wl.num_heads, wl.num_points).to(dev)
+    fin = gen.make_fused_inputs(wl_r, 2)
+    gcpu = torch.Generator().manual_seed(wl_r.seed)
+    q = torch.randn(wl.bs, wl.num_queries, C, generator=gcpu).to(dev).requires_grad_()
+    x = torch.randn(wl.bs, wl.num_keys, C, generator=gcpu).to(dev).requires_grad_()
+    go = torch.randn(wl.bs, wl.num_queries, C, generator=gcpu).to(dev)
+    ref = torch.from_numpy(fin["reference_points"]).to(dev)
+    shapes = torch.from_numpy(fin["spatial_shapes"]).to(dev)
+    lsi = torch.from_numpy(fin["level_start_index"]).to(dev)
+    mask = (torch.from_numpy(gen.padding_mask(wl_r)).to(dev) if args.padding_mask else None)
+    flush = torch.empty(max(2 * torch.cuda.get_device_properties(dev).L2_cache_size, 64 << 20) // 4,
+                        dtype=torch.float32, device=dev)
+
+    def step():
+        for prm in layer.parameters():
+            prm.grad = None
+        q.grad = x.grad = None
+        layer(q, ref, x, shapes, lsi, mask).backward(go)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record()
+        step()
+        e1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    ms_step = max_over_ranks(sum(ms) / len(ms), dist, dev)
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    cfg = _config(wl, args)
+    cfg["entry_points"] = ("module.MSDeformAttn: value / offset / weight / output projections "
+                           "(torch Linear, cuBLAS fp32) around msda_forward_fused / "
+                           "msda_backward_fused, autograd")
+    cfg["launch"] = "eager through autograd (no graphs; Python and autograd inside the events)"
+    line = {
+        "metric": METRIC, "value": job_rate(wl.points, ws, ms_step), "unit": "points/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (random query / input features, initial layer parameters)",
+        "config": cfg,
+        "passes": {"layer": {"ms": sum(ms) / len(ms), "median_ms": statistics.median(ms),
+                             "min_ms": min(ms)}},
+        "roofline": None, "clocks": clocks, "e2e": None,
+        # the library's kernels per step: fused forward; grad_value zero-fill + fused backward
+        "gpu_launches": 3 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
 def touched_roofline(wl, inp, passes, hbm_gbs):
     """Secondary roofline: the value (and grad_value) bytes counted over the
     distinct (b, key, m) rows the workload's samples touch with a non-zero
@@ -572,9 +660,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="encoder", choices=sorted(gen.WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--path", default="plain", choices=["plain", "fused"],
+    ap.add_argument("--path", default="plain", choices=["plain", "fused", "layer"],
                     help="fused: msda_forward_fused / msda_backward_fused from reference "
-                         "points, offsets and logits")
+                         "points, offsets and logits; layer: the MSDeformAttn layer with its "
+                         "projections, through autograd")
     ap.add_argument("--padding-mask", action="store_true",
                     help="with --path fused: pass a key padding mask (padded image batch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -588,6 +677,8 @@ def main():
     wl = gen.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, wl)
+    if args.path == "layer":
+        return run_layer(args, wl)
     return run_native(args, wl)
 
 

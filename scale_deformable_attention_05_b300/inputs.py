@@ -412,6 +412,13 @@ WORKLOADS: Dict[str, Workload] = {
         grad_kind="normal",
         description="encoder shape with bs=4, bf16 I/O, fp32 accumulation; forward+backward",
     ),
+    "encoder_f16": Workload(
+        name="encoder_f16", seed=1006, bs=4, spatial_shapes=DETR_PYRAMID, num_heads=8,
+        head_dim=32, num_points=4, num_queries=22223, dtype="f16", loc_kind="encoder",
+        loc_sigma=0.02, loc_clamp=(-0.05, 1.05), weight_kind="softmax", value_kind="normal",
+        grad_kind="normal",
+        description="encoder shape with bs=4, fp16 I/O, fp32 accumulation; forward+backward",
+    ),
     "envelope": Workload(
         name="envelope", seed=1005, bs=1, spatial_shapes=ENVELOPE_PYRAMID, num_heads=8,
         head_dim=256, num_points=16, num_queries=10000, dtype="f32", loc_kind="grid",

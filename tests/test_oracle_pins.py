@@ -395,7 +395,7 @@ def test_workload_generator_is_seeded_and_shaped():
                                                  wl.num_levels, wl.num_points, 2)
         if wl.weight_kind == "softmax":
             s = a["attention_weights"].astype(np.float64).sum(axis=(3, 4))
-            np.testing.assert_allclose(s, 1.0, atol=1e-2 if wl.dtype == "bf16" else 1e-5)
+            np.testing.assert_allclose(s, 1.0, atol=1e-2 if wl.dtype in ("bf16", "f16") else 1e-5)
     enc = gen.WORKLOADS["encoder"]
     assert enc.num_keys == enc.num_queries == 22223
     assert gen.level_start_index(enc.spatial_shapes).tolist() == [0, 16700, 20900, 21950]

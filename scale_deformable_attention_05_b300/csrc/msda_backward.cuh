@@ -296,7 +296,8 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                         const int vi = li + k * kLanes;
 #pragma unroll
                         for (int e = 0; e < V; ++e) v[k][e] = 0.f;
-                        if (keys[c] >= 0 && vi < nvec) VIO::load(p + vi * kVB, v[k]);
+                        if (keys[c] >= 0 && vi < nvec && row_in_range(keys[c], num_keys))
+                            VIO::load(p + vi * kVB, v[k]);
                     }
                     float d = 0.f;
 #pragma unroll
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                         for (int e = 0; e < V; ++e) d = fmaf(gr[k][e], v[k][e], d);
                     dots[s8 * 4 + c] = d;
                     // merged duplicates carry red weight 0 and send nothing
-                    if (keys[c] >= 0 && awc[c] != 0.f) {
+                    if (keys[c] >= 0 && awc[c] != 0.f && row_in_range(keys[c], num_keys)) {
                         float* gp = reinterpret_cast<float*>(
                             gvbase + (size_t)(unsigned)keys[c] * row_bytes32);
 #pragma unroll
@@ -640,7 +641,8 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                         const int vi = li + kk * kLanes;
 #pragma unroll
                         for (int e = 0; e < V; ++e) v[kk][e] = 0.f;
-                        if (keys[c] >= 0 && vi < nvec) IO<T>::load_vec(p + vi * 16, v[kk]);
+                        if (keys[c] >= 0 && vi < nvec && row_in_range(keys[c], num_keys))
+                            IO<T>::load_vec(p + vi * 16, v[kk]);
                     }
                     float d = 0.f;
 #pragma unroll
@@ -702,6 +704,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
 #pragma unroll 1
         for (int u = g; u < nu; u += G) {
             const int key = s_ukey[warp][u];
+            if (!row_in_range(key, num_keys)) continue;
             const float4 A4 = s_uA[warp][u];
             const float A[4] = {A4.x, A4.y, A4.z, A4.w};
             float* gp = reinterpret_cast<float*>(gvbase + (size_t)(unsigned)key * row_bytes32);

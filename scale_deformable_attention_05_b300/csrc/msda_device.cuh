@@ -42,11 +42,30 @@ constexpr int kMaxLevelPoints = 256;
 constexpr int kSamplesPerWarp = 64;
 
 // Set (atomicOr) by a kernel that meets a level whose pixels would fall
-// outside [0, num_keys); read and cleared by msda_last_device_error().
-// Defined here: all device code is compiled as the one translation unit
-// msda_kernels.cu (no relocatable device code).
+// outside [0, num_keys), or, in the checked build, a row index outside its
+// tensor; read and cleared by msda_last_device_error().  Defined here: all
+// device code is compiled as the one translation unit msda_kernels.cu (no
+// relocatable device code).
 __device__ unsigned int g_error_word = 0;
 constexpr unsigned int kErrLevelOutOfRange = 1u;
+constexpr unsigned int kErrRowOutOfRange = 2u;
+
+// Checked build (-DMSDA_BOUNDS_CHECK, the library's stand-in for a memory
+// sanitizer): every data-dependent value / grad_value row access first tests
+// its row index against [0, num_keys) and, outside it, records
+// kErrRowOutOfRange and skips the access.  The product build compiles the
+// test away.
+__device__ __forceinline__ bool row_in_range(int key, int num_keys) {
+#ifdef MSDA_BOUNDS_CHECK
+    if ((unsigned)key < (unsigned)num_keys) return true;
+    atomicOr(&g_error_word, kErrRowOutOfRange);
+    return false;
+#else
+    (void)key;
+    (void)num_keys;
+    return true;
+#endif
+}
 
 // ---------------------------------------------------------------- I/O traits
 template <typename T>

@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
                     const int vi = li + k * kLanes;
 #pragma unroll
                     for (int e = 0; e < V; ++e) v[c][k][e] = 0.f;
-                    if (keys[c] >= 0 && vi < nvec) VIO::load(p + vi * kVB, v[c][k]);
+                    if (keys[c] >= 0 && vi < nvec && row_in_range(keys[c], num_keys))
+                        VIO::load(p + vi * kVB, v[c][k]);
                 }
             }
 #pragma unroll

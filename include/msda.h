@@ -93,7 +93,9 @@ typedef enum {
     MSDA_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than msda_backward_workspace_bytes() */
     MSDA_ERR_CUDA = 6,          /* the CUDA runtime reported an error */
     MSDA_ERR_SHAPES = 7,        /* spatial_shapes / level_start_index inconsistent with num_keys */
-    MSDA_ERR_DEVICE_BOUNDS = 8  /* a kernel met an inconsistent level and skipped it */
+    MSDA_ERR_DEVICE_BOUNDS = 8  /* a kernel met an inconsistent level (or, in a library built
+                                   with MSDA_BOUNDS_CHECK, a row index outside its tensor)
+                                   and skipped it */
 } msda_status;
 
 /* Limits of this implementation.  The Ascend page's envelope ("约束说明":
@@ -228,8 +230,9 @@ MSDA_API int msda_check_shapes(const int64_t* spatial_shapes, const int64_t* lev
 /*
  * BLOCKING.  Synchronises `stream`, then returns MSDA_ERR_DEVICE_BOUNDS if
  * any kernel of this library on the current device met a level whose pixels
- * fall outside [0, num_keys) since the previous call, else MSDA_OK; clears
- * the word.
+ * fall outside [0, num_keys) since the previous call -- or, in a library built
+ * with -DMSDA_BOUNDS_CHECK, a value / grad_value row index outside the tensor
+ * (the access is skipped) -- else MSDA_OK; clears the word.
  */
 MSDA_API int msda_last_device_error(void* stream);
 
@@ -237,7 +240,7 @@ MSDA_API int msda_last_device_error(void* stream);
 MSDA_API const char* msda_status_string(int status);
 
 /*
- * Allocation-free bf16 backward.  No counterpart in the paper: an addition for
+ * Allocation-free bf16 backward.  Not part of the method: an addition for
  * callers that cannot allocate device memory (a host framework that owns every
  * allocation, a plug-in without access to the allocator, code that must not
  * call cudaMalloc while work is captured or timed).  Same arguments, results

@@ -94,7 +94,8 @@ const char* msda_status_string(int status) {
         case MSDA_ERR_SHAPES:
             return "spatial_shapes / level_start_index inconsistent with num_keys";
         case MSDA_ERR_DEVICE_BOUNDS:
-            return "a kernel skipped a level whose pixels fall outside [0, num_keys)";
+            return "a kernel skipped a level whose pixels fall outside [0, num_keys), or a row "
+                   "index outside its tensor (bounds-checked build)";
         default: return "unknown status";
     }
 }

@@ -177,6 +177,17 @@ def test_padding_mask_closed_form():
         fused.forward(value, sh, lsi, ref, off, logits))
 
 
+@pytest.mark.parametrize("ref_dim", [2, 4])
+def test_grad_value_is_the_adjoint_with_mask(ref_dim):
+    """Linear in value (masked or not): <out, G> = <value, grad_value>."""
+    v, sh, lsi, ref, off, logits, g = _problem(41 + ref_dim, ref_dim)
+    mask = np.random.default_rng(43).random(v.shape[:2]) < 0.3
+    out = fused.forward(v, sh, lsi, ref, off, logits, padding_mask=mask)
+    gv = fused.backward(v, sh, lsi, ref, off, logits, g, padding_mask=mask)[0]
+    np.testing.assert_allclose((v.astype(np.float64) * gv).sum(),
+                               (out * g.astype(np.float64)).sum(), rtol=1e-12)
+
+
 # ------------------------------------------------ planted mistakes must be caught
 def _mutant_locations_swapped(ref, off, shapes, exact=False):
     sh = np.asarray(shapes)[:, ::-1]                      # (H, W) rows read as (W, H)

@@ -421,3 +421,22 @@ def test_f16_rounding_is_round_to_nearest_even():
     assert bits[0] == 0x3C00 and bits[5] == 0x7BFF
     np.testing.assert_array_equal(gen.f16_bits_to_f32(bits),
                                   np.array([1.0, 1.0, 1.0 + 2 ** -9, 1.0, -2.5, 65504.0], np.float32))
+
+
+@pytest.mark.parametrize("exact", [False, True])
+def test_backward_is_the_adjoint_in_value_and_weights(exact):
+    """The operator is linear in value and in the attention weights, so its
+    gradients with respect to them are its adjoints: <out, G> must equal both
+    <value, grad_value> and <weights, grad_weights> for any G (random ragged
+    shapes, samples inside and outside the maps)."""
+    for seed, shapes in ((31, ((5, 7), (3, 2), (1, 1))), (32, ((9, 4), (4, 6)))):
+        wl = gen.random_workload(seed, 2, shapes, 3, 8, 5, 11)
+        inp = gen.make_inputs(wl)
+        args = (inp["value"], inp["spatial_shapes"], inp["level_start_index"],
+                inp["sampling_locations"], inp["attention_weights"])
+        out = oracle.forward(*args, exact_coords=exact)
+        gv, _, gw = oracle.backward(*args, inp["grad_output"], exact_coords=exact)
+        lhs = float((out * inp["grad_output"].astype(np.float64)).sum())
+        np.testing.assert_allclose((inp["value"].astype(np.float64) * gv).sum(), lhs, rtol=1e-12)
+        np.testing.assert_allclose((inp["attention_weights"].astype(np.float64) * gw).sum(), lhs,
+                                   rtol=1e-12)

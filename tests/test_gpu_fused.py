@@ -227,3 +227,51 @@ def test_fused_no_queries(B):
 def test_fused_f16_with_mask(B):
     wl = gen.random_workload(80, 2, ((9, 7), (5, 4)), 2, 64, 4, 11, dtype="f16")
     _run_and_check(B, wl, 4, mask_kind="detr")
+
+
+def _sweep_cases(n=12, seed=20260):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        L = int(rng.integers(1, 5))
+        P = int(rng.integers(1, 64 // L + 1))
+        shapes = tuple((int(rng.integers(1, 10)), int(rng.integers(1, 10))) for _ in range(L))
+        cases.append(dict(seed=300 + i, bs=int(rng.integers(1, 3)), shapes=shapes,
+                          M=int(rng.integers(1, 4)), D=int(rng.choice([8, 16, 32, 40, 64, 128])),
+                          P=P, Q=int(rng.integers(1, 20)),
+                          dtype=str(rng.choice(["f32", "bf16", "f16"])),
+                          ref_dim=int(rng.choice([2, 4])),
+                          mask=[None, "random", "detr"][int(rng.integers(0, 3))],
+                          idx32=bool(rng.integers(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("c", _sweep_cases(), ids=lambda c: f"seed{c['seed']}")
+def test_fused_random_sweep(B, c):
+    """Seeded sweep over levels, points (L*P <= 64), head_dim, heads, dtype,
+    reference width, padding mask and index width."""
+    wl = gen.random_workload(c["seed"], c["bs"], c["shapes"], c["M"], c["D"], c["P"], c["Q"],
+                             dtype=c["dtype"])
+    inp = gen.make_fused_inputs(wl, c["ref_dim"])
+    mask = _mask_for(wl, c["mask"])
+    names = ("value", "reference_points", "sampling_offsets", "attention_logits", "grad_output")
+    d = {k: _dev(inp, wl, k) for k in names}
+    index = torch.int32 if c["idx32"] else torch.int64
+    sh = torch.from_numpy(inp["spatial_shapes"]).to(index).cuda()
+    lsi = torch.from_numpy(inp["level_start_index"]).to(index).cuda()
+    dmask = None if mask is None else torch.from_numpy(mask).cuda()
+    args = (d["value"], sh, lsi, d["reference_points"], d["sampling_offsets"],
+            d["attention_logits"])
+    out = B.msda_forward_fused(*args, dmask)
+    gv, goff, glog, gref = B.msda_backward_fused(*args, d["grad_output"], dmask)
+    torch.cuda.synchronize()
+    assert B.msda_last_device_error() == 0
+    oargs = (inp["value"], inp["spatial_shapes"], inp["level_start_index"],
+             inp["reference_points"], inp["sampling_offsets"], inp["attention_logits"])
+    assert_out_close(host(out), ofused.forward(*oargs, padding_mask=mask), wl.dtype)
+    rv, roff, rlog, rref = ofused.backward(*oargs, inp["grad_output"], padding_mask=mask)
+    assert_grad_close(host(gv), rv, wl.dtype, "grad_value")
+    assert_grad_close(host(goff), roff, wl.dtype, "grad_sampling_offsets")
+    assert_grad_close(host(glog), rlog, wl.dtype, "grad_attn_logits")
+    assert_grad_close(host(gref), rref, wl.dtype, "grad_reference_points")
+    np.testing.assert_array_equal(np.any(host(gv) != 0, -1), np.any(rv != 0, -1))

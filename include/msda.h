@@ -165,9 +165,9 @@ MSDA_API int msda_backward(const void* value, const void* spatial_shapes,
  * and computes, per sample, a = softmax of its (b, q, m) row of logits and
  *   ref_dim 2: loc = ref + off / (W_l, H_l)
  *   ref_dim 4: loc = ref_xy + off / num_points * ref_wh * 0.5
- * in binary32, each operation rounded to nearest, with the reciprocals rounded
- * once: fl(ref + fl(off * fl(1/W))) and fl(ref_xy + fl(fl(off * w) *
- * fl(1/(2*num_points)))), then the same sum as msda_forward.
+ * in binary32, one correctly rounded operation at a time, left to right, with
+ * IEEE division: fl(ref + fl(off / W)) and fl(ref_xy + fl(fl(fl(off /
+ * num_points) * w) * 0.5)), then the same sum as msda_forward.
  *   key_padding_mask  [bs, num_keys] bytes (a torch.bool tensor), nonzero =
  *                     padded key, or NULL.  The module's masked_fill of value
  *                     (walk-through, "2.2.4", MSDeformAttn.forward) fused into

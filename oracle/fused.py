@@ -16,12 +16,12 @@ steps of ``MSDeformAttn.forward`` in the Deformable DETR walk-through
    key (b, k) is zero before sampling, so those rows contribute nothing and,
    through the masked_fill, receive no gradient.
 
-The locations decide which pixels are read, so they are formed in the same
-binary32 operations, in the same order, as the CUDA kernels take them (the
-reading of "where floating point decides an integer, both sides decide in the
-same precision"), dividing by multiplying with the once-rounded reciprocal:
-2-d: loc = fl(ref + fl(off * fl(1/W))); 4-d: loc = fl(ref_xy + fl(fl(off *
-ref_wh) * fl(1/(2P)))).  ``exact=True`` forms them in fp64 instead (for finite
+The locations decide which pixels are read, so the default mode takes the
+module's expression in binary32 exactly as written, one correctly rounded
+operation at a time, left to right, with IEEE division (the reading of "where
+floating point decides an integer, both sides decide in the same precision"):
+2-d: loc = fl(ref + fl(off / W)); 4-d: loc = fl(ref_xy + fl(fl(fl(off / P) *
+ref_wh) * 0.5)).  ``exact=True`` forms them in fp64 instead (for finite
 differences).  The backward is the chain rule through the same steps:
 
     grad_logits = a * (grad_a - sum_j a_j grad_a_j)          (softmax Jacobian)
@@ -57,13 +57,13 @@ def locations(reference_points: np.ndarray, sampling_offsets: np.ndarray,
     ft = np.float64 if exact else np.float32
     ref = ref.astype(ft)[:, :, None, :, None, :]              # [bs, Q, 1, L, 1, 2|4]
     off = off.astype(ft)
-    one = ft(1.0)
     if ref.shape[-1] == 2:
+        # offset_normalizer = stack([W, H]); each quotient rounded once
         norm = np.stack([np.asarray(spatial_shapes)[:, 1], np.asarray(spatial_shapes)[:, 0]], -1)
-        inv = one / norm.astype(ft)[None, None, None, :, None, :]   # fl(1/W), fl(1/H) per level
-        return ref + off * inv
+        return ref + off / norm.astype(ft)[None, None, None, :, None, :]
     if ref.shape[-1] == 4:
-        return ref[..., :2] + (off * ref[..., 2:]) * (one / ft(2 * P))
+        # off / n_points * ref_wh * 0.5, evaluated left to right
+        return ref[..., :2] + off / ft(P) * ref[..., 2:] * ft(0.5)
     raise ValueError("reference_points must end in 2 or 4")
 
 

@@ -66,8 +66,7 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
 template <int kSPG, int kStride, int kRef>
 __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* wax,
                                                  float4* woffwh, const SampleFetch& f,
-                                                 const PrepFetch& pf,
-                                                 const float2* s_inv, float inv_2p,
+                                                 const PrepFetch& pf, float points_f,
                                                  const unsigned char* __restrict__ mrow,
                                                  const LevelInfo* s_levels,
                                                  const unsigned char* s_level_of, int r0,
@@ -93,8 +92,8 @@ __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* 
             if constexpr (kRef != 0) {
                 if constexpr (kRef == 4)
                     woffwh[sg * kStride + sj] = make_float4(xy.x, xy.y, pf.rwh[h].x, pf.rwh[h].y);
-                const float2 inv = s_inv[l];
-                xy = prep_location<kRef>(pf.rxy[h], pf.rwh[h], xy, inv.x, inv.y, inv_2p);
+                xy = prep_location<kRef>(pf.rxy[h], pf.rwh[h], xy, (float)lv.W, (float)lv.H,
+                                         points_f);
             }
             Footprint fp = make_footprint(fmaf(xy.x, (float)lv.W, -0.5f),
                                           fmaf(xy.y, (float)lv.H, -0.5f), lv);
@@ -198,12 +197,13 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     constexpr int kBoxRecords = kRef == 4 ? Geom::kRecords : 1;
     __shared__ float4 s_offwh[kRef == 4 ? MSDA_BWD_WARPS : 1][kBoxRecords];
     __shared__ float4 s_gla[kPrep ? MSDA_BWD_WARPS : 1][kPrepRecords];
-    __shared__ float2 s_inv[kPrep ? kMaxLevels : 1];  // fl(1/W), fl(1/H) per level
 
     load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, idx32,
-                     num_levels, num_points, num_keys, kPrep ? s_inv : nullptr);
+                     num_levels, num_points, num_keys);
     __syncthreads();
+    // 1 / (2P): the derivative of the 4-d location along the offset is ref_wh / (2P)
     const float inv_2p = kPrep ? __frcp_rn((float)(2 * num_points)) : 0.f;
+    const float points_f = (float)num_points;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / kLanes, li = lane % kLanes;
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
         if constexpr (kPrep) fetch_refs<T, kRef>(pf, f, ref, tc, num_queries, num_levels, pl);
         if constexpr (kPrep) softmax_rows<kSPG>(f);
         backward_records<kSPG, kStride, kRef>(
-            wk, waw, wax, woffwh, f, pf, s_inv, inv_2p,
+            wk, waw, wax, woffwh, f, pf, points_f,
             mask ? mask + (int64_t)tc.b * num_keys : nullptr, s_levels, s_level_of, it.r0, lane,
             dedup);
         __syncwarp();

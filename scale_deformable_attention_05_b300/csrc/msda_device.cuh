@@ -358,7 +358,7 @@ __device__ __forceinline__ void load_level_table(LevelInfo* s_levels, unsigned c
                                                  const void* __restrict__ spatial_shapes,
                                                  const void* __restrict__ level_start_index,
                                                  int idx32, int num_levels, int num_points,
-                                                 int num_keys, float2* s_inv = nullptr) {
+                                                 int num_keys) {
     if (threadIdx.x < num_levels) {
         const int l = threadIdx.x;
         const int64_t H = index_at(spatial_shapes, 2 * l, idx32);
@@ -372,7 +372,6 @@ __device__ __forceinline__ void load_level_table(LevelInfo* s_levels, unsigned c
         li.start = ok ? (int)s : 0;
         li.ok = ok;
         s_levels[l] = li;
-        if (s_inv) s_inv[l] = make_float2(__frcp_rn((float)li.W), __frcp_rn((float)li.H));
         if (!ok && blockIdx.x == 0) atomicOr(&g_error_word, kErrLevelOutOfRange);
     }
     const int LP = num_levels * num_points;
@@ -588,18 +587,21 @@ __device__ __forceinline__ void prefetch_refs(const SampleFetch& f, const T* __r
         if (f.ok[h]) asm volatile("prefetch.global.L1 [%0];" ::"l"(rt + pl.ref_off[h]));
 }
 
-// Sampling location of one sample, in the binary32 operations (each rounded
-// to nearest) the oracle replays, with the reciprocals rounded once:
-//   2-d: loc = ref + off * fl(1/W)           (ref + off / (W, H))
-//   4-d: loc = ref_xy + (off * ref_wh) * fl(1/(2P))   (ref_xy + off / P * ref_wh * 0.5)
+// Sampling location of one sample: the module's expression (Deformable DETR
+// walk-through, "2.2.4 源码分析", MSDeformAttn.forward; 4-d references from
+// section "2.4") in binary32, one correctly rounded operation at a time, left
+// to right, with IEEE division:
+//   2-d: loc = ref + off / (W, H)
+//   4-d: loc = ref_xy + off / P * ref_wh * 0.5
+// w, h: the level's width and height; p: the number of points (exact floats).
 template <int kRef>
-__device__ __forceinline__ float2 prep_location(float2 rxy, float2 rwh, float2 off,
-                                                float inv_w, float inv_h, float inv_2p) {
+__device__ __forceinline__ float2 prep_location(float2 rxy, float2 rwh, float2 off, float w,
+                                                float h, float p) {
     if constexpr (kRef == 2)
-        return make_float2(__fadd_rn(rxy.x, __fmul_rn(off.x, inv_w)),
-                           __fadd_rn(rxy.y, __fmul_rn(off.y, inv_h)));
-    return make_float2(__fadd_rn(rxy.x, __fmul_rn(__fmul_rn(off.x, rwh.x), inv_2p)),
-                       __fadd_rn(rxy.y, __fmul_rn(__fmul_rn(off.y, rwh.y), inv_2p)));
+        return make_float2(__fadd_rn(rxy.x, __fdiv_rn(off.x, w)),
+                           __fadd_rn(rxy.y, __fdiv_rn(off.y, h)));
+    return make_float2(__fadd_rn(rxy.x, __fmul_rn(__fmul_rn(__fdiv_rn(off.x, p), rwh.x), 0.5f)),
+                       __fadd_rn(rxy.y, __fmul_rn(__fmul_rn(__fdiv_rn(off.y, p), rwh.y), 0.5f)));
 }
 
 // Replaces the logits in f.a by the softmax over each row's L*P samples.  A

@@ -45,8 +45,7 @@ namespace msda {
 // the location is formed from pf's reference point first.
 template <int kSPG, int kStride, int kRef>
 __device__ __forceinline__ void forward_records(int4* wk, float4* ww, const SampleFetch& f,
-                                                const PrepFetch& pf,
-                                                const float2* s_inv, float inv_2p,
+                                                const PrepFetch& pf, float points_f,
                                                 const unsigned char* __restrict__ mrow,
                                                 const LevelInfo* s_levels,
                                                 const unsigned char* s_level_of, int r0,
@@ -62,8 +61,8 @@ __device__ __forceinline__ void forward_records(int4* wk, float4* ww, const Samp
             const float a = f.a[h];
             float2 xy = f.xy[h];
             if constexpr (kRef != 0) {
-                const float2 inv = s_inv[s_level_of[r0 + sj]];
-                xy = prep_location<kRef>(pf.rxy[h], pf.rwh[h], xy, inv.x, inv.y, inv_2p);
+                xy = prep_location<kRef>(pf.rxy[h], pf.rwh[h], xy, (float)lv.W, (float)lv.H,
+                                         points_f);
             }
             Footprint fp = make_footprint(fmaf(xy.x, (float)lv.W, -0.5f),
                                           fmaf(xy.y, (float)lv.H, -0.5f), lv);
@@ -120,18 +119,17 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
                                 : MSDA_FWD_UNROLL;
     __shared__ LevelInfo s_levels[kMaxLevels];
     __shared__ unsigned char s_level_of[kMaxLevelPoints];
-    __shared__ float2 s_inv[kPrep ? kMaxLevels : 1];  // fl(1/W), fl(1/H) per level
     constexpr int kWarps = MSDA_FWD_WARPS;
     __shared__ int4 s_key[kWarps][Geom::kRecords];
     __shared__ float4 s_w[kWarps][Geom::kRecords];
 
     load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, idx32,
-                     num_levels, num_points, num_keys, kPrep ? s_inv : nullptr);
+                     num_levels, num_points, num_keys);
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / kLanes, li = lane % kLanes;
-    const float inv_2p = kPrep ? __frcp_rn((float)(2 * num_points)) : 0.f;
+    const float points_f = (float)num_points;
     const int LP = num_levels * num_points;
     const int nvec = head_dim / V;
     const unsigned row_bytes = (unsigned)(num_heads * head_dim) * (unsigned)sizeof(T);
@@ -164,7 +162,7 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
         if constexpr (kPrep) fetch_refs<T, kRef>(pf, f, ref, tc, num_queries, num_levels, pl);
         if constexpr (kPrep) softmax_rows<kSPG>(f);
         forward_records<kSPG, kStride, kRef>(
-            wk, ww, f, pf, s_inv, inv_2p, mask ? mask + (int64_t)tc.b * num_keys : nullptr,
+            wk, ww, f, pf, points_f, mask ? mask + (int64_t)tc.b * num_keys : nullptr,
             s_levels, s_level_of, it.r0, lane);
         __syncwarp();
         const TileCoord cur = tc;

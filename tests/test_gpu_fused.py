@@ -94,6 +94,96 @@ def test_fused_encoder_shape(B):
     _run_and_check(B, wl, 2, sigma=1.5)
 
 
+EDGE_SHAPES = ((6, 7), (5, 21), (3, 167))          # widths with inexact reciprocals
+
+
+def _cell(loc, W):
+    """Cell column of a binary32 location: floor of fl(loc * W - 0.5) (one rounding)."""
+    x = (np.asarray(loc, np.float64) * W - 0.5).astype(np.float32)
+    return np.floor(x)
+
+
+def _edge_case_inputs(ref_dim, seed=81, Q=4, M=2, P=3, D=32):
+    """Fused inputs whose every sample lies on a cell edge in x, placed so that
+    the module's expression with correctly rounded division (walk-through
+    "2.2.4 源码分析": off / (W, H); "2.4": off / P * wh * 0.5) picks one cell and
+    the same expression with once-rounded reciprocals picks its neighbour.  The
+    bilinear derivative along x jumps between the two cells, so the offset
+    gradient tells which form a kernel computed.  Returns the inputs and the
+    reciprocal form's cells next to the division form's."""
+    f = np.float32
+    rng = np.random.default_rng(seed)
+    L = len(EDGE_SHAPES)
+    ref = np.empty((1, Q, L, ref_dim), f)
+    off = np.zeros((1, Q, M, L, P, 2), f)
+    cells_div = np.zeros((1, Q, M, L, P))
+    cells_rec = np.zeros((1, Q, M, L, P))
+    for q in range(Q):
+        for l, (H, W) in enumerate(EDGE_SHAPES):
+            ref[0, q, l, 1] = (rng.integers(0, H) + 0.5 + 0.3) / H       # mid-cell in y
+            if ref_dim == 4:
+                ref[0, q, l, 2:] = rng.choice([0.375, 0.6875, 0.9375], 2)
+            wh = ref[0, q, l, 2] if ref_dim == 4 else f(1)
+            hits = []
+            for _ in range(200):            # a reference x that admits at least one edge
+                rx = ref[0, q, l, 0] = rng.uniform(0.1, 0.9)
+                rx = ref[0, q, l, 0]
+                if ref_dim == 2:
+                    form = lambda o: (f(rx + f(o / f(W))), f(rx + f(o * f(f(1) / f(W)))))
+                    scale = float(W)
+                else:
+                    form = lambda o: (f(rx + f(f(f(o / f(P)) * wh) * f(0.5))),
+                                      f(rx + f(f(o * wh) * f(f(1) / f(2 * P)))))
+                    scale = 2.0 * P / float(wh)
+                for n in range(1, W - 1):
+                    o = f((float(n + 0.5) / W - float(rx)) * scale)
+                    for _ in range(24):
+                        o = np.nextafter(o, f(np.inf))
+                        ld, lr = form(o)
+                        if _cell(ld, W) != _cell(lr, W):
+                            hits.append((o, _cell(ld, W), _cell(lr, W)))
+                            break
+                if hits:
+                    break
+            assert hits, "no edge sample found"
+            for i, (m, p) in enumerate(np.ndindex(M, P)):
+                o, cd, cr = hits[i % len(hits)]
+                off[0, q, m, l, p, 0] = o
+                cells_div[0, q, m, l, p] = cd
+                cells_rec[0, q, m, l, p] = cr
+    value = rng.standard_normal((1, gen.num_keys(EDGE_SHAPES), M, D)).astype(f)
+    logits = rng.standard_normal((1, Q, M, L * P)).astype(f)
+    g = rng.standard_normal((1, Q, M * D)).astype(f)
+    inp = {"value": value, "spatial_shapes": np.array(EDGE_SHAPES, np.int64),
+           "level_start_index": gen.level_start_index(EDGE_SHAPES), "reference_points": ref,
+           "sampling_offsets": off, "attention_logits": logits, "grad_output": g}
+    return inp, cells_div, cells_rec
+
+
+@pytest.mark.parametrize("ref_dim", [2, 4])
+def test_fused_locations_divide_on_cell_edges(B, ref_dim):
+    """The kernels form locations with IEEE division, as the oracle does: on
+    samples where a reciprocal product would land one cell over, the offset
+    gradients still agree."""
+    inp, cells_div, cells_rec = _edge_case_inputs(ref_dim)
+    assert (cells_div != cells_rec).all()
+    oargs = tuple(inp[k] for k in ("value", "spatial_shapes", "level_start_index",
+                                   "reference_points", "sampling_offsets", "attention_logits"))
+    t = lambda k: torch.from_numpy(np.ascontiguousarray(inp[k])).cuda()
+    args = (t("value"), t("spatial_shapes"), t("level_start_index"), t("reference_points"),
+            t("sampling_offsets"), t("attention_logits"))
+    out = B.msda_forward_fused(*args)
+    gv, goff, glog, gref = B.msda_backward_fused(*args, t("grad_output"))
+    torch.cuda.synchronize()
+    assert_out_close(host(out), ofused.forward(*oargs), "f32")
+    rv, roff, rlog, rref = ofused.backward(*oargs, inp["grad_output"])
+    assert_grad_close(host(goff), roff, "f32", "grad_sampling_offsets")
+    assert_grad_close(host(glog), rlog, "f32", "grad_attn_logits")
+    assert_grad_close(host(gv), rv, "f32", "grad_value")
+    np.testing.assert_array_equal(np.any(host(gv) != 0, -1), np.any(rv != 0, -1))
+    empty_cache()
+
+
 MASK_CASES = [
     ("pyramid-scattered", 71, 2, ((9, 7), (5, 4), (3, 2), (2, 1)), 3, 32, 4, 17, "f32", 2,
      "random"),

@@ -91,6 +91,51 @@ def test_four_d_references_with_matching_box_equal_the_two_d_form():
     np.testing.assert_allclose(b4[3][..., :2], b2[3], rtol=1e-12, atol=1e-12)
 
 
+NPOT_SHAPES = ((7, 21), (5, 13), (3, 9))       # no power of two: 1/W is inexact
+
+
+def _npot_offsets(ref_dim, seed=17, Q=8, M=2, P=7):
+    """Offsets whose quotients in the module's expression are short binary
+    fractions: 2-d off = (W, H) * t, 4-d off = P * t, t = k / 64.  The real
+    arithmetic of the walk-through's MSDeformAttn.forward ("2.2.4 源码分析": off /
+    (W, H); "2.4": off / P * wh * 0.5) then gives loc = ref + t and
+    ref_xy + t * wh / 2 exactly, and so must binary32 with correctly rounded
+    division."""
+    rng = np.random.default_rng(seed)
+    L = len(NPOT_SHAPES)
+    t = rng.integers(1, 256, (1, Q, M, L, P, 2)) / 64.0
+    if ref_dim == 2:
+        ref = rng.choice([0.0, 0.125, 0.25], (1, Q, L, 2))
+        scale = np.array([[W, H] for H, W in NPOT_SHAPES], np.float64)[None, None, None, :, None]
+        want = ref[:, :, None, :, None, :] + t
+    else:
+        xy = np.zeros((1, Q, L, 2))
+        wh = rng.choice([0.375, 0.6875, 0.9375], (1, Q, L, 2))
+        ref = np.concatenate([xy, wh], -1)
+        scale = np.float64(P)
+        want = t * wh[:, :, None, :, None, :] * 0.5
+    off = t * scale
+    assert np.array_equal(off.astype(np.float32).astype(np.float64), off)   # exact inputs
+    return ref.astype(np.float32), off.astype(np.float32), want
+
+
+@pytest.mark.parametrize("ref_dim", [2, 4])
+def test_locations_divide_as_the_module_writes(ref_dim):
+    ref, off, want = _npot_offsets(ref_dim)
+    loc = fused.locations(ref, off, np.array(NPOT_SHAPES))
+    assert loc.dtype == np.float32
+    np.testing.assert_array_equal(loc.astype(np.float64), want)
+    # the pin discriminates: products with once-rounded reciprocals miss some of them
+    f = np.float32
+    if ref_dim == 2:
+        inv = f(1) / np.array([[W, H] for H, W in NPOT_SHAPES], f)[None, None, None, :, None]
+        recip = ref[:, :, None, :, None, :] + off * inv
+    else:
+        recip = ref[:, :, None, :, None, :2] + (off * ref[:, :, None, :, None, 2:]) * (
+            f(1) / f(2 * off.shape[4]))
+    assert (recip.astype(np.float64) != want).any()
+
+
 def _pixel_coords(ref, off, shapes):
     loc = fused.locations(ref, off, shapes, exact=True)
     W = np.asarray(shapes)[:, 1].astype(np.float64)[None, None, None, :, None]
@@ -201,6 +246,19 @@ def _mutant_locations_no_half(ref, off, shapes, exact=False):
     return _ORIG_LOCATIONS(ref, off, shapes, exact)
 
 
+def _mutant_locations_reciprocal(ref, off, shapes, exact=False):
+    """Divides by multiplying with once-rounded reciprocals (1/W, 1/H, 1/(2P))."""
+    ref = np.asarray(ref)
+    f = np.float64 if exact else np.float32
+    r = ref.astype(f)[:, :, None, :, None, :]
+    o = np.asarray(off).astype(f)
+    if ref.shape[-1] == 2:
+        sh = np.asarray(shapes)
+        inv = f(1) / np.stack([sh[:, 1], sh[:, 0]], -1).astype(f)[None, None, None, :, None, :]
+        return r + o * inv
+    return r[..., :2] + (o * r[..., 2:]) * (f(1) / f(2 * o.shape[4]))
+
+
 def _mutant_softmax_wrong_axis(logits, L, P):
     z = np.asarray(logits, np.float64)
     e = np.exp(z - z.max(axis=2, keepdims=True))
@@ -216,6 +274,12 @@ def _mutant_mask_grad_kept(grad_value, keep):
     return grad_value                                     # padded rows keep their gradient
 
 
+def _npot_locations_exact(ref_dim):
+    ref, off, want = _npot_offsets(ref_dim)
+    np.testing.assert_array_equal(
+        fused.locations(ref, off, np.array(NPOT_SHAPES)).astype(np.float64), want)
+
+
 _ORIG_LOCATIONS = fused.locations
 _ORIG_KEEP = fused.keep_rows
 
@@ -229,6 +293,8 @@ def _battery():
         test_integer_offsets_shift_by_whole_pixels()
         test_four_d_references_with_matching_box_equal_the_two_d_form()
         for rd in (2, 4):
+            _npot_locations_exact(rd)
+        for rd in (2, 4):
             test_backward_matches_central_differences(rd)
         test_padding_mask_closed_form()
     except AssertionError:
@@ -239,6 +305,7 @@ def _battery():
 @pytest.mark.parametrize("name,attr,mutant", [
     ("normaliser_transposed", "locations", _mutant_locations_swapped),
     ("box_half_dropped", "locations", _mutant_locations_no_half),
+    ("reciprocal_instead_of_division", "locations", _mutant_locations_reciprocal),
     ("softmax_over_heads", "softmax_weights", _mutant_softmax_wrong_axis),
     ("mask_batch_flipped", "keep_rows", _mutant_mask_batch_flipped),
     ("mask_gradient_kept", "masked_fill_grad", _mutant_mask_grad_kept),

@@ -653,6 +653,40 @@ def run_native(args, wl):
     return 0
 
 
+CEILING_PROBES = [
+    # (name, probe, param, CTAs of 16 warps per SM)
+    ("gather_ldg128_l1", 0, 64 << 10, 2), ("gather_ldg128_l1", 0, 64 << 10, 4),
+    ("gather_ldg128_l2", 0, 64 << 20, 2), ("gather_ldg128_l2", 0, 64 << 20, 4),
+    ("gather_ldg256_l1", 1, 64 << 10, 4), ("gather_ldg256_l2", 1, 64 << 20, 4),
+    ("gather_lds128", 2, 0, 2), ("gather_lds128", 2, 0, 3),
+    ("red_shared_f32_conflict_free", 3, 0, 2), ("red_shared_f32_4way", 3, 1, 2),
+    ("red_shared_f32_stride33", 3, 2, 2), ("rmw_shared_f32_conflict_free", 5, 0, 2),
+    ("red_global_v4_l2", 4, 64 << 20, 2), ("red_global_v4_l2", 4, 64 << 20, 4),
+]
+
+
+def run_ceiling(iters=2048):
+    """On-chip ceilings of the row gathers and scatters (csrc/msda_ceiling.cu), one
+    JSON line per probe: random 128-byte rows per SM clock."""
+    import ctypes
+    from scale_deformable_attention_05_b300 import build as lib_build
+    lib = ctypes.CDLL(lib_build.build_ceiling())
+    lib.msda_ceiling_run.argtypes = [ctypes.c_int, ctypes.c_longlong, ctypes.c_int, ctypes.c_int,
+                                     ctypes.POINTER(ctypes.c_double)]
+    lib.msda_ceiling_run.restype = ctypes.c_int
+    for name, probe, param, ctas in CEILING_PROBES:
+        out = (ctypes.c_double * 4)()
+        rc = lib.msda_ceiling_run(probe, param, ctas, iters, out)
+        if rc != 0:
+            raise RuntimeError(f"ceiling probe {name} failed with CUDA error {rc}")
+        print(json.dumps({"ceiling": name, "warps_per_sm": 16 * ctas, "param": param,
+                          "rows_per_clk_per_sm": round(out[0], 4),
+                          "bytes_per_clk_per_sm": round(out[0] * 128, 1),
+                          "ms": round(out[1], 4), "sm_mhz": round(out[2], 1),
+                          "rows": out[3]}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -671,7 +705,12 @@ def main():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every pass through the Python binding instead of replaying "
                          "its captured CUDA graph")
+    ap.add_argument("--ceiling", action="store_true",
+                    help="print the on-chip gather / scatter ceilings (one JSON line per probe) "
+                         "instead of the benchmark line")
     args = ap.parse_args()
+    if args.ceiling:
+        return run_ceiling()
     # timing rule: at least three untimed warm-up steps
     args.warmup = max(args.warmup, 3)
     wl = gen.WORKLOADS[args.workload]

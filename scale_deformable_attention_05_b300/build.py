@@ -60,6 +60,25 @@ def build_checked(force: bool = False, verbose: bool = False) -> str:
                  lib=CHECKED_LIB)
 
 
+CEILING_LIB = os.path.join(PKG, "libmsda_ceiling.so")
+CEILING_SRC = os.path.join(CSRC, "msda_ceiling.cu")
+
+
+def build_ceiling(force: bool = False, verbose: bool = False) -> str:
+    """The on-chip ceiling probes (a measurement tool, not part of the ABI)."""
+    if (not force and os.path.exists(CEILING_LIB)
+            and os.path.getmtime(CEILING_LIB) >= os.path.getmtime(CEILING_SRC)):
+        return CEILING_LIB
+    tmp = CEILING_LIB + ".tmp"
+    cmd = [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
+           "-Xcompiler", "-fvisibility=hidden", "-cudart", "static", "-o", tmp, CEILING_SRC]
+    if verbose:
+        print(" ".join(cmd), file=sys.stderr)
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, CEILING_LIB)
+    return CEILING_LIB
+
+
 if __name__ == "__main__":
     args = sys.argv[1:]
     extra = [a for a in args if a not in ("--force",)]

@@ -37,8 +37,34 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
     dwy = cy ? wx : -wx;
 }
 
-#ifndef MSDA_BWD_MIN_BLOCKS
-#define MSDA_BWD_MIN_BLOCKS 2
+// CTA shape of backward_kernel.  The plain path with lane groups of at most 8
+// lanes and one vector per lane (head_dim <= 32) runs 3 resident CTAs of 8
+// warps per SM (80 registers per thread; measured against one CTA of 16 warps
+// with 128 registers: encoder fp32 452 -> 440 us, bf16 1073 -> 925 us, fp16
+// 1034 -> 918 us); wider rows and the fused entry points, whose state does not
+// fit 80 registers, keep one CTA of 16 warps.
+#ifndef MSDA_BWD_NARROW_WARPS
+#define MSDA_BWD_NARROW_WARPS 8
+#endif
+#ifndef MSDA_BWD_NARROW_BLOCKS
+#define MSDA_BWD_NARROW_BLOCKS 3
+#endif
+template <int kLanes, int kVPL, int kRef>
+struct BwdShape {
+    static constexpr bool kNarrow = kLanes <= 8 && kVPL == 1 && kRef == 0;
+    static constexpr int kWarps = kNarrow ? MSDA_BWD_NARROW_WARPS : MSDA_BWD_WARPS;
+    static constexpr int kMinBlocks = kNarrow ? MSDA_BWD_NARROW_BLOCKS : 1;
+};
+// backward_merge_kernel: one CTA of MSDA_MERGE_WARPS warps per SM (its 1 KB
+// rows measured 10% slower with 24 warps of 80 registers).
+#ifndef MSDA_MERGE_WARPS
+#define MSDA_MERGE_WARPS 16
+#endif
+
+// Locations, weights and grad_output rows of the next round loaded during this
+// round's gathers (1), or at the start of their round (0, fewer live registers).
+#ifndef MSDA_BWD_PREFETCH
+#define MSDA_BWD_PREFETCH 1
 #endif
 
 // Samples per transpose-reduce of the corner dot products (raised to kLanes / 4
@@ -163,10 +189,8 @@ __device__ __forceinline__ void load_grad_row(float (&gr)[kVPL][VecIO<T, kVB>::k
 // each covering half of every 32-byte sector of the row; the bf16 encoder
 // backward measured 1298 us that way against 1207 us with 8-byte vectors.)
 template <typename T, int kLanes, int kVPL, int kRef, int kVB>
-__global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
-                                  MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS > 0
-                                      ? MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS
-                                      : 1)
+__global__ void __launch_bounds__(BwdShape<kLanes, kVPL, kRef>::kWarps * 32,
+                                  BwdShape<kLanes, kVPL, kRef>::kMinBlocks)
     backward_kernel(const T* __restrict__ value, const void* __restrict__ spatial_shapes,
                     const void* __restrict__ level_start_index, int idx32, const T* __restrict__ loc,
                     const T* __restrict__ attn, const T* __restrict__ grad_out,
@@ -176,6 +200,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
                     int num_tiles, int tiles_per_cta, const T* __restrict__ ref,
                     const unsigned char* __restrict__ mask, float* __restrict__ grad_ref) {
     constexpr bool kPrep = kRef != 0;
+    constexpr int kWarps = BwdShape<kLanes, kVPL, kRef>::kWarps;
     using Geom = TileGeom<kLanes>;
     using VIO = VecIO<T, kVB>;
     constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
@@ -189,14 +214,14 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
 
     __shared__ LevelInfo s_levels[kMaxLevels];
     __shared__ unsigned char s_level_of[kMaxLevelPoints];
-    __shared__ int4 s_key[MSDA_BWD_WARPS][Geom::kRecords];
-    __shared__ float4 s_aw[MSDA_BWD_WARPS][Geom::kRecords];
-    __shared__ float4 s_aux[MSDA_BWD_WARPS][Geom::kRecords];
+    __shared__ int4 s_key[kWarps][Geom::kRecords];
+    __shared__ float4 s_aw[kWarps][Geom::kRecords];
+    __shared__ float4 s_aux[kWarps][Geom::kRecords];
     // fused mode: per sample (offset, box size) for 4-d references, (grad_loc, grad_a)
     constexpr int kPrepRecords = kPrep ? Geom::kRecords : 1;
     constexpr int kBoxRecords = kRef == 4 ? Geom::kRecords : 1;
-    __shared__ float4 s_offwh[kRef == 4 ? MSDA_BWD_WARPS : 1][kBoxRecords];
-    __shared__ float4 s_gla[kPrep ? MSDA_BWD_WARPS : 1][kPrepRecords];
+    __shared__ float4 s_offwh[kRef == 4 ? kWarps : 1][kBoxRecords];
+    __shared__ float4 s_gla[kPrep ? kWarps : 1][kPrepRecords];
 
     load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, idx32,
                      num_levels, num_points, num_keys);
@@ -227,20 +252,29 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     it.r0 = 0;
     it.LP = LP;
     it.spg = kSPG;
-    it.stride = MSDA_BWD_WARPS;
+    it.stride = kWarps;
     if (!it.valid()) return;
 
+    constexpr bool kPrefetch = MSDA_BWD_PREFETCH != 0 || kPrep;
     SampleFetch f;
     PrepFetch pf;
     TileCoord tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
-    fetch_samples<T, kSPG>(f, loc, attn, tc, 0, lane, LP, num_queries, num_heads);
     PrepLane pl;
     if constexpr (kPrep) pl = prep_lane<kSPG>(lane, num_levels, LP, kRef, s_level_of);
     float gr[kVPL][V], gnext[kVPL][V];
-    load_grad_row<T, kLanes, kVPL, kVB>(gnext, grad_out, tc, g, li, nvec, num_queries, num_heads,
-                                   head_dim);
+    if constexpr (kPrefetch) {
+        fetch_samples<T, kSPG>(f, loc, attn, tc, 0, lane, LP, num_queries, num_heads);
+        load_grad_row<T, kLanes, kVPL, kVB>(gnext, grad_out, tc, g, li, nvec, num_queries,
+                                            num_heads, head_dim);
+    }
 
     while (true) {
+        if constexpr (!kPrefetch) {
+            fetch_samples<T, kSPG>(f, loc, attn, tc, it.r0, lane, LP, num_queries, num_heads);
+            if (it.r0 == 0)
+                load_grad_row<T, kLanes, kVPL, kVB>(gr, grad_out, tc, g, li, nvec, num_queries,
+                                                    num_heads, head_dim);
+        }
         // ---- 1. footprints of this round (inputs fetched, references prefetched, a round ahead)
         if constexpr (kPrep) fetch_refs<T, kRef>(pf, f, ref, tc, num_queries, num_levels, pl);
         if constexpr (kPrep) softmax_rows<kSPG>(f);
@@ -251,7 +285,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
         __syncwarp();
         const TileCoord cur = tc;
         const int r0 = it.r0;
-        if (r0 == 0) {
+        if (kPrefetch && r0 == 0) {
 #pragma unroll
             for (int k = 0; k < kVPL; ++k)
 #pragma unroll
@@ -261,11 +295,15 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
         const bool more = it.valid();
         if (more) {
             tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);
-            fetch_samples<T, kSPG>(f, loc, attn, tc, it.r0, lane, LP, num_queries, num_heads);
-            if constexpr (kPrep) prefetch_refs<T, kRef>(f, ref, tc, num_queries, num_levels, pl);
-            if (it.r0 == 0)
-                load_grad_row<T, kLanes, kVPL, kVB>(gnext, grad_out, tc, g, li, nvec, num_queries,
-                                               num_heads, head_dim);
+            if constexpr (kPrefetch) {
+                fetch_samples<T, kSPG>(f, loc, attn, tc, it.r0, lane, LP, num_queries,
+                                       num_heads);
+                if constexpr (kPrep)
+                    prefetch_refs<T, kRef>(f, ref, tc, num_queries, num_levels, pl);
+                if (it.r0 == 0)
+                    load_grad_row<T, kLanes, kVPL, kVB>(gnext, grad_out, tc, g, li, nvec,
+                                                        num_queries, num_heads, head_dim);
+            }
         }
 
         const int64_t head0 = ((int64_t)cur.b * num_keys * num_heads + cur.m) * head_dim;
@@ -445,10 +483,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
 // queries).  The location and weight gradients come from the corner dot
 // products as in backward_kernel, each group handling its own query's samples.
 template <typename T, int kLanes, int kVPL>
-__global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
-                                  MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS > 0
-                                      ? MSDA_BWD_MIN_BLOCKS * 8 / MSDA_BWD_WARPS
-                                      : 1)
+__global__ void __launch_bounds__(MSDA_MERGE_WARPS * 32, 1)
     backward_merge_kernel(const T* __restrict__ value, const void* __restrict__ spatial_shapes,
                           const void* __restrict__ level_start_index, int idx32,
                           const T* __restrict__ loc, const T* __restrict__ attn,
@@ -469,10 +504,10 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
 
     __shared__ LevelInfo s_levels[kMaxLevels];
     __shared__ unsigned char s_level_of[kMaxLevelPoints];
-    __shared__ int4 s_key[MSDA_BWD_WARPS][32];       // corner keys (corner order) per round sample
-    __shared__ float4 s_aux[MSDA_BWD_WARPS][32];     // (a, fx, fy, level) per round sample
-    __shared__ int s_ukey[MSDA_BWD_WARPS][kMaxUnique];
-    __shared__ float4 s_uA[MSDA_BWD_WARPS][kMaxUnique];
+    __shared__ int4 s_key[MSDA_MERGE_WARPS][32];       // corner keys (corner order) per round sample
+    __shared__ float4 s_aux[MSDA_MERGE_WARPS][32];     // (a, fx, fy, level) per round sample
+    __shared__ int s_ukey[MSDA_MERGE_WARPS][kMaxUnique];
+    __shared__ float4 s_uA[MSDA_MERGE_WARPS][kMaxUnique];
 
     load_level_table(s_levels, s_level_of, spatial_shapes, level_start_index, idx32,
                      num_levels, num_points, num_keys);
@@ -493,7 +528,7 @@ __global__ void __launch_bounds__(MSDA_BWD_WARPS * 32,
     it.r0 = 0;
     it.LP = S;
     it.spg = 32;
-    it.stride = MSDA_BWD_WARPS;
+    it.stride = MSDA_MERGE_WARPS;
     if (!it.valid()) return;
 
     // round sample s = r0 + lane  ->  (level, query, point)

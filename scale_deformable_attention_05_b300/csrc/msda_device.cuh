@@ -458,10 +458,21 @@ __device__ __forceinline__ const char* row_ptr(const char* base, int key, unsign
 }
 
 // Fire-and-forget vector fp32 add into global memory (sm_90+ vector red).
+// No "memory" clobber unless MSDA_RED_CLOBBER: the kernels that call it never
+// read the buffer they add into, and without the clobber the compiler may
+// schedule the gathers of later samples ahead of these reds.
+#ifndef MSDA_RED_CLOBBER
+#define MSDA_RED_CLOBBER 0
+#endif
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+#if MSDA_RED_CLOBBER
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b),
                  "f"(c), "f"(d)
                  : "memory");
+#else
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b),
+                 "f"(c), "f"(d));
+#endif
 }
 
 // Geometry of a warp tile for lane groups of kLanes lanes.

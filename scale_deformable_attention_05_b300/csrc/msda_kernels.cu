@@ -126,13 +126,13 @@ int persistent_waves(const Problem& pb, int elem_bytes, bool backward) {
 
 // CTAs of `kernel` that fit on one SM at once (looked up once per kernel).
 template <typename K>
-int resident_ctas(K kernel, int threads) {
+int resident_ctas(K kernel, int threads, size_t dynamic_smem = 0) {
     static const int n = [&] {
         if (MSDA_SMEM_CARVEOUT >= 0)
             cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  MSDA_SMEM_CARVEOUT);
         int v = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, 0) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, dynamic_smem) !=
                 cudaSuccess ||
             v < 1)
             v = 1;
@@ -180,9 +180,10 @@ cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv
                               void* grad_loc, void* grad_attn, cudaStream_t st,
                               float* grad_ref = nullptr) {
     auto kernel = backward_kernel<T, kLanes, kVPL, kRef, kVB>;
-    constexpr int kThreads = MSDA_BWD_WARPS * 32;
+    constexpr int kWarps = BwdShape<kLanes, kVPL, kRef>::kWarps;
+    constexpr int kThreads = kWarps * 32;
     const TileGrid tg =
-        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS,
+        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), kWarps,
                   persistent_waves(pb, (int)sizeof(T), true));
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
@@ -272,9 +273,9 @@ cudaError_t launch_backward_merge_t(const Problem& pb, int log2_points, const vo
                                     float* gv32, void* grad_loc, void* grad_attn,
                                     cudaStream_t st) {
     auto kernel = backward_merge_kernel<T, kLanes, kVPL>;
-    constexpr int kThreads = MSDA_BWD_WARPS * 32;
+    constexpr int kThreads = MSDA_MERGE_WARPS * 32;
     const TileGrid tg =
-        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_BWD_WARPS,
+        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_MERGE_WARPS,
                   persistent_waves(pb, (int)sizeof(T), true));
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),

@@ -120,9 +120,10 @@ def backward(value, spatial_shapes, level_start_index, sampling_locations, atten
 
 
 def touched_rows(spatial_shapes, level_start_index, sampling_locations, attention_weights,
-                 bs: int, num_keys: int, num_heads: int) -> int:
-    """Distinct (b, key, m) value rows read with a non-zero weight by one forward."""
-    lib = load()
+                 bs: int, num_keys: int, num_heads: int, lib=None) -> int:
+    """Distinct (b, key, m) value rows read with a non-zero weight by one forward
+    (fp32 coordinate contract)."""
+    lib = lib if lib is not None else load()
     loc, w = _f64(sampling_locations), _f64(attention_weights)
     shapes, lsi = _i64(spatial_shapes), _i64(level_start_index)
     _, Q, M, L, P, _ = loc.shape

@@ -253,8 +253,11 @@ MSDA_API const char* msda_status_string(int status);
  *     but MSDA_BF16 (optionally with MSDA_INDEX_INT32; the fp32 backward needs
  *     no workspace: use msda_backward).
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it with the device's CUDA context; make
+ *     that first call before any stream capture.  A call in a new context of
+ *     the device (after cudaDeviceReset) looks the address up again.
+ *   - Each loaded copy of the library holds its own array (64 MiB per copy
+ *     and device).
  *   - Every call on a device shares the one array and zero-fills the part it
  *     uses before accumulating; calls whose work overlaps on the GPU (other
  *     streams, other host threads) race on it and must be serialised.

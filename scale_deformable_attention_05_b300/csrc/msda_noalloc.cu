@@ -11,10 +11,12 @@
 //
 // The array is file-scope device memory.  On the host its name is only a
 // stand-in symbol, never a device address: the address is looked up with
-// cudaGetSymbolAddress once per device (the first call on that device, made
-// with that device current) and cached.  That first call should therefore come
-// before any stream capture.  Every call on a device shares the one array and
-// zero-fills it before use; calls whose work overlaps on the GPU race on it.
+// cudaGetSymbolAddress on the first call on each device (made with that device
+// current) and cached with the device's context; a later call in a new context
+// (after a device reset) looks it up again.  The first call on a device should
+// therefore come before any stream capture.  Every call on a device shares the
+// one array and zero-fills it before use; calls whose work overlaps on the GPU
+// race on it.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -31,21 +33,53 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
-float* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device (looked up once per device).
+// The array's device address on one device, and the CUDA context it belongs to.
+// A device reset (cudaDeviceReset) destroys the context and loads the module
+// again in a new one, where the array may sit elsewhere: the address is looked
+// up again whenever the calling thread's context differs from the cached one.
+struct ScratchAddress {
+    void* context;
+    float* ptr;
+};
+ScratchAddress g_scratch[kMaxDevices] = {};
+
+// The calling thread's current context (the driver's cuCtxGetCurrent, reached
+// through the runtime's entry-point query, so the library needs no link to the
+// driver library), or null when it cannot be queried.
+void* current_context() {
+    using GetCurrent = int (*)(void**);
+    static const GetCurrent get = [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult found = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                             &found) != cudaSuccess ||
+            found != cudaDriverEntryPointSuccess)
+            fn = nullptr;
+        return reinterpret_cast<GetCurrent>(fn);
+    }();
+    void* ctx = nullptr;
+    if (get == nullptr || get(&ctx) != 0) return nullptr;
+    return ctx;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up with that
+// device current on the first call and again after its context changed.
 int scratch_for_current_device(float** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MSDA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return MSDA_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    ScratchAddress& entry = g_scratch[dev];
+    void* ctx = current_context();
+    if (entry.ptr == nullptr || ctx == nullptr || entry.context != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
             return MSDA_ERR_CUDA;
-        g_scratch_ptr[dev] = static_cast<float*>(p);
+        entry.ptr = static_cast<float*>(p);
+        entry.context = current_context();   // the lookup makes the context current if needed
     }
-    *out = g_scratch_ptr[dev];
+    *out = entry.ptr;
     return MSDA_OK;
 }
 

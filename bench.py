@@ -429,12 +429,61 @@ def _e2e_pipelined(B, args, wl, fused, names, host, d, shapes, lsi, results, wor
     e1.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, dev)
+    link = _link_baseline(host, sets[0][0], sets[0][1], sets[0][2], s_in, s_out, n_e2e, h2d, d2h,
+                          wl.points)
     return {"value": job_rate(wl.points, world, e2e_ms), "unit": "points/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "link": link,
             "path": "per step: pinned host -> device copies of the inputs, msda_forward%s and "
                     "msda_backward%s through the Python API, device -> pinned host copies of the "
                     "output and the three gradients; two buffer sets, uploads / compute / "
                     "downloads on three streams" % (("_fused",) * 2 if fused else ("", ""))}
+
+
+def _link_baseline(host, din, dres, hres, s_in, s_out, reps, h2d, d2h, points):
+    """The same copies as one end-to-end step with no compute: the step's uploads
+    alone, its downloads alone, and both at once on their two streams (one
+    cudaMemcpyAsync per tensor, pinned host memory), so that e2e reads as a
+    fraction of what the link moves."""
+    import torch
+
+    def up():
+        with torch.cuda.stream(s_in):
+            for k in host:
+                din[k].copy_(host[k], non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(s_out):
+            for h, x in zip(hres, dres):
+                h.copy_(x, non_blocking=True)
+
+    def timed(fns, first, last):
+        for fn in fns:
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(first)
+        if last is not first:
+            last.wait_event(a)
+        for _ in range(reps):
+            for fn in fns:
+                fn()
+        if last is not first:
+            done = torch.cuda.Event()
+            done.record(first)
+            last.wait_event(done)
+        b.record(last)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    up_ms = timed([up], s_in, s_in)
+    down_ms = timed([down], s_out, s_out)
+    both_ms = timed([up, down], s_in, s_out)
+    return {"h2d_gbs": h2d / up_ms / 1e6, "d2h_gbs": d2h / down_ms / 1e6,
+            "h2d_ms": up_ms, "d2h_ms": down_ms, "both_directions_ms": both_ms,
+            "copy_only_points_per_s": points / both_ms * 1e3,
+            "what": "the step's copies without compute: uploads alone, downloads alone, and "
+                    "both at once on two streams"}
 
 
 class _CapturedPass:

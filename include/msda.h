@@ -272,6 +272,26 @@ MSDA_API int msda_backward_noalloc(const void* value, const void* spatial_shapes
                                    int head_dim, int num_levels, int num_points, int num_queries,
                                    int dtype, unsigned flags, void* stream);
 
+/*
+ * Linear projection on the tensor cores: y = x * w^T + bias, the nn.Linear
+ * layers around the operator in MSDeformAttn.forward (walk-through, "2.2.4
+ * 源码分析": value_proj, sampling_offsets, attention_weights, output_proj).
+ *   x    [rows, in_features]          bf16, row-major, device pointer
+ *   w    [out_features, in_features]  bf16 (nn.Linear weight layout)
+ *   bias [out_features]               fp32, or NULL
+ *   y    [rows, out_features]         bf16, overwritten; fp32 accumulation,
+ *                                      one rounding to bf16 after the bias
+ * dtype must be MSDA_BF16.  in_features must be a multiple of 64 and
+ * out_features a multiple of 16, both at most MSDA_LINEAR_MAX_FEATURES (else
+ * MSDA_ERR_UNSUPPORTED); every pointer 16-byte aligned (MSDA_ERR_ALIGN).
+ * One kernel launch (one CTA per SM, tcgen05.mma with the accumulator in
+ * tensor memory).  A device-side wait that runs out of its iteration limit
+ * stops the kernel and raises the error word msda_last_device_error() reads.
+ */
+#define MSDA_LINEAR_MAX_FEATURES 256
+MSDA_API int msda_linear(const void* x, const void* w, const float* bias, void* y, int rows,
+                         int in_features, int out_features, int dtype, void* stream);
+
 /* MSDA_VERSION of the built library. */
 MSDA_API int msda_version(void);
 

@@ -20,7 +20,7 @@ __all__ = [
     "MsdaError", "LIB_PATH",
     "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
-    "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused",
+    "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused", "msda_linear",
     "MSDeformAttnFunction", "MSDeformAttnFusedFunction", "ms_deform_attn", "ms_deform_attn_fused",
     "EXPORTED_SYMBOLS", "load_library",
 ]
@@ -36,7 +36,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsda.so"
 EXPORTED_SYMBOLS = (
     "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
-    "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused",
+    "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused", "msda_linear",
 )
 
 _vp = ctypes.c_void_p
@@ -74,6 +74,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msda_version.restype = _int
     lib.msda_backward_noalloc.argtypes = [_vp] * 9 + _DIMS + [_int, ctypes.c_uint, _vp]
     lib.msda_backward_noalloc.restype = _int
+    lib.msda_linear.argtypes = [_vp] * 4 + [_int] * 4 + [_vp]
+    lib.msda_linear.restype = _int
     lib.msda_forward_fused.argtypes = [_vp] * 8 + _DIMS + [_int, _int, _vp]
     lib.msda_forward_fused.restype = _int
     lib.msda_backward_fused.argtypes = ([_vp] * 13 + [ctypes.c_size_t] + _DIMS +
@@ -243,6 +245,36 @@ def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_loc
         _dtype_code(value, spatial_shapes), MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0,
         _stream(stream)))
     return grad_value, grad_sampling_loc, grad_attn_weight
+
+
+def msda_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y = x @ weight.T + bias on the tensor cores (see msda_linear in include/msda.h):
+    x [..., in] and weight [out, in] bf16 CUDA tensors, bias fp32 [out] or None;
+    returns bf16 [..., out]."""
+    if x.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise TypeError("msda_linear takes bf16 x and weight")
+    if not (x.is_cuda and weight.is_cuda) or x.device != weight.device:
+        raise ValueError("x and weight must be CUDA tensors on one device")
+    if weight.dim() != 2 or x.shape[-1] != weight.shape[1]:
+        raise ValueError("weight must be [out_features, in_features] with in_features = x.shape[-1]")
+    x2 = x.reshape(-1, x.shape[-1])
+    if not x2.is_contiguous():
+        raise ValueError("x must be contiguous")
+    weight = weight.contiguous()
+    n_out = int(weight.shape[0])
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.shape != (n_out,) or bias.device != x.device:
+            raise ValueError("bias must be an fp32 [out_features] tensor on x's device")
+        bias = bias.contiguous()
+    if out is None:
+        out = torch.empty(*x.shape[:-1], n_out, dtype=torch.bfloat16, device=x.device)
+    elif out.dtype != torch.bfloat16 or out.shape != (*x.shape[:-1], n_out) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 [..., out_features] tensor")
+    _check("msda_linear", _LIB.msda_linear(
+        _ptr(x2), _ptr(weight), _ptr(bias) if bias is not None else None, _ptr(out),
+        int(x2.shape[0]), int(x2.shape[1]), n_out, MSDA_BF16, _stream(stream)))
+    return out
 
 
 def _fused_dims(value, spatial_shapes, reference_points, sampling_offsets, attn_logits):

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libmsda.so")
 CHECKED_LIB = os.path.join(PKG, "libmsda_checked.so")
 SOURCES = ["msda_kernels.cu", "msda_api.cpp", "msda_noalloc.cu"]
-HEADERS = ["msda_device.cuh", "msda_forward.cuh", "msda_backward.cuh", "msda_launch.h"]
+HEADERS = ["msda_device.cuh", "msda_forward.cuh", "msda_backward.cuh", "msda_launch.h",
+           "msda_linear.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -430,3 +430,7 @@ cudaError_t read_and_clear_error(cudaStream_t st, unsigned* word) {
 }
 
 }  // namespace msda
+
+// The tensor-core linear projection (msda_linear), in this translation unit
+// because it shares the device error word.
+#include "msda_linear.cuh"

@@ -1,0 +1,348 @@
+// Linear projection y = x * w^T + bias on the fifth-generation tensor cores
+// (tcgen05), bf16 operands with fp32 accumulation, for the projections around
+// the operator in MSDeformAttn.forward (Deformable DETR walk-through, "2.2.4
+// 源码分析": value_proj, sampling_offsets, attention_weights and output_proj
+// are nn.Linear layers of input width d_model).
+//
+//   x    [rows, K]  bf16, row-major (K contiguous)
+//   w    [N, K]     bf16, the nn.Linear weight layout (K contiguous)
+//   bias [N]        fp32 or NULL
+//   y    [rows, N]  bf16, y[r, n] = sum_k x[r, k] w[n, k] + bias[n], rounded once
+//
+// Design (one CTA of 4 warps per SM, persistent over 128-row tiles):
+//   * w stays in shared memory for the whole launch (N x K bf16 <= 128 KB),
+//     loaded once with TMA in 128-byte-swizzled 64-column blocks;
+//   * each 128-row tile of x is loaded with TMA in the same layout (K / 64
+//     boxes of 128 x 64), one elected thread issues K / 16 tcgen05.mma
+//     (M = 128, N, K = 16 each, both operands K-major) into an fp32
+//     accumulator of N columns in tensor memory and commits them to an
+//     mbarrier;
+//   * the four warps read the accumulator back with tcgen05.ld (warp i owns
+//     lanes 32i..32i+31, i.e. rows), add the bias, round to bf16 and store.
+// Every wait on an mbarrier has an iteration limit; when it runs out the CTA
+// records kErrTimeout in the device error word, stops, frees its tensor memory
+// and returns.  Compiled as part of msda_kernels.cu (it shares the error word).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/msda.h"
+#include "msda_device.cuh"
+
+namespace msda {
+namespace linear {
+
+constexpr int kBM = 128;                 // rows per tile (the MMA's M)
+constexpr int kBK = 64;                  // bf16 columns per 128-byte swizzle atom
+constexpr int kThreads = 128;            // 4 warps
+constexpr unsigned kErrTimeout = 4u;     // bit of the device error word (an mbarrier wait ran out)
+constexpr int kSpinLimit = 1 << 22;      // try_wait rounds before giving up
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Bounded wait for the phase with parity `parity` of the mbarrier to complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (int i = 0; i < kSpinLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.b32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// 2-d TMA tile load into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand stored as 128-byte rows
+// with the 128-byte swizzle (what TMA writes with CU_TENSOR_MAP_SWIZZLE_128B):
+// start address, stride of 1024 bytes between 8-row groups, version 1, layout
+// SWIZZLE_128B.  The leading-dimension offset is unused for this layout (the
+// MMA's 16 columns never leave one 128-byte atom).
+__device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);          // start address (16-byte units)
+    d |= (uint64_t)1 << 16;                          // leading byte offset (unused): 16 B
+    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: 1024 B
+    d |= (uint64_t)1 << 46;                          // descriptor version
+    d |= (uint64_t)2 << 61;                          // layout: 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both K-major,
+// M = 128 and N = n.
+__host__ __device__ constexpr uint32_t bf16_idesc(int n) {
+    return (1u << 4)                         // D format: f32
+           | (1u << 7)                       // A format: bf16
+           | (1u << 10)                      // B format: bf16
+           | ((uint32_t)(n >> 3) << 17)      // N / 8
+           | ((uint32_t)(kBM >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+        "[%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory layout of one CTA (byte offsets from a 1024-aligned base).
+struct Smem {
+    uint32_t w, x, bars, tmem_slot, total;
+};
+__host__ __device__ inline Smem smem_layout(int n, int k) {
+    Smem s;
+    s.w = 0;                                    // K/64 blocks of n rows x 128 B
+    s.x = s.w + (uint32_t)n * (uint32_t)k * 2;  // K/64 blocks of 128 rows x 128 B
+    s.bars = s.x + (uint32_t)kBM * (uint32_t)k * 2;
+    s.tmem_slot = s.bars + 3 * 8;
+    s.total = s.tmem_slot + 8;
+    return s;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_bf16_kernel(const __grid_constant__ CUtensorMap x_map,
+                       const __grid_constant__ CUtensorMap w_map, const float* __restrict__ bias,
+                       __nv_bfloat16* __restrict__ y, int rows, int n, int k, int tmem_cols) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // TMA destinations with the 128-byte swizzle must sit on 1024-byte boundaries
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Smem L = smem_layout(n, k);
+    const uint32_t s_w = smem_u32(base + L.w), s_x = smem_u32(base + L.x);
+    const uint32_t bar_w = smem_u32(base + L.bars), bar_x = bar_w + 8, bar_mma = bar_w + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.tmem_slot);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kblocks = k / kBK;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(bar_w, 1);
+        mbar_init(bar_x, 1);
+        mbar_init(bar_mma, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    if (threadIdx.x == 0) {
+        mbar_expect_tx(bar_w, (uint32_t)n * (uint32_t)k * 2);
+        for (int kb = 0; kb < kblocks; ++kb)
+            tma_load_2d(s_w + (uint32_t)kb * (uint32_t)n * 128, &w_map, kb * kBK, 0, bar_w);
+    }
+    const uint32_t idesc = bf16_idesc(n);
+    const int tiles = (rows + kBM - 1) / kBM;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int r0 = t * kBM;
+        if (threadIdx.x == 0) {
+            mbar_expect_tx(bar_x, (uint32_t)kBM * (uint32_t)k * 2);
+            for (int kb = 0; kb < kblocks; ++kb)
+                tma_load_2d(s_x + (uint32_t)kb * kBM * 128, &x_map, kb * kBK, r0, bar_x);
+            bool ready = (t != (int)blockIdx.x) || mbar_wait(bar_w, 0);
+            ready = ready && mbar_wait(bar_x, phase);
+            if (ready) {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                for (int s = 0; s < k / 16; ++s) {
+                    const int kb = s >> 2;
+                    const uint32_t koff = (uint32_t)(s & 3) * 32;   // 16 bf16 columns
+                    const uint64_t a = kmajor_sw128_desc(s_x + (uint32_t)kb * kBM * 128 + koff);
+                    const uint64_t b =
+                        kmajor_sw128_desc(s_w + (uint32_t)kb * (uint32_t)n * 128 + koff);
+                    umma_bf16(tmem, a, b, idesc, s > 0);
+                }
+                umma_commit(bar_mma);
+            } else {
+                atomicOr(&msda::g_error_word, kErrTimeout);
+            }
+        }
+        // every thread waits for the accumulator (a thread whose wait runs out stops)
+        if (!mbar_wait(bar_mma, phase)) {
+            atomicOr(&msda::g_error_word, kErrTimeout);
+            ok = false;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (ok) {
+            const int row = r0 + warp * 32 + lane;
+            const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+            for (int c0 = 0; c0 < n; c0 += 32) {
+                float v[32];
+                tmem_ld32(lane_addr + (uint32_t)c0, v);
+                // the last chunk of a row may hold 16 valid columns (n % 16 == 0)
+                const int valid = n - c0 < 32 ? n - c0 : 32;
+                if (row < rows) {
+                    uint4 out[4];
+                    uint32_t* o = reinterpret_cast<uint32_t*>(out);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const bool in = 2 * i < valid;
+                        const float b0 = bias && in ? __ldg(bias + c0 + 2 * i) : 0.f;
+                        const float b1 = bias && in ? __ldg(bias + c0 + 2 * i + 1) : 0.f;
+                        const __nv_bfloat162 h =
+                            __floats2bfloat162_rn(v[2 * i] + b0, v[2 * i + 1] + b1);
+                        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(y + (size_t)row * n + c0);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (8 * i < valid) dst[i] = out[i];
+                }
+            }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();            // accumulator read and x buffer free for the next tile
+        ok = __syncthreads_and(ok);
+        phase ^= 1u;
+    }
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(tmem_cols)
+                     : "memory");
+}
+
+// ------------------------------------------------------------------- host
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled() {
+    static const EncodeTiled fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult found = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &found) != cudaSuccess ||
+            found != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiled>(p);
+    }();
+    return fn;
+}
+
+// Row-major bf16 matrix [outer, inner] read in boxes of [box_rows, 64] with the
+// 128-byte swizzle; rows past `outer` read as zero.
+bool make_map(CUtensorMap* map, const void* ptr, int inner, int outer, int box_rows) {
+    const EncodeTiled enc = encode_tiled();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms > 0 ? sms : 1;
+}
+
+}  // namespace linear
+}  // namespace msda
+
+extern "C" int msda_linear(const void* x, const void* w, const float* bias, void* y,
+                                    int rows, int in_features, int out_features, int dtype,
+                                    void* stream) {
+    if (dtype != MSDA_BF16) return MSDA_ERR_UNSUPPORTED;
+    if (rows < 0 || in_features < 0 || out_features < 0) return MSDA_ERR_DIM;
+    using namespace msda::linear;
+    if (in_features % kBK != 0 || in_features < kBK || in_features > MSDA_LINEAR_MAX_FEATURES ||
+        out_features % 16 != 0 || out_features < 16 || out_features > MSDA_LINEAR_MAX_FEATURES)
+        return MSDA_ERR_UNSUPPORTED;
+    if (rows == 0) return MSDA_OK;
+    if (x == nullptr || w == nullptr || y == nullptr) return MSDA_ERR_NULL;
+    const auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (misaligned(x) || misaligned(w) || misaligned(y) || (bias && misaligned(bias)))
+        return MSDA_ERR_ALIGN;
+    if ((int64_t)rows * in_features > 2147483647LL * 64) return MSDA_ERR_DIM;
+    CUtensorMap xm, wm;
+    if (!make_map(&xm, x, in_features, rows, kBM) ||
+        !make_map(&wm, w, in_features, out_features, out_features))
+        return MSDA_ERR_CUDA;
+    int cols = 32;
+    while (cols < out_features) cols <<= 1;
+    const Smem L = smem_layout(out_features, in_features);
+    const size_t smem = (size_t)L.total + 1024;
+    static std::once_flag attr_once;
+    std::call_once(attr_once, [] {
+        cudaFuncSetAttribute(linear_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(smem_layout(MSDA_LINEAR_MAX_FEATURES, MSDA_LINEAR_MAX_FEATURES)
+                                       .total +
+                                   1024));
+    });
+    const int tiles = (rows + kBM - 1) / kBM;
+    const int grid = tiles < sm_count() ? tiles : sm_count();
+    linear_bf16_kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+        xm, wm, bias, static_cast<__nv_bfloat16*>(y), rows, out_features, in_features, cols);
+    return cudaGetLastError() == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA;
+}

@@ -196,20 +196,21 @@ def run_layer(args, wl):
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     from scale_deformable_attention_05_b300.module import MSDeformAttn
-    if wl.dtype != "f32":
-        raise SystemExit("--path layer runs fp32 workloads")
+    if wl.dtype not in ("f32", "bf16"):
+        raise SystemExit("--path layer runs fp32 or bf16 workloads")
     torch.backends.cuda.matmul.allow_tf32 = False
     dev = torch.device("cuda", local)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     wl_r = rank_workload(wl, rank)
     C = wl.num_heads * wl.head_dim
     torch.manual_seed(wl_r.seed)
-    layer = MSDeformAttn(C, wl.num_levels, wl.num_heads, wl.num_points).to(dev)
+    layer = MSDeformAttn(C, wl.num_levels, wl.num_heads, wl.num_points).to(dev).to(tdt)
     fin = gen.make_fused_inputs(wl_r, 2)
     gcpu = torch.Generator().manual_seed(wl_r.seed)
-    q = torch.randn(wl.bs, wl.num_queries, C, generator=gcpu).to(dev).requires_grad_()
-    x = torch.randn(wl.bs, wl.num_keys, C, generator=gcpu).to(dev).requires_grad_()
-    go = torch.randn(wl.bs, wl.num_queries, C, generator=gcpu).to(dev)
-    ref = torch.from_numpy(fin["reference_points"]).to(dev)
+    q = torch.randn(wl.bs, wl.num_queries, C, generator=gcpu).to(dev, tdt).requires_grad_()
+    x = torch.randn(wl.bs, wl.num_keys, C, generator=gcpu).to(dev, tdt).requires_grad_()
+    go = torch.randn(wl.bs, wl.num_queries, C, generator=gcpu).to(dev, tdt)
+    ref = torch.from_numpy(fin["reference_points"]).to(dev, tdt)
     shapes = torch.from_numpy(fin["spatial_shapes"]).to(dev)
     lsi = torch.from_numpy(fin["level_start_index"]).to(dev)
     mask = (torch.from_numpy(gen.padding_mask(wl_r)).to(dev) if args.padding_mask else None)
@@ -222,6 +223,33 @@ def run_layer(args, wl):
         q.grad = x.grad = None
         layer(q, ref, x, shapes, lsi, mask).backward(go)
 
+    def timed_steps(n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record()
+            step()
+            e1.record()
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    compare = None
+    if wl.dtype == "bf16":
+        # the same layer with torch.nn.Linear (cuBLAS) projections, for comparison;
+        # both configurations warm up twice as long as asked (first-use costs of
+        # the allocator and of each kernel module)
+        layer.tensor_core_projections = False
+        for _ in range(2 * args.warmup):
+            flush.zero_()
+            step()
+        cublas_ms = timed_steps(args.steps)
+        layer.tensor_core_projections = True
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+        compare = {"cublas_projections_ms": statistics.median(cublas_ms),
+                   "gemm": _projection_gemm(layer.output_proj, wl.bs * wl.num_keys, dev, flush)}
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -249,8 +277,10 @@ def run_layer(args, wl):
         return 0
     cfg = _config(wl, args)
     cfg["entry_points"] = ("module.MSDeformAttn: value / offset / weight / output projections "
-                           "(torch Linear, cuBLAS fp32) around msda_forward_fused / "
-                           "msda_backward_fused, autograd")
+                           + ("(msda_linear on the tensor cores forward and for the input "
+                              "gradients; weight gradients with torch, cuBLAS bf16)"
+                              if wl.dtype == "bf16" else "(torch Linear, cuBLAS fp32)")
+                           + " around msda_forward_fused / msda_backward_fused, autograd")
     cfg["launch"] = "eager through autograd (no graphs; Python and autograd inside the events)"
     line = {
         "metric": METRIC, "value": job_rate(wl.points, ws, ms_step), "unit": "points/s",
@@ -260,14 +290,53 @@ def run_layer(args, wl):
         "config": cfg,
         "passes": {"layer": {"ms": sum(ms) / len(ms), "median_ms": statistics.median(ms),
                              "min_ms": min(ms)}},
+        "projections": compare,
         "roofline": None, "clocks": clocks, "e2e": None,
-        # the library's kernels per step: fused forward; grad_value zero-fill + fused backward
-        "gpu_launches": 3 * args.steps,
+        # the library's kernels per step: fused forward; grad_value (or fp32 workspace)
+        # zero-fill + fused backward (+ the bf16 finalize); in bf16 four msda_linear
+        # forward and four backward
+        "gpu_launches": (3 if wl.dtype == "f32" else 4 + 8) * args.steps,
     }
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+def _projection_gemm(linear, rows, dev, flush, reps=20):
+    """One d_model x d_model projection of `rows` bf16 tokens: msda_linear (tcgen05)
+    against torch's F.linear (cuBLAS), CUDA events, L2 flushed before each call."""
+    import torch
+    import torch.nn.functional as F
+    from scale_deformable_attention_05_b300 import binding as B
+    g = torch.Generator(device=dev).manual_seed(11)
+    xg = torch.randn(rows, linear.in_features, generator=g, device=dev).to(torch.bfloat16)
+    w, b = linear.weight.detach(), linear.bias.detach()
+    bf = b.float()
+    out = torch.empty(rows, linear.out_features, dtype=torch.bfloat16, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    tc = timed(lambda: B.msda_linear(xg, w, bf, out=out))
+    cb = timed(lambda: F.linear(xg, w, b))
+    flops = 2.0 * rows * linear.in_features * linear.out_features
+    nbytes = 2.0 * rows * (linear.in_features + linear.out_features)
+    return {"rows": rows, "in_features": linear.in_features,
+            "out_features": linear.out_features,
+            "tcgen05_us": tc * 1e3, "cublas_us": cb * 1e3,
+            "tcgen05_tflops": flops / tc / 1e9, "tcgen05_gbs": nbytes / tc / 1e6}
 
 
 def touched_roofline(wl, inp, passes, hbm_gbs):

@@ -31,6 +31,7 @@ MSDA_F16 = 2
 MSDA_INDEX_INT32 = 0x100
 MSDA_GRAD_VALUE_ACCUMULATE = 1
 MSDA_MAX_FUSED_LEVEL_POINTS = 64
+MSDA_LINEAR_MAX_FEATURES = 256
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsda.so")
 EXPORTED_SYMBOLS = (

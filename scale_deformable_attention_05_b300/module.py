@@ -10,12 +10,16 @@ them,
     out     = output_proj(msda(value masked by input_padding_mask,
                                softmax(logits), reference_points + offsets))
 
-The four projections are plain dense GEMMs (``torch.nn.Linear``, cuBLAS);
-everything between them -- masking, softmax, locations from 2-d or 4-d
-reference points, bilinear sampling and their backward -- is one launch of
-the fused entry points of ``libmsda.so`` each way.  The tensors the GEMMs
-produce are already in the operator's layouts, so nothing is copied or
-transposed between them.
+The four projections are dense GEMMs.  In bf16 they run on the library's
+tensor-core kernel (``msda_linear``: tcgen05.mma with the accumulator in tensor
+memory) for the forward and for the input gradient (x-gradient = grad_y times
+the weight, i.e. the same kernel with the transposed weight); the weight
+gradient (a reduction over all tokens) and every fp32 projection use
+``torch.nn.Linear`` (cuBLAS).  Everything between the projections -- masking,
+softmax, locations from 2-d or 4-d reference points, bilinear sampling and
+their backward -- is one launch of the fused entry points of ``libmsda.so``
+each way.  The tensors the GEMMs produce are already in the operator's
+layouts, so nothing is copied or transposed between them.
 """
 from __future__ import annotations
 
@@ -28,9 +32,55 @@ from torch import nn
 from . import binding as B
 
 
+def _tensor_core_shape(in_features: int, out_features: int) -> bool:
+    return (in_features % 64 == 0 and out_features % 16 == 0 and
+            in_features <= B.MSDA_LINEAR_MAX_FEATURES and
+            out_features <= B.MSDA_LINEAR_MAX_FEATURES)
+
+
+class TensorCoreLinear(torch.autograd.Function):
+    """y = x w^T + b with bf16 x and w on the tensor cores (msda_linear); the
+    input gradient through the same kernel with w^T when its shape allows
+    (else a cuBLAS matmul), the weight and bias gradients with torch."""
+
+    @staticmethod
+    def forward(ctx, x, weight, bias):
+        ctx.save_for_backward(x, weight)
+        ctx.has_bias = bias is not None
+        return B.msda_linear(x.contiguous(), weight,
+                             None if bias is None else bias.float())
+
+    @staticmethod
+    def backward(ctx, grad_y):
+        x, weight = ctx.saved_tensors
+        n_out, n_in = weight.shape
+        gy = grad_y.contiguous()
+        if _tensor_core_shape(n_out, n_in):
+            gx = B.msda_linear(gy, weight.t().contiguous())
+        else:
+            gx = gy @ weight
+        g2 = gy.reshape(-1, n_out)
+        gw = g2.t() @ x.reshape(-1, n_in)
+        gb = g2.float().sum(0).to(weight.dtype) if ctx.has_bias else None
+        return gx, gw, gb
+
+
+def project(linear: nn.Linear, x: torch.Tensor, tensor_cores: bool = True) -> torch.Tensor:
+    """linear(x), on the tensor-core kernel for bf16 operands of supported widths."""
+    if (tensor_cores and x.is_cuda and x.dtype == torch.bfloat16 and
+            linear.weight.dtype == torch.bfloat16 and
+            _tensor_core_shape(linear.in_features, linear.out_features)):
+        return TensorCoreLinear.apply(x, linear.weight, linear.bias)
+    return linear(x)
+
+
 class MSDeformAttn(nn.Module):
     """Multi-scale deformable attention with d_model channels split into
-    n_heads heads, sampling n_points points on each of n_levels levels."""
+    n_heads heads, sampling n_points points on each of n_levels levels.
+    tensor_core_projections: bf16 projections on the library's tensor-core
+    kernel (True) or on torch.nn.Linear (False)."""
+
+    tensor_core_projections = True
 
     def __init__(self, d_model: int = 256, n_levels: int = 4, n_heads: int = 8,
                  n_points: int = 4):
@@ -82,9 +132,10 @@ class MSDeformAttn(nn.Module):
         N, Len_q, _ = query.shape
         Len_in = input_flatten.shape[1]
         M, L, P = self.n_heads, self.n_levels, self.n_points
-        value = self.value_proj(input_flatten).view(N, Len_in, M, self.d_model // M)
-        offsets = self.sampling_offsets(query).view(N, Len_q, M, L, P, 2)
-        logits = self.attention_weights(query).view(N, Len_q, M, L * P)
+        tc = self.tensor_core_projections
+        value = project(self.value_proj, input_flatten, tc).view(N, Len_in, M, self.d_model // M)
+        offsets = project(self.sampling_offsets, query, tc).view(N, Len_q, M, L, P, 2)
+        logits = project(self.attention_weights, query, tc).view(N, Len_q, M, L * P)
         out = B.ms_deform_attn_fused(value, input_spatial_shapes, input_level_start_index,
                                      reference_points, offsets, logits, input_padding_mask)
-        return self.output_proj(out)
+        return project(self.output_proj, out, tc)

@@ -278,18 +278,21 @@ MSDA_API int msda_backward_noalloc(const void* value, const void* spatial_shapes
  * 源码分析": value_proj, sampling_offsets, attention_weights, output_proj).
  *   x    [rows, in_features]          bf16, row-major, device pointer
  *   w    [out_features, in_features]  bf16 (nn.Linear weight layout)
- *   bias [out_features]               fp32, or NULL
+ *   bias [out_features]               fp32, or bf16 when dtype has
+ *                                      MSDA_LINEAR_BIAS_BF16, or NULL
  *   y    [rows, out_features]         bf16, overwritten; fp32 accumulation,
  *                                      one rounding to bf16 after the bias
- * dtype must be MSDA_BF16.  in_features must be a multiple of 64 and
+ * dtype must be MSDA_BF16 (optionally | MSDA_LINEAR_BIAS_BF16).  in_features
+ * must be a multiple of 64 and
  * out_features a multiple of 16, both at most MSDA_LINEAR_MAX_FEATURES (else
  * MSDA_ERR_UNSUPPORTED); every pointer 16-byte aligned (MSDA_ERR_ALIGN).
- * One kernel launch (one CTA per SM, tcgen05.mma with the accumulator in
- * tensor memory).  A device-side wait that runs out of its iteration limit
+ * One kernel launch (one persistent CTA per SM: TMA loads, tcgen05.mma into
+ * two alternating accumulators in tensor memory, TMA stores).  A device-side wait that runs out of its iteration limit
  * stops the kernel and raises the error word msda_last_device_error() reads.
  */
 #define MSDA_LINEAR_MAX_FEATURES 256
-MSDA_API int msda_linear(const void* x, const void* w, const float* bias, void* y, int rows,
+#define MSDA_LINEAR_BIAS_BF16 0x200
+MSDA_API int msda_linear(const void* x, const void* w, const void* bias, void* y, int rows,
                          int in_features, int out_features, int dtype, void* stream);
 
 /* MSDA_VERSION of the built library. */

@@ -32,6 +32,7 @@ MSDA_INDEX_INT32 = 0x100
 MSDA_GRAD_VALUE_ACCUMULATE = 1
 MSDA_MAX_FUSED_LEVEL_POINTS = 64
 MSDA_LINEAR_MAX_FEATURES = 256
+MSDA_LINEAR_BIAS_BF16 = 0x200
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsda.so")
 EXPORTED_SYMBOLS = (
@@ -251,8 +252,8 @@ def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_loc
 def msda_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """y = x @ weight.T + bias on the tensor cores (see msda_linear in include/msda.h):
-    x [..., in] and weight [out, in] bf16 CUDA tensors, bias fp32 [out] or None;
-    returns bf16 [..., out]."""
+    x [..., in] and weight [out, in] bf16 CUDA tensors, bias fp32 or bf16 [out] or
+    None; returns bf16 [..., out]."""
     if x.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
         raise TypeError("msda_linear takes bf16 x and weight")
     if not (x.is_cuda and weight.is_cuda) or x.device != weight.device:
@@ -264,17 +265,21 @@ def msda_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tens
         raise ValueError("x must be contiguous")
     weight = weight.contiguous()
     n_out = int(weight.shape[0])
+    code = MSDA_BF16
     if bias is not None:
-        if bias.dtype != torch.float32 or bias.shape != (n_out,) or bias.device != x.device:
-            raise ValueError("bias must be an fp32 [out_features] tensor on x's device")
+        if (bias.dtype not in (torch.float32, torch.bfloat16) or bias.shape != (n_out,)
+                or bias.device != x.device):
+            raise ValueError("bias must be an fp32 or bf16 [out_features] tensor on x's device")
         bias = bias.contiguous()
+        if bias.dtype == torch.bfloat16:
+            code |= MSDA_LINEAR_BIAS_BF16
     if out is None:
         out = torch.empty(*x.shape[:-1], n_out, dtype=torch.bfloat16, device=x.device)
     elif out.dtype != torch.bfloat16 or out.shape != (*x.shape[:-1], n_out) or not out.is_contiguous():
         raise ValueError("out must be a contiguous bf16 [..., out_features] tensor")
     _check("msda_linear", _LIB.msda_linear(
         _ptr(x2), _ptr(weight), _ptr(bias) if bias is not None else None, _ptr(out),
-        int(x2.shape[0]), int(x2.shape[1]), n_out, MSDA_BF16, _stream(stream)))
+        int(x2.shape[0]), int(x2.shape[1]), n_out, code, _stream(stream)))
     return out
 
 

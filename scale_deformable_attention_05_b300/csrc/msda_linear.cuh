@@ -9,19 +9,25 @@
 //   bias [N]        fp32 or NULL
 //   y    [rows, N]  bf16, y[r, n] = sum_k x[r, k] w[n, k] + bias[n], rounded once
 //
-// Design (one CTA of 4 warps per SM, persistent over 128-row tiles):
+// Design (one persistent CTA of 6 warps per SM over 128-row tiles):
 //   * w stays in shared memory for the whole launch (N x K bf16 <= 128 KB),
 //     loaded once with TMA in 128-byte-swizzled 64-column blocks;
-//   * each 128-row tile of x is loaded with TMA in the same layout (K / 64
-//     boxes of 128 x 64), one elected thread issues K / 16 tcgen05.mma
-//     (M = 128, N, K = 16 each, both operands K-major) into an fp32
-//     accumulator of N columns in tensor memory and commits them to an
-//     mbarrier;
-//   * the four warps read the accumulator back with tcgen05.ld (warp i owns
-//     lanes 32i..32i+31, i.e. rows), add the bias, round to bf16 and store.
-// Every wait on an mbarrier has an iteration limit; when it runs out the CTA
-// records kErrTimeout in the device error word, stops, frees its tensor memory
-// and returns.  Compiled as part of msda_kernels.cu (it shares the error word).
+//   * warp 0 streams the 128 x 64 blocks of x through a ring of kStages
+//     shared-memory stages with TMA (same swizzled layout);
+//   * warp 1 issues, per block, four tcgen05.mma (M = 128, N, K = 16, both
+//     operands K-major) into one of two fp32 accumulators of 256 columns in
+//     tensor memory, frees the block's stage with tcgen05.commit, and hands a
+//     finished accumulator to the epilogue with another commit;
+//   * warps 2..9 (two per tensor-memory lane quarter, each taking every other
+//     32-column piece) read the accumulator with tcgen05.ld, add the bias (kept
+//     in shared memory), round to bf16, stage 32 x 32 pieces in shared memory
+//     and write them with TMA stores (which clip the ragged last tile), then
+//     free the accumulator for the tile after next.
+// So loads, MMAs and the epilogue of consecutive tiles overlap.  Every wait on
+// an mbarrier has an iteration limit; when it runs out the thread records
+// kErrTimeout in the device error word and stops, and the CTA frees its
+// tensor memory and returns.  Compiled as part of msda_kernels.cu (it shares
+// the error word).
 #pragma once
 
 #include <cuda.h>
@@ -39,7 +45,11 @@ namespace linear {
 
 constexpr int kBM = 128;                 // rows per tile (the MMA's M)
 constexpr int kBK = 64;                  // bf16 columns per 128-byte swizzle atom
-constexpr int kThreads = 128;            // 4 warps
+constexpr int kStages = 4;               // x blocks in flight
+constexpr int kEpiWarps = 8;             // warps 2..9, two per tensor-memory lane quarter
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kAccCols = 256;            // tensor-memory columns per accumulator
+constexpr int kChunk = 32;               // output columns per staged piece
 constexpr unsigned kErrTimeout = 4u;     // bit of the device error word (an mbarrier wait ran out)
 constexpr int kSpinLimit = 1 << 22;      // try_wait rounds before giving up
 
@@ -56,7 +66,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 
-// Bounded wait for the phase with parity `parity` of the mbarrier to complete.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait for the phase with parity `parity` of the mbarrier to complete
+// (a fresh barrier counts its phase of parity 1 as complete).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     for (int i = 0; i < kSpinLimit; ++i) {
         uint32_t done;
@@ -69,6 +84,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
             : "memory");
         if (done) return true;
     }
+    atomicOr(&msda::g_error_word, kErrTimeout);
     return false;
 }
 
@@ -80,6 +96,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
+}
+
+// 2-d TMA tile store from shared memory (elements past the tensor are not written).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1,
+                                             uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(src)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor of a K-major operand stored as 128-byte rows
@@ -143,44 +170,59 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 
 // Shared-memory layout of one CTA (byte offsets from a 1024-aligned base).
 struct Smem {
-    uint32_t w, x, bars, tmem_slot, total;
+    uint32_t w, x, stage_out, bias, bars, tmem_slot, total;
 };
 __host__ __device__ inline Smem smem_layout(int n, int k) {
     Smem s;
-    s.w = 0;                                    // K/64 blocks of n rows x 128 B
-    s.x = s.w + (uint32_t)n * (uint32_t)k * 2;  // K/64 blocks of 128 rows x 128 B
-    s.bars = s.x + (uint32_t)kBM * (uint32_t)k * 2;
-    s.tmem_slot = s.bars + 3 * 8;
+    s.w = 0;                                                 // K/64 blocks of n rows x 128 B
+    s.x = s.w + (uint32_t)n * (uint32_t)k * 2;               // kStages blocks of 128 x 128 B
+    s.stage_out = s.x + (uint32_t)kStages * kBM * 128;       // 2 x 32 x 32 bf16 per epilogue warp
+    s.bias = s.stage_out + (uint32_t)kEpiWarps * 2 * kChunk * kChunk * 2;   // 256 fp32
+    s.bars = s.bias + MSDA_LINEAR_MAX_FEATURES * 4;
+    s.tmem_slot = s.bars + (1 + 2 * kStages + 4) * 8;
     s.total = s.tmem_slot + 8;
     return s;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     linear_bf16_kernel(const __grid_constant__ CUtensorMap x_map,
-                       const __grid_constant__ CUtensorMap w_map, const float* __restrict__ bias,
-                       __nv_bfloat16* __restrict__ y, int rows, int n, int k, int tmem_cols) {
+                       const __grid_constant__ CUtensorMap w_map,
+                       const __grid_constant__ CUtensorMap y_map, const void* __restrict__ bias,
+                       int bias_bf16, int rows, int n, int k) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // TMA destinations with the 128-byte swizzle must sit on 1024-byte boundaries
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Smem L = smem_layout(n, k);
     const uint32_t s_w = smem_u32(base + L.w), s_x = smem_u32(base + L.x);
-    const uint32_t bar_w = smem_u32(base + L.bars), bar_x = bar_w + 8, bar_mma = bar_w + 16;
+    const uint32_t bars = smem_u32(base + L.bars);
+    const uint32_t w_full = bars;
+    auto x_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto x_empty = [&](int s) { return bars + 8u * (1 + kStages + s); };
+    auto acc_full = [&](int a) { return bars + 8u * (1 + 2 * kStages + a); };
+    auto acc_empty = [&](int a) { return bars + 8u * (3 + 2 * kStages + a); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.tmem_slot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kblocks = k / kBK;
+    const int tiles = (rows + kBM - 1) / kBM;
 
-    if (warp == 0) {
+    if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
-                     "r"(tmem_cols)
+                     "r"(2 * kAccCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (threadIdx.x == 0) {
-        mbar_init(bar_w, 1);
-        mbar_init(bar_x, 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(w_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(x_full(s), 1);
+            mbar_init(x_empty(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full(a), 1);
+            mbar_init(acc_empty(a), kEpiWarps);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -189,80 +231,127 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
 
-    if (threadIdx.x == 0) {
-        mbar_expect_tx(bar_w, (uint32_t)n * (uint32_t)k * 2);
-        for (int kb = 0; kb < kblocks; ++kb)
-            tma_load_2d(s_w + (uint32_t)kb * (uint32_t)n * 128, &w_map, kb * kBK, 0, bar_w);
-    }
-    const uint32_t idesc = bf16_idesc(n);
-    const int tiles = (rows + kBM - 1) / kBM;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        const int r0 = t * kBM;
-        if (threadIdx.x == 0) {
-            mbar_expect_tx(bar_x, (uint32_t)kBM * (uint32_t)k * 2);
+    if (warp == 0) {
+        // ---- producer: w once, then the x blocks of every tile through the ring
+        if (lane == 0) {
+            mbar_expect_tx(w_full, (uint32_t)n * (uint32_t)k * 2);
             for (int kb = 0; kb < kblocks; ++kb)
-                tma_load_2d(s_x + (uint32_t)kb * kBM * 128, &x_map, kb * kBK, r0, bar_x);
-            bool ready = (t != (int)blockIdx.x) || mbar_wait(bar_w, 0);
-            ready = ready && mbar_wait(bar_x, phase);
-            if (ready) {
+                tma_load_2d(s_w + (uint32_t)kb * (uint32_t)n * 128, &w_map, kb * kBK, 0, w_full);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x)
+                for (int kb = 0; kb < kblocks && ok; ++kb, ++it) {
+                    const int s = (int)(it % kStages);
+                    const uint32_t ph = (it / kStages) & 1u;
+                    ok = mbar_wait(x_empty(s), ph ^ 1u);
+                    if (!ok) break;
+                    mbar_expect_tx(x_full(s), (uint32_t)kBM * 128);
+                    tma_load_2d(s_x + (uint32_t)s * kBM * 128, &x_map, kb * kBK, t * kBM,
+                                x_full(s));
+                }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = bf16_idesc(n);
+            bool ok = mbar_wait(w_full, 0);
+            uint32_t it = 0, acc_it = 0;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++acc_it) {
+                const int a = (int)(acc_it & 1u);
+                const uint32_t aph = (acc_it >> 1) & 1u;
+                ok = mbar_wait(acc_empty(a), aph ^ 1u);
+                if (!ok) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                for (int s = 0; s < k / 16; ++s) {
-                    const int kb = s >> 2;
-                    const uint32_t koff = (uint32_t)(s & 3) * 32;   // 16 bf16 columns
-                    const uint64_t a = kmajor_sw128_desc(s_x + (uint32_t)kb * kBM * 128 + koff);
-                    const uint64_t b =
-                        kmajor_sw128_desc(s_w + (uint32_t)kb * (uint32_t)n * 128 + koff);
-                    umma_bf16(tmem, a, b, idesc, s > 0);
-                }
-                umma_commit(bar_mma);
-            } else {
-                atomicOr(&msda::g_error_word, kErrTimeout);
-            }
-        }
-        // every thread waits for the accumulator (a thread whose wait runs out stops)
-        if (!mbar_wait(bar_mma, phase)) {
-            atomicOr(&msda::g_error_word, kErrTimeout);
-            ok = false;
-        }
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (ok) {
-            const int row = r0 + warp * 32 + lane;
-            const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-            for (int c0 = 0; c0 < n; c0 += 32) {
-                float v[32];
-                tmem_ld32(lane_addr + (uint32_t)c0, v);
-                // the last chunk of a row may hold 16 valid columns (n % 16 == 0)
-                const int valid = n - c0 < 32 ? n - c0 : 32;
-                if (row < rows) {
-                    uint4 out[4];
-                    uint32_t* o = reinterpret_cast<uint32_t*>(out);
+                const uint32_t d = tmem + (uint32_t)(a * kAccCols);
+                for (int kb = 0; kb < kblocks && ok; ++kb, ++it) {
+                    const int s = (int)(it % kStages);
+                    const uint32_t ph = (it / kStages) & 1u;
+                    ok = mbar_wait(x_full(s), ph);
+                    if (!ok) break;
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const bool in = 2 * i < valid;
-                        const float b0 = bias && in ? __ldg(bias + c0 + 2 * i) : 0.f;
-                        const float b1 = bias && in ? __ldg(bias + c0 + 2 * i + 1) : 0.f;
-                        const __nv_bfloat162 h =
-                            __floats2bfloat162_rn(v[2 * i] + b0, v[2 * i + 1] + b1);
-                        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+                    for (int ks = 0; ks < kBK / 16; ++ks) {
+                        const uint32_t koff = (uint32_t)ks * 32;   // 16 bf16 columns
+                        umma_bf16(d, kmajor_sw128_desc(s_x + (uint32_t)s * kBM * 128 + koff),
+                                  kmajor_sw128_desc(s_w + (uint32_t)kb * (uint32_t)n * 128 + koff),
+                                  idesc, kb > 0 || ks > 0);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(y + (size_t)row * n + c0);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (8 * i < valid) dst[i] = out[i];
+                    umma_commit(x_empty(s));     // the stage is free once these MMAs finish
                 }
+                if (ok) umma_commit(acc_full(a));
             }
         }
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncthreads();            // accumulator read and x buffer free for the next tile
-        ok = __syncthreads_and(ok);
-        phase ^= 1u;
+    } else {
+        // ---- epilogue: warp w (2..9) reads lanes 32 * (w % 4) .. + 31 of the
+        //      accumulator, the 32-column pieces c0 = 32 * half, 32 * half + 64, ...
+        const int quarter = warp & 3;
+        const int ew = warp - 2;
+        const int half = ew >> 2;
+        float* s_bias = reinterpret_cast<float*>(base + L.bias);
+        // the bias, zero past n, in shared memory (the epilogue warps' own copy)
+        for (int c = ew * 32 + lane; c < MSDA_LINEAR_MAX_FEATURES; c += kEpiWarps * 32) {
+            float bv = 0.f;
+            if (bias != nullptr && c < n)
+                bv = bias_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(bias)[c])
+                               : static_cast<const float*>(bias)[c];
+            s_bias[c] = bv;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+        const uint32_t stage_base =
+            smem_u32(base + L.stage_out) + (uint32_t)ew * 2 * kChunk * kChunk * 2;
+        unsigned char* stage_ptr = base + L.stage_out + (size_t)ew * 2 * kChunk * kChunk * 2;
+        uint32_t acc_it = 0, piece = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++acc_it) {
+            const int a = (int)(acc_it & 1u);
+            ok = mbar_wait(acc_full(a), (acc_it >> 1) & 1u);
+            if (!ok) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t taddr =
+                tmem + (uint32_t)(a * kAccCols) + ((uint32_t)(quarter * 32) << 16);
+            for (int c0 = half * kChunk; c0 < n; c0 += 2 * kChunk, ++piece) {
+                float v[32];
+                tmem_ld32(taddr + (uint32_t)c0, v);
+                const float4* bq = reinterpret_cast<const float4*>(s_bias + c0);
+                uint32_t o[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 bb = bq[i];
+                    const __nv_bfloat162 h0 =
+                        __floats2bfloat162_rn(v[4 * i] + bb.x, v[4 * i + 1] + bb.y);
+                    const __nv_bfloat162 h1 =
+                        __floats2bfloat162_rn(v[4 * i + 2] + bb.z, v[4 * i + 3] + bb.w);
+                    o[2 * i] = *reinterpret_cast<const uint32_t*>(&h0);
+                    o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+                }
+                // the staging buffer of this piece must have been read by its previous store
+                const int buf = (int)(piece & 1u);
+                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                __syncwarp();
+                uint4* dst = reinterpret_cast<uint4*>(stage_ptr + (size_t)buf * kChunk * kChunk * 2 +
+                                                      (size_t)lane * kChunk * 2);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0)
+                    tma_store_2d(&y_map, c0, t * kBM + quarter * 32,
+                                 stage_base + (uint32_t)buf * kChunk * kChunk * 2);
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(a));   // accumulator free for tile + 2
+        }
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
     }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (warp == 0)
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(tmem_cols)
+                     "r"(2 * kAccCols)
                      : "memory");
 }
 
@@ -285,17 +374,20 @@ EncodeTiled encode_tiled() {
     return fn;
 }
 
-// Row-major bf16 matrix [outer, inner] read in boxes of [box_rows, 64] with the
-// 128-byte swizzle; rows past `outer` read as zero.
-bool make_map(CUtensorMap* map, const void* ptr, int inner, int outer, int box_rows) {
+// Row-major bf16 matrix [outer, inner] moved in boxes of [box_rows, box_cols]
+// (with the 128-byte swizzle when swizzle); elements past the matrix read as
+// zero and are not written.
+bool make_map(CUtensorMap* map, const void* ptr, int inner, int outer, int box_cols, int box_rows,
+              bool swizzle) {
     const EncodeTiled enc = encode_tiled();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
     const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
@@ -310,10 +402,11 @@ int sm_count() {
 }  // namespace linear
 }  // namespace msda
 
-extern "C" int msda_linear(const void* x, const void* w, const float* bias, void* y,
+extern "C" int msda_linear(const void* x, const void* w, const void* bias, void* y,
                                     int rows, int in_features, int out_features, int dtype,
                                     void* stream) {
-    if (dtype != MSDA_BF16) return MSDA_ERR_UNSUPPORTED;
+    if ((dtype & ~MSDA_LINEAR_BIAS_BF16) != MSDA_BF16) return MSDA_ERR_UNSUPPORTED;
+    const int bias_bf16 = (dtype & MSDA_LINEAR_BIAS_BF16) ? 1 : 0;
     if (rows < 0 || in_features < 0 || out_features < 0) return MSDA_ERR_DIM;
     using namespace msda::linear;
     if (in_features % kBK != 0 || in_features < kBK || in_features > MSDA_LINEAR_MAX_FEATURES ||
@@ -325,12 +418,11 @@ extern "C" int msda_linear(const void* x, const void* w, const float* bias, void
     if (misaligned(x) || misaligned(w) || misaligned(y) || (bias && misaligned(bias)))
         return MSDA_ERR_ALIGN;
     if ((int64_t)rows * in_features > 2147483647LL * 64) return MSDA_ERR_DIM;
-    CUtensorMap xm, wm;
-    if (!make_map(&xm, x, in_features, rows, kBM) ||
-        !make_map(&wm, w, in_features, out_features, out_features))
+    CUtensorMap xm, wm, ym;
+    if (!make_map(&xm, x, in_features, rows, kBK, kBM, true) ||
+        !make_map(&wm, w, in_features, out_features, kBK, out_features, true) ||
+        !make_map(&ym, y, out_features, rows, kChunk, kChunk, false))
         return MSDA_ERR_CUDA;
-    int cols = 32;
-    while (cols < out_features) cols <<= 1;
     const Smem L = smem_layout(out_features, in_features);
     const size_t smem = (size_t)L.total + 1024;
     static std::once_flag attr_once;
@@ -343,6 +435,6 @@ extern "C" int msda_linear(const void* x, const void* w, const float* bias, void
     const int tiles = (rows + kBM - 1) / kBM;
     const int grid = tiles < sm_count() ? tiles : sm_count();
     linear_bf16_kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-        xm, wm, bias, static_cast<__nv_bfloat16*>(y), rows, out_features, in_features, cols);
+        xm, wm, ym, bias, bias_bf16, rows, out_features, in_features);
     return cudaGetLastError() == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA;
 }

@@ -47,8 +47,7 @@ class TensorCoreLinear(torch.autograd.Function):
     def forward(ctx, x, weight, bias):
         ctx.save_for_backward(x, weight)
         ctx.has_bias = bias is not None
-        return B.msda_linear(x.contiguous(), weight,
-                             None if bias is None else bias.float())
+        return B.msda_linear(x.contiguous(), weight, bias)
 
     @staticmethod
     def backward(ctx, grad_y):
@@ -61,7 +60,7 @@ class TensorCoreLinear(torch.autograd.Function):
             gx = gy @ weight
         g2 = gy.reshape(-1, n_out)
         gw = g2.t() @ x.reshape(-1, n_in)
-        gb = g2.float().sum(0).to(weight.dtype) if ctx.has_bias else None
+        gb = torch.sum(g2, 0, dtype=torch.float32).to(weight.dtype) if ctx.has_bias else None
         return gx, gw, gb
 
 
@@ -70,7 +69,9 @@ def project(linear: nn.Linear, x: torch.Tensor, tensor_cores: bool = True) -> to
     if (tensor_cores and x.is_cuda and x.dtype == torch.bfloat16 and
             linear.weight.dtype == torch.bfloat16 and
             _tensor_core_shape(linear.in_features, linear.out_features)):
-        return TensorCoreLinear.apply(x, linear.weight, linear.bias)
+        if torch.is_grad_enabled() and (x.requires_grad or linear.weight.requires_grad):
+            return TensorCoreLinear.apply(x, linear.weight, linear.bias)
+        return B.msda_linear(x.contiguous(), linear.weight, linear.bias)
     return linear(x)
 
 

@@ -71,3 +71,16 @@ def test_linear_rejects_unsupported_shapes(B):
     with pytest.raises(B.MsdaError) as e:
         B.msda_linear(x, w)                       # out_features not a multiple of 16
     assert e.value.status == 3
+
+
+def test_linear_bf16_bias(B):
+    """The bias may be the bf16 parameter of a bf16 layer (widened in the kernel)."""
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(300, 256, generator=g).to(torch.bfloat16)
+    w = (torch.randn(128, 256, generator=g) / 16).to(torch.bfloat16)
+    b = torch.randn(128, generator=g).to(torch.bfloat16)
+    y = B.msda_linear(x.cuda(), w.cuda(), b.cuda())
+    torch.cuda.synchronize()
+    ref = x.double().numpy() @ w.double().numpy().T + b.double().numpy()
+    err = np.abs(y.float().cpu().double().numpy() - ref)
+    assert (err <= 2.0 ** -8 * np.abs(ref) + 1e-4 * np.abs(ref).max()).all()

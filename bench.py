@@ -183,8 +183,8 @@ def cpu_baseline(wl, inp, budget_s=12.0, min_reps=1):
 
 
 def run_layer(args, wl):
-    """The MSDeformAttn layer (module.MSDeformAttn: four cuBLAS projections around
-    the fused entry points) forward + backward through autograd on the workload's
+    """The MSDeformAttn layer (module.MSDeformAttn: four tensor-core projections
+    around the fused entry points) forward + backward through autograd on the workload's
     shape: seeded random query / input features, the workload's fused reference
     points, the layer's initial parameters.  Each step is timed with CUDA events
     as the layer runs (Python and autograd included); L2 flushed before each."""
@@ -234,22 +234,20 @@ def run_layer(args, wl):
         torch.cuda.synchronize()
         return [e0.elapsed_time(e1) for e0, e1 in evs]
 
-    compare = None
-    if wl.dtype == "bf16":
-        # the same layer with torch.nn.Linear (cuBLAS) projections, for comparison;
-        # both configurations warm up twice as long as asked (first-use costs of
-        # the allocator and of each kernel module)
-        layer.tensor_core_projections = False
-        for _ in range(2 * args.warmup):
-            flush.zero_()
-            step()
-        cublas_ms = timed_steps(args.steps)
-        layer.tensor_core_projections = True
-        for _ in range(args.warmup):
-            flush.zero_()
-            step()
-        compare = {"cublas_projections_ms": statistics.median(cublas_ms),
-                   "gemm": _projection_gemm(layer.output_proj, wl.bs * wl.num_keys, dev, flush)}
+    # the same layer with torch.nn.Linear (cuBLAS) projections, for comparison;
+    # both configurations warm up twice as long as asked (first-use costs of
+    # the allocator and of each kernel module)
+    layer.tensor_core_projections = False
+    for _ in range(2 * args.warmup):
+        flush.zero_()
+        step()
+    cublas_ms = timed_steps(args.steps)
+    layer.tensor_core_projections = True
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    compare = {"cublas_projections_ms": statistics.median(cublas_ms),
+               "gemm": _projection_gemm(layer.output_proj, wl.bs * wl.num_keys, dev, flush)}
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -279,7 +277,10 @@ def run_layer(args, wl):
     cfg["entry_points"] = ("module.MSDeformAttn: value / offset / weight / output projections "
                            + ("(msda_linear on the tensor cores forward and for the input "
                               "gradients; weight gradients with torch, cuBLAS bf16)"
-                              if wl.dtype == "bf16" else "(torch Linear, cuBLAS fp32)")
+                              if wl.dtype == "bf16" else
+                              "(msda_linear_f32, three TF32 products on the tensor cores, "
+                              "forward and for the input gradients; weight gradients with "
+                              "torch, cuBLAS fp32)")
                            + " around msda_forward_fused / msda_backward_fused, autograd")
     cfg["launch"] = "eager through autograd (no graphs; Python and autograd inside the events)"
     line = {
@@ -293,9 +294,10 @@ def run_layer(args, wl):
         "projections": compare,
         "roofline": None, "clocks": clocks, "e2e": None,
         # the library's kernels per step: fused forward; grad_value (or fp32 workspace)
-        # zero-fill + fused backward (+ the bf16 finalize); in bf16 four msda_linear
-        # forward and four backward
-        "gpu_launches": (3 if wl.dtype == "f32" else 4 + 8) * args.steps,
+        # zero-fill + fused backward (+ the bf16 finalize); four projections forward
+        # and four input gradients, one launch each in bf16 and three (two splits and
+        # the GEMM) in fp32
+        "gpu_launches": (3 + 8 * 3 if wl.dtype == "f32" else 4 + 8) * args.steps,
     }
     print(json.dumps(line), flush=True)
     if dist:
@@ -310,10 +312,13 @@ def _projection_gemm(linear, rows, dev, flush, reps=20):
     import torch.nn.functional as F
     from scale_deformable_attention_05_b300 import binding as B
     g = torch.Generator(device=dev).manual_seed(11)
-    xg = torch.randn(rows, linear.in_features, generator=g, device=dev).to(torch.bfloat16)
+    dt = linear.weight.dtype
+    xg = torch.randn(rows, linear.in_features, generator=g, device=dev).to(dt)
     w, b = linear.weight.detach(), linear.bias.detach()
     bf = b.float()
-    out = torch.empty(rows, linear.out_features, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(rows, linear.out_features, dtype=dt, device=dev)
+    ws = torch.empty(B.msda_linear_workspace_bytes(rows, linear.in_features, linear.out_features),
+                     dtype=torch.uint8, device=dev)
 
     def timed(fn):
         for _ in range(3):
@@ -329,10 +334,13 @@ def _projection_gemm(linear, rows, dev, flush, reps=20):
             ts.append(e0.elapsed_time(e1))
         return statistics.median(ts)
 
-    tc = timed(lambda: B.msda_linear(xg, w, bf, out=out))
+    if dt == torch.bfloat16:
+        tc = timed(lambda: B.msda_linear(xg, w, bf, out=out))
+    else:
+        tc = timed(lambda: B.msda_linear_f32(xg, w, b, out=out, workspace=ws))
     cb = timed(lambda: F.linear(xg, w, b))
     flops = 2.0 * rows * linear.in_features * linear.out_features
-    nbytes = 2.0 * rows * (linear.in_features + linear.out_features)
+    nbytes = float(xg.element_size()) * rows * (linear.in_features + linear.out_features)
     return {"rows": rows, "in_features": linear.in_features,
             "out_features": linear.out_features,
             "tcgen05_us": tc * 1e3, "cublas_us": cb * 1e3,

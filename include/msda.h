@@ -295,6 +295,35 @@ MSDA_API int msda_backward_noalloc(const void* value, const void* spatial_shapes
 MSDA_API int msda_linear(const void* x, const void* w, const void* bias, void* y, int rows,
                          int in_features, int out_features, int dtype, void* stream);
 
+/*
+ * The same projection in fp32 on the tensor cores, to fp32 accuracy: each
+ * operand is split into its TF32 rounding and the exact remainder,
+ * a = a_hi + a_lo, and the product is accumulated in fp32 as
+ * x_hi w_hi + x_hi w_lo + x_lo w_hi (three tcgen05.mma of kind::tf32 per K
+ * step).  The dropped x_lo w_lo term and the TF32 reading of the remainders
+ * contribute below 2^-19 of sum_k |x[r,k]| |w[n,k]|, under fp32 accumulation's
+ * own rounding.
+ *   x    [rows, in_features]          fp32, row-major, device pointer
+ *   w    [out_features, in_features]  fp32 (nn.Linear weight layout)
+ *   bias [out_features]               fp32 or NULL
+ *   y    [rows, out_features]         fp32, overwritten
+ *   workspace  device scratch of at least msda_linear_workspace_bytes(rows,
+ *              in_features, out_features, MSDA_F32) bytes, 16-byte aligned,
+ *              owned by the caller; overwritten (the four split operands)
+ * in_features must be a multiple of 32 and out_features a multiple of 16,
+ * both at most MSDA_LINEAR_MAX_FEATURES (else MSDA_ERR_UNSUPPORTED); every
+ * pointer 16-byte aligned (MSDA_ERR_ALIGN); a short or NULL workspace gives
+ * MSDA_ERR_WORKSPACE.  Three launches on `stream`: the splits of x and of w,
+ * then the GEMM (persistent CTAs, TMA loads and stores, two accumulators in
+ * tensor memory).  A device-side wait that runs out of its iteration limit
+ * stops the kernel and raises the error word msda_last_device_error() reads.
+ */
+MSDA_API size_t msda_linear_workspace_bytes(int rows, int in_features, int out_features,
+                                            int dtype);
+MSDA_API int msda_linear_f32(const float* x, const float* w, const float* bias, float* y,
+                             void* workspace, size_t workspace_bytes, int rows, int in_features,
+                             int out_features, void* stream);
+
 /* MSDA_VERSION of the built library. */
 MSDA_API int msda_version(void);
 

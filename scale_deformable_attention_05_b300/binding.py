@@ -21,6 +21,7 @@ __all__ = [
     "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
     "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused", "msda_linear",
+    "msda_linear_f32", "msda_linear_workspace_bytes",
     "MSDeformAttnFunction", "MSDeformAttnFusedFunction", "ms_deform_attn", "ms_deform_attn_fused",
     "EXPORTED_SYMBOLS", "load_library",
 ]
@@ -39,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
     "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused", "msda_linear",
+    "msda_linear_f32", "msda_linear_workspace_bytes",
 )
 
 _vp = ctypes.c_void_p
@@ -78,6 +80,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msda_backward_noalloc.restype = _int
     lib.msda_linear.argtypes = [_vp] * 4 + [_int] * 4 + [_vp]
     lib.msda_linear.restype = _int
+    lib.msda_linear_workspace_bytes.argtypes = [_int] * 4
+    lib.msda_linear_workspace_bytes.restype = ctypes.c_size_t
+    lib.msda_linear_f32.argtypes = [_vp] * 5 + [ctypes.c_size_t] + [_int] * 3 + [_vp]
+    lib.msda_linear_f32.restype = _int
     lib.msda_forward_fused.argtypes = [_vp] * 8 + _DIMS + [_int, _int, _vp]
     lib.msda_forward_fused.restype = _int
     lib.msda_backward_fused.argtypes = ([_vp] * 13 + [ctypes.c_size_t] + _DIMS +
@@ -280,6 +286,47 @@ def msda_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tens
     _check("msda_linear", _LIB.msda_linear(
         _ptr(x2), _ptr(weight), _ptr(bias) if bias is not None else None, _ptr(out),
         int(x2.shape[0]), int(x2.shape[1]), n_out, code, _stream(stream)))
+    return out
+
+
+def msda_linear_workspace_bytes(rows: int, in_features: int, out_features: int,
+                                dtype: int = MSDA_F32) -> int:
+    return int(_LIB.msda_linear_workspace_bytes(rows, in_features, out_features, dtype))
+
+
+def msda_linear_f32(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                    out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """y = x @ weight.T + bias in fp32 on the tensor cores, three TF32 products
+    (see msda_linear_f32 in include/msda.h): x [..., in], weight [out, in] and
+    bias [out] (or None) fp32 CUDA tensors; returns fp32 [..., out].  The split
+    operands go to `workspace` (allocated here when None)."""
+    if x.dtype != torch.float32 or weight.dtype != torch.float32:
+        raise TypeError("msda_linear_f32 takes fp32 x and weight")
+    if not (x.is_cuda and weight.is_cuda) or x.device != weight.device:
+        raise ValueError("x and weight must be CUDA tensors on one device")
+    if weight.dim() != 2 or x.shape[-1] != weight.shape[1]:
+        raise ValueError("weight must be [out_features, in_features] with in_features = x.shape[-1]")
+    x2 = x.reshape(-1, x.shape[-1])
+    if not x2.is_contiguous():
+        raise ValueError("x must be contiguous")
+    weight = weight.contiguous()
+    rows, n_in, n_out = int(x2.shape[0]), int(x2.shape[1]), int(weight.shape[0])
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.shape != (n_out,) or bias.device != x.device:
+            raise ValueError("bias must be an fp32 [out_features] tensor on x's device")
+        bias = bias.contiguous()
+    if out is None:
+        out = torch.empty(*x.shape[:-1], n_out, dtype=torch.float32, device=x.device)
+    elif out.dtype != torch.float32 or out.shape != (*x.shape[:-1], n_out) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous fp32 [..., out_features] tensor")
+    need = msda_linear_workspace_bytes(rows, n_in, n_out, MSDA_F32)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("msda_linear_f32", _LIB.msda_linear_f32(
+        _ptr(x2), _ptr(weight), _ptr(bias) if bias is not None else None, _ptr(out),
+        _ptr(workspace), ws_bytes, rows, n_in, n_out, _stream(stream)))
     return out
 
 

@@ -355,6 +355,223 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
 }
 
+// ---------------------------------------------------------- fp32 (3 x TF32)
+// fp32 projections keep fp32 accuracy on the tensor cores by splitting each
+// operand into a TF32 head and the fp32 remainder, a = a_hi + a_lo with a_hi =
+// a rounded to TF32 (10 explicit mantissa bits) and a_lo = a - a_hi exact, and
+// summing three TF32 products, x_hi w_hi + x_hi w_lo + x_lo w_hi, in the fp32
+// accumulator (the dropped x_lo w_lo and the TF32 reading of the remainders
+// are below 2^-20 of |x||w|).  A first kernel writes the four parts to the
+// caller's workspace; the GEMM streams them through a 2-stage TMA ring (both
+// parts of an x block and of a w block per stage) and issues the three
+// kind::tf32 MMAs per K step of 8; the epilogue writes fp32 with TMA stores.
+constexpr int kBKF = 32;                 // fp32 columns per 128-byte swizzle atom
+constexpr int kStagesF = 2;
+
+__global__ void split_tf32_kernel(const float4* __restrict__ a, float4* __restrict__ hi,
+                                  float4* __restrict__ lo, size_t n4) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const float4 v = a[i];
+        float h[4];
+        const float in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t t;
+            asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(t) : "f"(in[j]));
+            h[j] = __uint_as_float(t);
+        }
+        hi[i] = make_float4(h[0], h[1], h[2], h[3]);
+        lo[i] = make_float4(in[0] - h[0], in[1] - h[1], in[2] - h[2], in[3] - h[3]);
+    }
+}
+
+// Instruction descriptor of kind::tf32 (TF32 A and B, fp32 D, both K-major), M = 128, N = n.
+__host__ __device__ constexpr uint32_t tf32_idesc(int n) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate));
+}
+
+struct SmemF {
+    uint32_t stage_bytes, stages, stage_out, bias, bars, tmem_slot, total;
+};
+__host__ __device__ inline SmemF smem_layout_f(int n) {
+    SmemF s;
+    s.stage_bytes = 2u * kBM * 128 + 2u * (uint32_t)n * 128;   // x_hi, x_lo, w_hi, w_lo blocks
+    s.stages = 0;
+    s.stage_out = s.stages + kStagesF * s.stage_bytes;         // 32 x 32 fp32 per epilogue warp
+    s.bias = s.stage_out + (uint32_t)kEpiWarps * kChunk * kChunk * 4;
+    s.bars = s.bias + MSDA_LINEAR_MAX_FEATURES * 4;
+    s.tmem_slot = s.bars + (4 * kStagesF + 4) * 8;
+    s.total = s.tmem_slot + 8;
+    return s;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_f32x3_kernel(const __grid_constant__ CUtensorMap xhi_map,
+                        const __grid_constant__ CUtensorMap xlo_map,
+                        const __grid_constant__ CUtensorMap whi_map,
+                        const __grid_constant__ CUtensorMap wlo_map,
+                        const __grid_constant__ CUtensorMap y_map, const float* __restrict__ bias,
+                        int rows, int n, int k) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const SmemF L = smem_layout_f(n);
+    const uint32_t s_stage = smem_u32(base + L.stages);
+    auto xhi = [&](int s) { return s_stage + (uint32_t)s * L.stage_bytes; };
+    auto xlo = [&](int s) { return xhi(s) + (uint32_t)kBM * 128; };
+    auto whi = [&](int s) { return xhi(s) + 2u * kBM * 128; };
+    auto wlo = [&](int s) { return whi(s) + (uint32_t)n * 128; };
+    const uint32_t bars = smem_u32(base + L.bars);
+    auto x_full = [&](int s) { return bars + 8u * s; };
+    auto x_empty = [&](int s) { return bars + 8u * (kStagesF + s); };
+    auto acc_full = [&](int a) { return bars + 8u * (2 * kStagesF + a); };
+    auto acc_empty = [&](int a) { return bars + 8u * (2 * kStagesF + 2 + a); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.tmem_slot);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kblocks = k / kBKF;
+    const int tiles = (rows + kBM - 1) / kBM;
+
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(2 * kAccCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStagesF; ++s) {
+            mbar_init(x_full(s), 1);
+            mbar_init(x_empty(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full(a), 1);
+            mbar_init(acc_empty(a), kEpiWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---- producer: both parts of an x block and of a w block per stage
+        if (lane == 0) {
+            const uint32_t bytes = 2u * kBM * 128 + 2u * (uint32_t)n * 128;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x)
+                for (int kb = 0; kb < kblocks && ok; ++kb, ++it) {
+                    const int s = (int)(it % kStagesF);
+                    const uint32_t ph = (it / kStagesF) & 1u;
+                    ok = mbar_wait(x_empty(s), ph ^ 1u);
+                    if (!ok) break;
+                    mbar_expect_tx(x_full(s), bytes);
+                    tma_load_2d(xhi(s), &xhi_map, kb * kBKF, t * kBM, x_full(s));
+                    tma_load_2d(xlo(s), &xlo_map, kb * kBKF, t * kBM, x_full(s));
+                    tma_load_2d(whi(s), &whi_map, kb * kBKF, 0, x_full(s));
+                    tma_load_2d(wlo(s), &wlo_map, kb * kBKF, 0, x_full(s));
+                }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer: three TF32 products per K step of 8
+        if (lane == 0) {
+            const uint32_t idesc = tf32_idesc(n);
+            bool ok = true;
+            uint32_t it = 0, acc_it = 0;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++acc_it) {
+                const int a = (int)(acc_it & 1u);
+                ok = mbar_wait(acc_empty(a), ((acc_it >> 1) & 1u) ^ 1u);
+                if (!ok) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t d = tmem + (uint32_t)(a * kAccCols);
+                for (int kb = 0; kb < kblocks && ok; ++kb, ++it) {
+                    const int s = (int)(it % kStagesF);
+                    ok = mbar_wait(x_full(s), (it / kStagesF) & 1u);
+                    if (!ok) break;
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+                    for (int ks = 0; ks < kBKF / 8; ++ks) {
+                        const uint32_t koff = (uint32_t)ks * 32;   // 8 fp32 columns
+                        const uint64_t ah = kmajor_sw128_desc(xhi(s) + koff);
+                        const uint64_t al = kmajor_sw128_desc(xlo(s) + koff);
+                        const uint64_t bh = kmajor_sw128_desc(whi(s) + koff);
+                        const uint64_t bl = kmajor_sw128_desc(wlo(s) + koff);
+                        umma_tf32(d, ah, bh, idesc, kb > 0 || ks > 0);
+                        umma_tf32(d, ah, bl, idesc, true);
+                        umma_tf32(d, al, bh, idesc, true);
+                    }
+                    umma_commit(x_empty(s));
+                }
+                if (ok) umma_commit(acc_full(a));
+            }
+        }
+    } else {
+        // ---- epilogue: as in the bf16 kernel, fp32 pieces staged with the 128-byte swizzle
+        const int quarter = warp & 3;
+        const int ew = warp - 2;
+        const int half = ew >> 2;
+        float* s_bias = reinterpret_cast<float*>(base + L.bias);
+        for (int c = ew * 32 + lane; c < MSDA_LINEAR_MAX_FEATURES; c += kEpiWarps * 32)
+            s_bias[c] = bias != nullptr && c < n ? bias[c] : 0.f;
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+        const uint32_t stage_addr = smem_u32(base + L.stage_out) + (uint32_t)ew * kChunk * kChunk * 4;
+        unsigned char* stage_ptr = base + L.stage_out + (size_t)ew * kChunk * kChunk * 4;
+        uint32_t acc_it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++acc_it) {
+            const int a = (int)(acc_it & 1u);
+            ok = mbar_wait(acc_full(a), (acc_it >> 1) & 1u);
+            if (!ok) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t taddr =
+                tmem + (uint32_t)(a * kAccCols) + ((uint32_t)(quarter * 32) << 16);
+            for (int c0 = half * kChunk; c0 < n; c0 += 2 * kChunk) {
+                float v[32];
+                tmem_ld32(taddr + (uint32_t)c0, v);
+                const float4* bq = reinterpret_cast<const float4*>(s_bias + c0);
+                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                __syncwarp();
+                // row `lane` of the piece: 16-byte chunk j at position j ^ (row % 8)
+                unsigned char* row = stage_ptr + (size_t)lane * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 bb = bq[j];
+                    *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
+                        make_float4(v[4 * j] + bb.x, v[4 * j + 1] + bb.y, v[4 * j + 2] + bb.z,
+                                    v[4 * j + 3] + bb.w);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) tma_store_2d(&y_map, c0, t * kBM + quarter * 32, stage_addr);
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(a));
+        }
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(2 * kAccCols)
+                     : "memory");
+}
+
 // ------------------------------------------------------------------- host
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -374,18 +591,19 @@ EncodeTiled encode_tiled() {
     return fn;
 }
 
-// Row-major bf16 matrix [outer, inner] moved in boxes of [box_rows, box_cols]
+// Row-major bf16 (or fp32) matrix [outer, inner] moved in boxes of [box_rows, box_cols]
 // (with the 128-byte swizzle when swizzle); elements past the matrix read as
 // zero and are not written.
 bool make_map(CUtensorMap* map, const void* ptr, int inner, int outer, int box_cols, int box_rows,
-              bool swizzle) {
+              bool swizzle, bool fp32 = false) {
     const EncodeTiled enc = encode_tiled();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-    const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)inner * (fp32 ? 4 : 2)};
     const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+    return enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void*>(ptr), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
@@ -436,5 +654,64 @@ extern "C" int msda_linear(const void* x, const void* w, const void* bias, void*
     const int grid = tiles < sm_count() ? tiles : sm_count();
     linear_bf16_kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
         xm, wm, ym, bias, bias_bf16, rows, out_features, in_features);
+    return cudaGetLastError() == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA;
+}
+
+extern "C" size_t msda_linear_workspace_bytes(int rows, int in_features, int out_features,
+                                              int dtype) {
+    if (dtype != MSDA_F32 || rows < 0 || in_features < 0 || out_features < 0) return 0;
+    return ((size_t)rows + (size_t)out_features) * (size_t)in_features * 2 * sizeof(float);
+}
+
+extern "C" int msda_linear_f32(const float* x, const float* w, const float* bias, float* y,
+                               void* workspace, size_t workspace_bytes, int rows, int in_features,
+                               int out_features, void* stream) {
+    using namespace msda::linear;
+    if (rows < 0 || in_features < 0 || out_features < 0) return MSDA_ERR_DIM;
+    if (in_features % kBKF != 0 || in_features < kBKF ||
+        in_features > MSDA_LINEAR_MAX_FEATURES || out_features % 16 != 0 || out_features < 16 ||
+        out_features > MSDA_LINEAR_MAX_FEATURES)
+        return MSDA_ERR_UNSUPPORTED;
+    if (rows == 0) return MSDA_OK;
+    if (x == nullptr || w == nullptr || y == nullptr) return MSDA_ERR_NULL;
+    const auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (misaligned(x) || misaligned(w) || misaligned(y) || (bias && misaligned(bias)))
+        return MSDA_ERR_ALIGN;
+    const size_t need = msda_linear_workspace_bytes(rows, in_features, out_features, MSDA_F32);
+    if (workspace == nullptr || workspace_bytes < need) return MSDA_ERR_WORKSPACE;
+    if (misaligned(workspace)) return MSDA_ERR_ALIGN;
+    if ((int64_t)rows * in_features > 2147483647LL * 64) return MSDA_ERR_DIM;
+    float* x_hi = static_cast<float*>(workspace);
+    float* x_lo = x_hi + (size_t)rows * in_features;
+    float* w_hi = x_lo + (size_t)rows * in_features;
+    float* w_lo = w_hi + (size_t)out_features * in_features;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int sms = sm_count();
+    const size_t nx4 = (size_t)rows * in_features / 4, nw4 = (size_t)out_features * in_features / 4;
+    split_tf32_kernel<<<sms * 4, 256, 0, st>>>(reinterpret_cast<const float4*>(x),
+                                                 reinterpret_cast<float4*>(x_hi),
+                                                 reinterpret_cast<float4*>(x_lo), nx4);
+    split_tf32_kernel<<<sms, 256, 0, st>>>(reinterpret_cast<const float4*>(w),
+                                            reinterpret_cast<float4*>(w_hi),
+                                            reinterpret_cast<float4*>(w_lo), nw4);
+    if (cudaGetLastError() != cudaSuccess) return MSDA_ERR_CUDA;
+    CUtensorMap xh, xl, wh, wl, ym;
+    if (!make_map(&xh, x_hi, in_features, rows, kBKF, kBM, true, true) ||
+        !make_map(&xl, x_lo, in_features, rows, kBKF, kBM, true, true) ||
+        !make_map(&wh, w_hi, in_features, out_features, kBKF, out_features, true, true) ||
+        !make_map(&wl, w_lo, in_features, out_features, kBKF, out_features, true, true) ||
+        !make_map(&ym, y, out_features, rows, kChunk, kChunk, true, true))
+        return MSDA_ERR_CUDA;
+    const SmemF L = smem_layout_f(out_features);
+    static std::once_flag attr_once;
+    std::call_once(attr_once, [] {
+        cudaFuncSetAttribute(linear_f32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(smem_layout_f(MSDA_LINEAR_MAX_FEATURES).total + 1024));
+    });
+    const int tiles = (rows + kBM - 1) / kBM;
+    const int grid = tiles < sms ? tiles : sms;
+    linear_f32x3_kernel<<<grid, kThreads, (size_t)L.total + 1024, st>>>(xh, xl, wh, wl, ym, bias,
+                                                                         rows, out_features,
+                                                                         in_features);
     return cudaGetLastError() == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA;
 }

@@ -10,12 +10,12 @@ them,
     out     = output_proj(msda(value masked by input_padding_mask,
                                softmax(logits), reference_points + offsets))
 
-The four projections are dense GEMMs.  In bf16 they run on the library's
-tensor-core kernel (``msda_linear``: tcgen05.mma with the accumulator in tensor
-memory) for the forward and for the input gradient (x-gradient = grad_y times
-the weight, i.e. the same kernel with the transposed weight); the weight
-gradient (a reduction over all tokens) and every fp32 projection use
-``torch.nn.Linear`` (cuBLAS).  Everything between the projections -- masking,
+The four projections are dense GEMMs.  They run on the library's tensor-core
+kernels (tcgen05.mma with the accumulator in tensor memory) for the forward and
+for the input gradient (x-gradient = grad_y times the weight, i.e. the same
+kernel with the transposed weight): ``msda_linear`` in bf16, ``msda_linear_f32``
+(three TF32 products per step, fp32 accuracy) in fp32.  The weight gradient (a
+reduction over all tokens) uses torch (cuBLAS).  Everything between the projections -- masking,
 softmax, locations from 2-d or 4-d reference points, bilinear sampling and
 their backward -- is one launch of the fused entry points of ``libmsda.so``
 each way.  The tensors the GEMMs produce are already in the operator's
@@ -32,30 +32,41 @@ from torch import nn
 from . import binding as B
 
 
-def _tensor_core_shape(in_features: int, out_features: int) -> bool:
-    return (in_features % 64 == 0 and out_features % 16 == 0 and
+_TC_DTYPES = (torch.bfloat16, torch.float32)
+
+
+def _tensor_core_shape(in_features: int, out_features: int, dtype=torch.bfloat16) -> bool:
+    k_step = 64 if dtype == torch.bfloat16 else 32        # one 128-byte swizzle atom of K
+    return (in_features % k_step == 0 and out_features % 16 == 0 and
             in_features <= B.MSDA_LINEAR_MAX_FEATURES and
             out_features <= B.MSDA_LINEAR_MAX_FEATURES)
 
 
+def _tc_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor]) -> torch.Tensor:
+    if x.dtype == torch.bfloat16:
+        return B.msda_linear(x, weight, bias)
+    return B.msda_linear_f32(x, weight, bias)
+
+
 class TensorCoreLinear(torch.autograd.Function):
-    """y = x w^T + b with bf16 x and w on the tensor cores (msda_linear); the
-    input gradient through the same kernel with w^T when its shape allows
-    (else a cuBLAS matmul), the weight and bias gradients with torch."""
+    """y = x w^T + b with x and w both bf16 or both fp32 on the tensor cores
+    (msda_linear / msda_linear_f32); the input gradient through the same kernel
+    with w^T when its shape allows (else a cuBLAS matmul), the weight and bias
+    gradients with torch."""
 
     @staticmethod
     def forward(ctx, x, weight, bias):
         ctx.save_for_backward(x, weight)
         ctx.has_bias = bias is not None
-        return B.msda_linear(x.contiguous(), weight, bias)
+        return _tc_linear(x.contiguous(), weight, bias)
 
     @staticmethod
     def backward(ctx, grad_y):
         x, weight = ctx.saved_tensors
         n_out, n_in = weight.shape
         gy = grad_y.contiguous()
-        if _tensor_core_shape(n_out, n_in):
-            gx = B.msda_linear(gy, weight.t().contiguous())
+        if _tensor_core_shape(n_out, n_in, weight.dtype):
+            gx = _tc_linear(gy, weight.t().contiguous(), None)
         else:
             gx = gy @ weight
         g2 = gy.reshape(-1, n_out)
@@ -65,21 +76,21 @@ class TensorCoreLinear(torch.autograd.Function):
 
 
 def project(linear: nn.Linear, x: torch.Tensor, tensor_cores: bool = True) -> torch.Tensor:
-    """linear(x), on the tensor-core kernel for bf16 operands of supported widths."""
-    if (tensor_cores and x.is_cuda and x.dtype == torch.bfloat16 and
-            linear.weight.dtype == torch.bfloat16 and
-            _tensor_core_shape(linear.in_features, linear.out_features)):
+    """linear(x), on the tensor-core kernels for bf16 or fp32 operands of supported widths."""
+    if (tensor_cores and x.is_cuda and x.dtype in _TC_DTYPES and
+            linear.weight.dtype == x.dtype and
+            _tensor_core_shape(linear.in_features, linear.out_features, x.dtype)):
         if torch.is_grad_enabled() and (x.requires_grad or linear.weight.requires_grad):
             return TensorCoreLinear.apply(x, linear.weight, linear.bias)
-        return B.msda_linear(x.contiguous(), linear.weight, linear.bias)
+        return _tc_linear(x.contiguous(), linear.weight, linear.bias)
     return linear(x)
 
 
 class MSDeformAttn(nn.Module):
     """Multi-scale deformable attention with d_model channels split into
     n_heads heads, sampling n_points points on each of n_levels levels.
-    tensor_core_projections: bf16 projections on the library's tensor-core
-    kernel (True) or on torch.nn.Linear (False)."""
+    tensor_core_projections: bf16 and fp32 projections on the library's
+    tensor-core kernels (True) or on torch.nn.Linear (False)."""
 
     tensor_core_projections = True
 

@@ -84,3 +84,73 @@ def test_linear_bf16_bias(B):
     ref = x.double().numpy() @ w.double().numpy().T + b.double().numpy()
     err = np.abs(y.float().cpu().double().numpy() - ref)
     assert (err <= 2.0 ** -8 * np.abs(ref) + 1e-4 * np.abs(ref).max()).all()
+
+
+# ----------------------------------------------------------------------------- fp32 (3 x TF32)
+# msda_linear_f32 against the same fp64 product.  Bound, from the arithmetic:
+# x = x_hi + x_lo exactly with |x_lo| <= 2^-11 |x| (TF32 keeps 10 explicit
+# mantissa bits, rounded to nearest); the three products miss x_lo w_lo
+# (<= 2^-22 |x||w|) and read the remainders as TF32 (<= 2^-10 of each, so
+# <= 2^-21 |x||w| twice): <= 2^-19.4 |x||w| per term.  The fp32 accumulation
+# of K <= 256 terms adds at most K u S with u = 2^-24 and S = sum |x||w|, but
+# sums of signed random terms stay near u S; the test allows 2^-18 S, which a
+# single TF32 product (about 2^-12 |x||w| per term) exceeds.
+
+def _check_f32(B, rows, k, n, bias=True, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(rows, k, generator=g)
+    w = torch.randn(n, k, generator=g) / np.sqrt(k)
+    b = torch.randn(n, generator=g) if bias else None
+    y = B.msda_linear_f32(x.cuda(), w.cuda(), b.cuda() if bias else None)
+    torch.cuda.synchronize()
+    assert B.msda_last_device_error() == 0
+    xd, wd = x.double().numpy(), w.double().numpy()
+    ref = xd @ wd.T + (b.double().numpy() if bias else 0.0)
+    s = np.abs(xd) @ np.abs(wd).T
+    err = np.abs(y.cpu().double().numpy() - ref)
+    bound = 2.0 ** -18 * s + (2.0 ** -23 * np.abs(b.double().numpy()) if bias else 0.0)
+    assert (err <= bound).all(), f"max err {err.max():.3e}, worst excess {(err - bound).max():.3e}"
+    return err, s
+
+
+@pytest.mark.parametrize("rows,k,n", [
+    (128, 256, 256),          # one full tile
+    (300, 256, 256),          # a ragged last tile
+    (1, 32, 16),              # smallest shapes
+    (1000, 256, 128),         # attention-weight projection width
+    (517, 96, 80),            # K of three fp32 swizzle atoms, N not a power of two
+    (44446, 256, 256),        # encoder tokens x d_model: many tiles per CTA
+])
+def test_linear_f32_matches_fp64(B, rows, k, n):
+    _check_f32(B, rows, k, n, seed=rows + k + n)
+
+
+def test_linear_f32_is_more_accurate_than_one_tf32_product(B):
+    """The split matters: the error stays far below what TF32 operands alone give."""
+    err, s = _check_f32(B, 2048, 256, 256, bias=False, seed=11)
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(2048, 256, generator=g)
+    w = torch.randn(256, 256, generator=g) / 16
+    tf32 = lambda a: (a.view(torch.int32) + 0x1000 & ~0x1FFF).view(torch.float32)  # round to 10 bits
+    one = tf32(x).double() @ tf32(w).double().T
+    err1 = (one - x.double() @ w.double().T).abs().numpy()
+    assert err.max() * 16 < err1.max()
+
+
+def test_linear_f32_without_bias_batched_and_checks(B):
+    _check_f32(B, 257, 128, 64, bias=False, seed=3)
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(2, 37, 256, generator=g).cuda()
+    w = torch.randn(128, 256, generator=g).cuda()
+    ws = torch.empty(B.msda_linear_workspace_bytes(74, 256, 128), dtype=torch.uint8, device="cuda")
+    y = B.msda_linear_f32(x, w, workspace=ws)
+    ref = x.double() @ w.double().T
+    torch.cuda.synchronize()
+    assert y.shape == (2, 37, 128)
+    assert (y.double() - ref).abs().max().item() <= 2.0 ** -18 * (x.abs().double() @ w.abs().double().T).max().item()
+    with pytest.raises(B.MsdaError) as e:
+        B.msda_linear_f32(x, w, workspace=ws[:-16])           # workspace one chunk short
+    assert e.value.status == 5
+    with pytest.raises(B.MsdaError) as e:
+        B.msda_linear_f32(torch.zeros(8, 48, device="cuda"), torch.zeros(16, 48, device="cuda"))
+    assert e.value.status == 3                                 # in_features not a multiple of 32

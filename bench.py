@@ -187,7 +187,9 @@ def run_layer(args, wl):
     around the fused entry points) forward + backward through autograd on the workload's
     shape: seeded random query / input features, the workload's fused reference
     points, the layer's initial parameters.  Each step is timed with CUDA events
-    as the layer runs (Python and autograd included); L2 flushed before each."""
+    as the layer runs (Python and autograd included) and, unless --no-graph, as
+    replays of one CUDA graph of the whole step (the line's value); L2 flushed
+    before each."""
     import torch
     ws, rank, local = _dist()
     torch.cuda.set_device(local)
@@ -223,51 +225,73 @@ def run_layer(args, wl):
         q.grad = x.grad = None
         layer(q, ref, x, shapes, lsi, mask).backward(go)
 
-    def timed_steps(n):
+    def timed_steps(n, run=step, sampler=None):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
         for e0, e1 in evs:
             flush.zero_()
             e0.record()
-            step()
+            run()
             e1.record()
         torch.cuda.synchronize()
-        return [e0.elapsed_time(e1) for e0, e1 in evs]
+        clocks = sampler.stop() if sampler else None
+        return [e0.elapsed_time(e1) for e0, e1 in evs], clocks
 
-    # the same layer with torch.nn.Linear (cuBLAS) projections, for comparison;
-    # both configurations warm up twice as long as asked (first-use costs of
-    # the allocator and of each kernel module)
-    layer.tensor_core_projections = False
-    for _ in range(2 * args.warmup):
-        flush.zero_()
-        step()
-    cublas_ms = timed_steps(args.steps)
-    layer.tensor_core_projections = True
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    compare = {"cublas_projections_ms": statistics.median(cublas_ms),
-               "gemm": _projection_gemm(layer.output_proj, wl.bs * wl.num_keys, dev, flush)}
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
+    def capture():
+        """The whole forward + backward as one CUDA graph (warmed up on a side
+        stream first, gradients unset so that the captured backward writes them
+        into the graph's own memory); replays rewrite the same gradient tensors."""
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        for prm in layer.parameters():
+            prm.grad = None
+        q.grad = x.grad = None
+        with torch.cuda.graph(graph):
+            layer(q, ref, x, shapes, lsi, mask).backward(go)
+        torch.cuda.synchronize()
+        return graph
+
+    use_graph = not args.no_graph
+
+    def measure(tensor_cores, warmup, sampler=None):
+        layer.tensor_core_projections = tensor_cores
+        for _ in range(warmup):
+            flush.zero_()
+            step()
+        eager, clk = timed_steps(args.steps, sampler=None if use_graph else sampler)
+        if not use_graph:
+            return eager, None, clk
+        graph = capture()
+        for _ in range(2):
+            graph.replay()
+        replayed, clk = timed_steps(args.steps, run=graph.replay, sampler=sampler)
+        del graph
+        return eager, replayed, clk
+
+    # the same layer with torch.nn.Linear (cuBLAS) projections first, for
+    # comparison; it warms up twice as long as asked (first-use costs of the
+    # allocator and of each kernel module)
+    cb_eager, cb_graph, _ = measure(False, 2 * args.warmup)
+    compare = {"cublas_projections_ms": statistics.median(cb_graph or cb_eager),
+               "cublas_projections_eager_ms": statistics.median(cb_eager),
+               "gemm": None}
     if dist:
         dist.barrier()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     sampler = ClockSampler(local)
-    sampler.start()
-    for e0, e1 in ev:
-        flush.zero_()
-        e0.record()
-        step()
-        e1.record()
-    torch.cuda.synchronize()
+    tc_eager, tc_graph, clocks = measure(True, args.warmup, sampler)
     if dist:
         dist.barrier()
-    clocks = sampler.stop()
-    ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    compare["gemm"] = _projection_gemm(layer.output_proj, wl.bs * wl.num_keys, dev, flush)
+    ms = tc_graph or tc_eager
     ms_step = max_over_ranks(sum(ms) / len(ms), dist, dev)
     if rank != 0:
         if dist:
@@ -282,7 +306,10 @@ def run_layer(args, wl):
                               "forward and for the input gradients; weight gradients with "
                               "torch, cuBLAS fp32)")
                            + " around msda_forward_fused / msda_backward_fused, autograd")
-    cfg["launch"] = "eager through autograd (no graphs; Python and autograd inside the events)"
+    cfg["launch"] = ("eager through autograd (Python and autograd inside the events)"
+                     if not use_graph else
+                     "forward + backward through autograd captured once as one CUDA graph and "
+                     "replayed (the eager step is timed beside it)")
     line = {
         "metric": METRIC, "value": job_rate(wl.points, ws, ms_step), "unit": "points/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -290,7 +317,9 @@ def run_layer(args, wl):
         "data": "synthetic (random query / input features, initial layer parameters)",
         "config": cfg,
         "passes": {"layer": {"ms": sum(ms) / len(ms), "median_ms": statistics.median(ms),
-                             "min_ms": min(ms)}},
+                             "min_ms": min(ms)},
+                   "layer_eager": {"ms": sum(tc_eager) / len(tc_eager),
+                                   "median_ms": statistics.median(tc_eager)}},
         "projections": compare,
         "roofline": None, "clocks": clocks, "e2e": None,
         # the library's kernels per step: fused forward; grad_value (or fp32 workspace)
@@ -306,8 +335,9 @@ def run_layer(args, wl):
 
 
 def _projection_gemm(linear, rows, dev, flush, reps=20):
-    """One d_model x d_model projection of `rows` bf16 tokens: msda_linear (tcgen05)
-    against torch's F.linear (cuBLAS), CUDA events, L2 flushed before each call."""
+    """One d_model x d_model projection of `rows` tokens in the layer's dtype:
+    msda_linear / msda_linear_f32 (tcgen05) against torch's F.linear (cuBLAS),
+    CUDA events, L2 flushed before each call."""
     import torch
     import torch.nn.functional as F
     from scale_deformable_attention_05_b300 import binding as B
@@ -321,18 +351,20 @@ def _projection_gemm(linear, rows, dev, flush, reps=20):
                      dtype=torch.uint8, device=dev)
 
     def timed(fn):
+        # every rep enqueued before the one synchronisation, so that the host's
+        # marshalling runs ahead of the device and stays outside the events
         for _ in range(3):
             fn()
-        ts = []
-        for _ in range(reps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
             flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()
             e1.record()
-            e1.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        return statistics.median(ts)
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
 
     if dt == torch.bfloat16:
         tc = timed(lambda: B.msda_linear(xg, w, bf, out=out))

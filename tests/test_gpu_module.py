@@ -174,3 +174,67 @@ def test_bf16_module_on_tensor_cores_matches_fp64_composition():
     got.update(query=tq.grad, input_flatten=tx.grad, reference_points=tref.grad)
     for name, ref_grad in grads.items():
         assert_grad_close(host(got[name]), ref_grad, "bf16", name)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_module_step_replays_as_one_cuda_graph(dtype):
+    """Forward + backward of the layer captured as one CUDA graph (every entry
+    point on the caller's stream, no host synchronisation, workspaces from the
+    caller's allocator) and replayed: output and gradients equal the eager
+    step's up to the order of the backward's atomic sums."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from scale_deformable_attention_05_b300.module import MSDeformAttn
+    torch.backends.cuda.matmul.allow_tf32 = False
+    shapes = ((16, 20), (8, 10))
+    C, M, L, P, N, Q = 128, 4, len(shapes), 4, 2, 300
+    wl = gen.random_workload(5, N, shapes, M, C // M, P, Q)
+    g = torch.Generator().manual_seed(5)
+    layer = MSDeformAttn(C, L, M, P).cuda().to(dtype)
+    q = torch.randn(N, Q, C, generator=g).cuda().to(dtype).requires_grad_()
+    x = torch.randn(N, wl.num_keys, C, generator=g).cuda().to(dtype).requires_grad_()
+    go = torch.randn(N, Q, C, generator=g).cuda().to(dtype)
+    ref = torch.rand(N, Q, L, 2, generator=g).cuda().to(dtype)
+    sh = torch.tensor(shapes, dtype=torch.int64, device="cuda")
+    lsi = torch.from_numpy(gen.level_start_index(shapes)).cuda()
+
+    def run():
+        out = layer(q, ref, x, sh, lsi)
+        out.backward(go)
+        return out
+
+    def clear():
+        for p in layer.parameters():
+            p.grad = None
+        q.grad = x.grad = None
+
+    def grads():
+        d = {n: p.grad.detach().clone() for n, p in layer.named_parameters()}
+        d.update(query=q.grad.detach().clone(), input_flatten=x.grad.detach().clone())
+        return d
+
+    clear()
+    want_out = run().detach().clone()
+    want = grads()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            clear()
+            run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    clear()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        static_out = run()
+    q.grad.zero_()                      # replays must rewrite, not accumulate
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    got = grads()
+    tol = 1e-5 if dtype == torch.float32 else 1e-2
+    scale = lambda t: t.float().abs().max().item() + 1e-30
+    assert (static_out.float() - want_out.float()).abs().max().item() <= tol * scale(want_out)
+    for name, w in want.items():
+        assert (got[name].float() - w.float()).abs().max().item() <= tol * scale(w), name

@@ -324,9 +324,9 @@ def run_layer(args, wl):
         "roofline": None, "clocks": clocks, "e2e": None,
         # the library's kernels per step: fused forward; grad_value (or fp32 workspace)
         # zero-fill + fused backward (+ the bf16 finalize); four projections forward
-        # and four input gradients, one launch each in bf16 and three (two splits and
-        # the GEMM) in fp32
-        "gpu_launches": (3 + 8 * 3 if wl.dtype == "f32" else 4 + 8) * args.steps,
+        # and four input gradients, one launch each in bf16 and two (the split of w
+        # and the GEMM) in fp32
+        "gpu_launches": (3 + 8 * 2 if wl.dtype == "f32" else 4 + 8) * args.steps,
     }
     print(json.dumps(line), flush=True)
     if dist:

@@ -308,14 +308,15 @@ MSDA_API int msda_linear(const void* x, const void* w, const void* bias, void* y
  *   bias [out_features]               fp32 or NULL
  *   y    [rows, out_features]         fp32, overwritten
  *   workspace  device scratch of at least msda_linear_workspace_bytes(rows,
- *              in_features, out_features, MSDA_F32) bytes, 16-byte aligned,
- *              owned by the caller; overwritten (the four split operands)
- * in_features must be a multiple of 32 and out_features a multiple of 16,
- * both at most MSDA_LINEAR_MAX_FEATURES (else MSDA_ERR_UNSUPPORTED); every
+ *              in_features, out_features, MSDA_F32) bytes (the two parts of
+ *              w, 8 * out_features * in_features), 16-byte aligned, owned by
+ *              the caller; overwritten
+ * in_features and out_features must be multiples of 16, both at most
+ * MSDA_LINEAR_MAX_FEATURES (else MSDA_ERR_UNSUPPORTED); every
  * pointer 16-byte aligned (MSDA_ERR_ALIGN); a short or NULL workspace gives
- * MSDA_ERR_WORKSPACE.  Three launches on `stream`: the splits of x and of w,
- * then the GEMM (persistent CTAs, TMA loads and stores, two accumulators in
- * tensor memory).  A device-side wait that runs out of its iteration limit
+ * MSDA_ERR_WORKSPACE.  Two launches on `stream`: the split of w, then the
+ * GEMM (persistent CTAs, TMA loads and stores, x split in shared memory, two
+ * accumulators in tensor memory).  A device-side wait that runs out of its iteration limit
  * stops the kernel and raises the error word msda_last_device_error() reads.
  */
 MSDA_API size_t msda_linear_workspace_bytes(int rows, int in_features, int out_features,

@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -357,16 +358,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------- fp32 (3 x TF32)
 // fp32 projections keep fp32 accuracy on the tensor cores by splitting each
-// operand into a TF32 head and the fp32 remainder, a = a_hi + a_lo with a_hi =
-// a rounded to TF32 (10 explicit mantissa bits) and a_lo = a - a_hi exact, and
-// summing three TF32 products, x_hi w_hi + x_hi w_lo + x_lo w_hi, in the fp32
-// accumulator (the dropped x_lo w_lo and the TF32 reading of the remainders
-// are below 2^-20 of |x||w|).  A first kernel writes the four parts to the
-// caller's workspace; the GEMM streams them through a 2-stage TMA ring (both
-// parts of an x block and of a w block per stage) and issues the three
-// kind::tf32 MMAs per K step of 8; the epilogue writes fp32 with TMA stores.
-constexpr int kBKF = 32;                 // fp32 columns per 128-byte swizzle atom
-constexpr int kStagesF = 2;
+// operand into its TF32 rounding and the fp32 remainder, a = a_hi + a_lo with
+// a_hi = a rounded to nearest TF32 (10 explicit mantissa bits) and a_lo = a -
+// a_hi exact, and summing three TF32 products, x_hi w_hi + x_hi w_lo + x_lo
+// w_hi, in the fp32 accumulator (the dropped x_lo w_lo and the TF32 reading of
+// the remainders are below 2^-19 of |x||w|).
+//   * w is split once per call by a small kernel into the caller's workspace;
+//   * the work is cut into units of 128 rows x up to 256 output columns (a
+//     row tile and one column part);
+//   * warp 0 loads, per stage, one raw 128 x 16 fp32 block of x and the split
+//     16-column blocks of the unit's w rows (w_hi, w_lo) with TMA (64-byte
+//     swizzle; small stages keep four of them in flight, which the loads'
+//     latency needs); the parts of a row tile run on neighbouring CTAs at the
+//     same time, so later reads of the x block come from L2;
+//   * warps 10..13 split the x block in shared memory: x_hi over the raw
+//     block in place and x_lo into the stage's second buffer, at the same
+//     offsets (the split is elementwise, so the swizzled layout carries over);
+//   * warp 1 issues, per K step of 8, the three kind::tf32 MMAs into one of
+//     two fp32 accumulators in tensor memory;
+//   * warps 2..9 drain a finished accumulator as in the bf16 kernel, adding
+//     the bias and writing fp32 32 x 32 pieces with TMA stores.
+constexpr int kBKF = 16;                 // fp32 columns per stage: 64-byte rows, 64-byte swizzle
+constexpr int kStagesF = 4;
+constexpr int kPartF = 256;              // output columns per unit (the MMA's N, at most)
+constexpr uint32_t kRowF = kBKF * 4;     // bytes per operand row in a stage
+constexpr int kConvWarps = 4;            // warps 10..13: one 32-row quarter of the x block each
+constexpr int kThreadsF = 32 * (2 + kEpiWarps + kConvWarps);
 
 __global__ void split_tf32_kernel(const float4* __restrict__ a, float4* __restrict__ hi,
                                   float4* __restrict__ lo, size_t n4) {
@@ -386,6 +403,20 @@ __global__ void split_tf32_kernel(const float4* __restrict__ a, float4* __restri
     }
 }
 
+// Shared-memory matrix descriptor of a K-major operand stored as 64-byte rows
+// with the 64-byte swizzle (CU_TENSOR_MAP_SWIZZLE_64B): 8-row groups 512 bytes
+// apart, version 1, layout SWIZZLE_64B; the MMA's 8 TF32 columns (32 bytes)
+// never leave one 64-byte row.
+__device__ __forceinline__ uint64_t kmajor_sw64_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);          // start address (16-byte units)
+    d |= (uint64_t)1 << 16;                          // leading byte offset (unused): 16 B
+    d |= (uint64_t)(512 >> 4) << 32;                 // stride byte offset: 512 B
+    d |= (uint64_t)1 << 46;                          // descriptor version
+    d |= (uint64_t)4 << 61;                          // layout: 64-byte swizzle
+    return d;
+}
+
 // Instruction descriptor of kind::tf32 (TF32 A and B, fp32 D, both K-major), M = 128, N = n.
 __host__ __device__ constexpr uint32_t tf32_idesc(int n) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) |
@@ -403,21 +434,20 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a, uint64_t 
 struct SmemF {
     uint32_t stage_bytes, stages, stage_out, bias, bars, tmem_slot, total;
 };
-__host__ __device__ inline SmemF smem_layout_f(int n) {
+__host__ __device__ inline SmemF smem_layout_f() {
     SmemF s;
-    s.stage_bytes = 2u * kBM * 128 + 2u * (uint32_t)n * 128;   // x_hi, x_lo, w_hi, w_lo blocks
+    s.stage_bytes = 2u * kBM * kRowF + 2u * kPartF * kRowF;    // x (-> x_hi), x_lo, w_hi, w_lo
     s.stages = 0;
     s.stage_out = s.stages + kStagesF * s.stage_bytes;         // 32 x 32 fp32 per epilogue warp
     s.bias = s.stage_out + (uint32_t)kEpiWarps * kChunk * kChunk * 4;
     s.bars = s.bias + MSDA_LINEAR_MAX_FEATURES * 4;
-    s.tmem_slot = s.bars + (4 * kStagesF + 4) * 8;
+    s.tmem_slot = s.bars + (3 * kStagesF + 4) * 8;
     s.total = s.tmem_slot + 8;
     return s;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    linear_f32x3_kernel(const __grid_constant__ CUtensorMap xhi_map,
-                        const __grid_constant__ CUtensorMap xlo_map,
+__global__ void __launch_bounds__(kThreadsF, 1)
+    linear_f32x3_kernel(const __grid_constant__ CUtensorMap x_map,
                         const __grid_constant__ CUtensorMap whi_map,
                         const __grid_constant__ CUtensorMap wlo_map,
                         const __grid_constant__ CUtensorMap y_map, const float* __restrict__ bias,
@@ -425,32 +455,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemF L = smem_layout_f(n);
+    const SmemF L = smem_layout_f();
     const uint32_t s_stage = smem_u32(base + L.stages);
     auto xhi = [&](int s) { return s_stage + (uint32_t)s * L.stage_bytes; };
-    auto xlo = [&](int s) { return xhi(s) + (uint32_t)kBM * 128; };
-    auto whi = [&](int s) { return xhi(s) + 2u * kBM * 128; };
-    auto wlo = [&](int s) { return whi(s) + (uint32_t)n * 128; };
+    auto xlo = [&](int s) { return xhi(s) + (uint32_t)kBM * kRowF; };
+    auto whi = [&](int s) { return xhi(s) + 2u * kBM * kRowF; };
+    auto wlo = [&](int s) { return whi(s) + (uint32_t)kPartF * kRowF; };
     const uint32_t bars = smem_u32(base + L.bars);
-    auto x_full = [&](int s) { return bars + 8u * s; };
-    auto x_empty = [&](int s) { return bars + 8u * (kStagesF + s); };
-    auto acc_full = [&](int a) { return bars + 8u * (2 * kStagesF + a); };
-    auto acc_empty = [&](int a) { return bars + 8u * (2 * kStagesF + 2 + a); };
+    auto x_full = [&](int s) { return bars + 8u * s; };                   // TMA landed
+    auto x_split = [&](int s) { return bars + 8u * (kStagesF + s); };     // x split in place
+    auto x_empty = [&](int s) { return bars + 8u * (2 * kStagesF + s); }; // MMAs done with it
+    auto acc_full = [&](int a) { return bars + 8u * (3 * kStagesF + a); };
+    auto acc_empty = [&](int a) { return bars + 8u * (3 * kStagesF + 2 + a); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.tmem_slot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kblocks = k / kBKF;
-    const int tiles = (rows + kBM - 1) / kBM;
+    const int parts = (n + kPartF - 1) / kPartF;
+    const int units = (rows + kBM - 1) / kBM * parts;   // unit u: row tile u / parts, part u % parts
 
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
-                     "r"(2 * kAccCols)
+                     "r"(2 * kPartF)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStagesF; ++s) {
             mbar_init(x_full(s), 1);
+            mbar_init(x_split(s), kConvWarps);
             mbar_init(x_empty(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -466,48 +499,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---- producer: both parts of an x block and of a w block per stage
+        // ---- producer: the raw x block and both parts of the unit's w block per stage
+        //      (the w box is min(n, kPartF) rows; rows past n read as zero and count in full)
         if (lane == 0) {
-            const uint32_t bytes = 2u * kBM * 128 + 2u * (uint32_t)n * 128;
+            const uint32_t wrows = (uint32_t)min(n, kPartF);     // the w box's rows
+            const uint32_t bytes = (uint32_t)kBM * kRowF + 2u * wrows * kRowF;
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x)
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const int t = u / parts, part = u - t * parts;
                 for (int kb = 0; kb < kblocks && ok; ++kb, ++it) {
                     const int s = (int)(it % kStagesF);
-                    const uint32_t ph = (it / kStagesF) & 1u;
-                    ok = mbar_wait(x_empty(s), ph ^ 1u);
+                    ok = mbar_wait(x_empty(s), ((it / kStagesF) & 1u) ^ 1u);
                     if (!ok) break;
                     mbar_expect_tx(x_full(s), bytes);
-                    tma_load_2d(xhi(s), &xhi_map, kb * kBKF, t * kBM, x_full(s));
-                    tma_load_2d(xlo(s), &xlo_map, kb * kBKF, t * kBM, x_full(s));
-                    tma_load_2d(whi(s), &whi_map, kb * kBKF, 0, x_full(s));
-                    tma_load_2d(wlo(s), &wlo_map, kb * kBKF, 0, x_full(s));
+                    tma_load_2d(xhi(s), &x_map, kb * kBKF, t * kBM, x_full(s));
+                    tma_load_2d(whi(s), &whi_map, kb * kBKF, part * kPartF, x_full(s));
+                    tma_load_2d(wlo(s), &wlo_map, kb * kBKF, part * kPartF, x_full(s));
                 }
+            }
         }
     } else if (warp == 1) {
         // ---- MMA issuer: three TF32 products per K step of 8
         if (lane == 0) {
-            const uint32_t idesc = tf32_idesc(n);
             bool ok = true;
             uint32_t it = 0, acc_it = 0;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++acc_it) {
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++acc_it) {
+                const int part = u % parts;
+                const int cols = min(kPartF, n - part * kPartF);
+                const uint32_t idesc = tf32_idesc(cols);
                 const int a = (int)(acc_it & 1u);
                 ok = mbar_wait(acc_empty(a), ((acc_it >> 1) & 1u) ^ 1u);
                 if (!ok) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t d = tmem + (uint32_t)(a * kAccCols);
+                const uint32_t d = tmem + (uint32_t)(a * kPartF);
                 for (int kb = 0; kb < kblocks && ok; ++kb, ++it) {
                     const int s = (int)(it % kStagesF);
-                    ok = mbar_wait(x_full(s), (it / kStagesF) & 1u);
+                    const uint32_t ph = (it / kStagesF) & 1u;
+                    ok = mbar_wait(x_full(s), ph) && mbar_wait(x_split(s), ph);
                     if (!ok) break;
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
                     for (int ks = 0; ks < kBKF / 8; ++ks) {
                         const uint32_t koff = (uint32_t)ks * 32;   // 8 fp32 columns
-                        const uint64_t ah = kmajor_sw128_desc(xhi(s) + koff);
-                        const uint64_t al = kmajor_sw128_desc(xlo(s) + koff);
-                        const uint64_t bh = kmajor_sw128_desc(whi(s) + koff);
-                        const uint64_t bl = kmajor_sw128_desc(wlo(s) + koff);
+                        const uint64_t ah = kmajor_sw64_desc(xhi(s) + koff);
+                        const uint64_t al = kmajor_sw64_desc(xlo(s) + koff);
+                        const uint64_t bh = kmajor_sw64_desc(whi(s) + koff);
+                        const uint64_t bl = kmajor_sw64_desc(wlo(s) + koff);
                         umma_tf32(d, ah, bh, idesc, kb > 0 || ks > 0);
                         umma_tf32(d, ah, bl, idesc, true);
                         umma_tf32(d, al, bh, idesc, true);
@@ -517,8 +555,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) umma_commit(acc_full(a));
             }
         }
+    } else if (warp >= 2 + kEpiWarps) {
+        // ---- x split: converter warp c takes rows 32c .. 32c+31 of the block (2 KB),
+        //      four 16-byte chunks per lane, consecutive lanes on consecutive chunks
+        const int c = warp - 2 - kEpiWarps;
+        unsigned char* stage0 = base + L.stages;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x)
+            for (int kb = 0; kb < kblocks && ok; ++kb, ++it) {
+                const int s = (int)(it % kStagesF);
+                ok = mbar_wait(x_full(s), (it / kStagesF) & 1u);
+                if (!ok) break;
+                float4* hi = reinterpret_cast<float4*>(stage0 + (size_t)s * L.stage_bytes +
+                                                       (size_t)c * 32 * kRowF);
+                float4* lo = reinterpret_cast<float4*>(reinterpret_cast<unsigned char*>(hi) +
+                                                       kBM * kRowF);
+#pragma unroll
+                for (int i = 0; i < (int)(32 * kRowF / 16 / 32); ++i) {
+                    const int j = i * 32 + lane;
+                    const float4 v = hi[j];
+                    const float in[4] = {v.x, v.y, v.z, v.w};
+                    float h[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t r;
+                        asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(in[e]));
+                        h[e] = __uint_as_float(r);
+                    }
+                    hi[j] = make_float4(h[0], h[1], h[2], h[3]);
+                    lo[j] = make_float4(in[0] - h[0], in[1] - h[1], in[2] - h[2], in[3] - h[3]);
+                }
+                // the tensor cores read these buffers through the async proxy
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(x_split(s));
+            }
     } else {
-        // ---- epilogue: as in the bf16 kernel, fp32 pieces staged with the 128-byte swizzle
+        // ---- epilogue: warps 2..9 as in the bf16 kernel; fp32 pieces staged with the
+        //      128-byte swizzle (chunk j of row r at j ^ (r % 8)) that the store map reads
         const int quarter = warp & 3;
         const int ew = warp - 2;
         const int half = ew >> 2;
@@ -526,25 +601,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = ew * 32 + lane; c < MSDA_LINEAR_MAX_FEATURES; c += kEpiWarps * 32)
             s_bias[c] = bias != nullptr && c < n ? bias[c] : 0.f;
         asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-        const uint32_t stage_addr = smem_u32(base + L.stage_out) + (uint32_t)ew * kChunk * kChunk * 4;
-        unsigned char* stage_ptr = base + L.stage_out + (size_t)ew * kChunk * kChunk * 4;
+        const uint32_t stage_addr =
+            smem_u32(base + L.stage_out) + (uint32_t)ew * kChunk * kChunk * 4;
+        unsigned char* row = base + L.stage_out + (size_t)ew * kChunk * kChunk * 4 +
+                             (size_t)lane * 128;
         uint32_t acc_it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++acc_it) {
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++acc_it) {
+            const int t = u / parts, part = u - t * parts;
+            const int col0 = part * kPartF, cols = min(kPartF, n - col0);
             const int a = (int)(acc_it & 1u);
             ok = mbar_wait(acc_full(a), (acc_it >> 1) & 1u);
             if (!ok) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t taddr =
-                tmem + (uint32_t)(a * kAccCols) + ((uint32_t)(quarter * 32) << 16);
-            for (int c0 = half * kChunk; c0 < n; c0 += 2 * kChunk) {
+                tmem + (uint32_t)(a * kPartF) + ((uint32_t)(quarter * 32) << 16);
+            for (int c0 = half * kChunk; c0 < cols; c0 += 2 * kChunk) {
                 float v[32];
                 tmem_ld32(taddr + (uint32_t)c0, v);
-                const float4* bq = reinterpret_cast<const float4*>(s_bias + c0);
+                const float4* bq = reinterpret_cast<const float4*>(s_bias + col0 + c0);
+                // the staging buffer must have been read by this warp's previous store
                 if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                 __syncwarp();
-                // row `lane` of the piece: 16-byte chunk j at position j ^ (row % 8)
-                unsigned char* row = stage_ptr + (size_t)lane * 128;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const float4 bb = bq[j];
@@ -554,7 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) tma_store_2d(&y_map, c0, t * kBM + quarter * 32, stage_addr);
+                if (lane == 0)
+                    tma_store_2d(&y_map, col0 + c0, t * kBM + quarter * 32, stage_addr);
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
@@ -568,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(2 * kAccCols)
+                     "r"(2 * kPartF)
                      : "memory");
 }
 
@@ -592,10 +671,10 @@ EncodeTiled encode_tiled() {
 }
 
 // Row-major bf16 (or fp32) matrix [outer, inner] moved in boxes of [box_rows, box_cols]
-// (with the 128-byte swizzle when swizzle); elements past the matrix read as
+// (with the 128- or 64-byte swizzle, or none); elements past the matrix read as
 // zero and are not written.
 bool make_map(CUtensorMap* map, const void* ptr, int inner, int outer, int box_cols, int box_rows,
-              bool swizzle, bool fp32 = false) {
+              int swizzle_bytes, bool fp32 = false) {
     const EncodeTiled enc = encode_tiled();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
@@ -605,7 +684,9 @@ bool make_map(CUtensorMap* map, const void* ptr, int inner, int outer, int box_c
     return enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                const_cast<void*>(ptr), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+               : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                     : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
@@ -637,9 +718,9 @@ extern "C" int msda_linear(const void* x, const void* w, const void* bias, void*
         return MSDA_ERR_ALIGN;
     if ((int64_t)rows * in_features > 2147483647LL * 64) return MSDA_ERR_DIM;
     CUtensorMap xm, wm, ym;
-    if (!make_map(&xm, x, in_features, rows, kBK, kBM, true) ||
-        !make_map(&wm, w, in_features, out_features, kBK, out_features, true) ||
-        !make_map(&ym, y, out_features, rows, kChunk, kChunk, false))
+    if (!make_map(&xm, x, in_features, rows, kBK, kBM, 128) ||
+        !make_map(&wm, w, in_features, out_features, kBK, out_features, 128) ||
+        !make_map(&ym, y, out_features, rows, kChunk, kChunk, 0))
         return MSDA_ERR_CUDA;
     const Smem L = smem_layout(out_features, in_features);
     const size_t smem = (size_t)L.total + 1024;
@@ -659,8 +740,9 @@ extern "C" int msda_linear(const void* x, const void* w, const void* bias, void*
 
 extern "C" size_t msda_linear_workspace_bytes(int rows, int in_features, int out_features,
                                               int dtype) {
-    if (dtype != MSDA_F32 || rows < 0 || in_features < 0 || out_features < 0) return 0;
-    return ((size_t)rows + (size_t)out_features) * (size_t)in_features * 2 * sizeof(float);
+    (void)rows;
+    if (dtype != MSDA_F32 || in_features < 0 || out_features < 0) return 0;
+    return (size_t)out_features * (size_t)in_features * 2 * sizeof(float);   // w_hi, w_lo
 }
 
 extern "C" int msda_linear_f32(const float* x, const float* w, const float* bias, float* y,
@@ -680,38 +762,33 @@ extern "C" int msda_linear_f32(const float* x, const float* w, const float* bias
     const size_t need = msda_linear_workspace_bytes(rows, in_features, out_features, MSDA_F32);
     if (workspace == nullptr || workspace_bytes < need) return MSDA_ERR_WORKSPACE;
     if (misaligned(workspace)) return MSDA_ERR_ALIGN;
-    if ((int64_t)rows * in_features > 2147483647LL * 64) return MSDA_ERR_DIM;
-    float* x_hi = static_cast<float*>(workspace);
-    float* x_lo = x_hi + (size_t)rows * in_features;
-    float* w_hi = x_lo + (size_t)rows * in_features;
+    float* w_hi = static_cast<float*>(workspace);
     float* w_lo = w_hi + (size_t)out_features * in_features;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int sms = sm_count();
-    const size_t nx4 = (size_t)rows * in_features / 4, nw4 = (size_t)out_features * in_features / 4;
-    split_tf32_kernel<<<sms * 4, 256, 0, st>>>(reinterpret_cast<const float4*>(x),
-                                                 reinterpret_cast<float4*>(x_hi),
-                                                 reinterpret_cast<float4*>(x_lo), nx4);
-    split_tf32_kernel<<<sms, 256, 0, st>>>(reinterpret_cast<const float4*>(w),
-                                            reinterpret_cast<float4*>(w_hi),
-                                            reinterpret_cast<float4*>(w_lo), nw4);
+    const size_t nw4 = (size_t)out_features * in_features / 4;
+    split_tf32_kernel<<<(int)((nw4 + 255) / 256), 256, 0, st>>>(
+        reinterpret_cast<const float4*>(w), reinterpret_cast<float4*>(w_hi),
+        reinterpret_cast<float4*>(w_lo), nw4);
     if (cudaGetLastError() != cudaSuccess) return MSDA_ERR_CUDA;
-    CUtensorMap xh, xl, wh, wl, ym;
-    if (!make_map(&xh, x_hi, in_features, rows, kBKF, kBM, true, true) ||
-        !make_map(&xl, x_lo, in_features, rows, kBKF, kBM, true, true) ||
-        !make_map(&wh, w_hi, in_features, out_features, kBKF, out_features, true, true) ||
-        !make_map(&wl, w_lo, in_features, out_features, kBKF, out_features, true, true) ||
-        !make_map(&ym, y, out_features, rows, kChunk, kChunk, true, true))
+    CUtensorMap xm, wh, wl, ym;
+    if (!make_map(&xm, x, in_features, rows, kBKF, kBM, 64, true) ||
+        !make_map(&wh, w_hi, in_features, out_features, kBKF, std::min(out_features, kPartF), 64,
+                  true) ||
+        !make_map(&wl, w_lo, in_features, out_features, kBKF, std::min(out_features, kPartF), 64,
+                  true) ||
+        !make_map(&ym, y, out_features, rows, kChunk, kChunk, 128, true))
         return MSDA_ERR_CUDA;
-    const SmemF L = smem_layout_f(out_features);
+    const SmemF L = smem_layout_f();
     static std::once_flag attr_once;
     std::call_once(attr_once, [] {
         cudaFuncSetAttribute(linear_f32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(smem_layout_f(MSDA_LINEAR_MAX_FEATURES).total + 1024));
+                             (int)(smem_layout_f().total + 1024));
     });
-    const int tiles = (rows + kBM - 1) / kBM;
-    const int grid = tiles < sms ? tiles : sms;
-    linear_f32x3_kernel<<<grid, kThreads, (size_t)L.total + 1024, st>>>(xh, xl, wh, wl, ym, bias,
-                                                                         rows, out_features,
-                                                                         in_features);
+    const int units = (rows + kBM - 1) / kBM * ((out_features + kPartF - 1) / kPartF);
+    const int sms = sm_count();
+    const int grid = units < sms ? units : sms;
+    linear_f32x3_kernel<<<grid, kThreadsF, (size_t)L.total + 1024, st>>>(xm, wh, wl, ym, bias,
+                                                                          rows, out_features,
+                                                                          in_features);
     return cudaGetLastError() == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA;
 }

@@ -36,7 +36,7 @@ _TC_DTYPES = (torch.bfloat16, torch.float32)
 
 
 def _tensor_core_shape(in_features: int, out_features: int, dtype=torch.bfloat16) -> bool:
-    k_step = 64 if dtype == torch.bfloat16 else 32        # one 128-byte swizzle atom of K
+    k_step = 64 if dtype == torch.bfloat16 else 16        # the kernels' K block
     return (in_features % k_step == 0 and out_features % 16 == 0 and
             in_features <= B.MSDA_LINEAR_MAX_FEATURES and
             out_features <= B.MSDA_LINEAR_MAX_FEATURES)

@@ -118,7 +118,8 @@ def _check_f32(B, rows, k, n, bias=True, seed=0):
     (300, 256, 256),          # a ragged last tile
     (1, 32, 16),              # smallest shapes
     (1000, 256, 128),         # attention-weight projection width
-    (517, 96, 80),            # K of three fp32 swizzle atoms, N not a power of two
+    (517, 96, 80),            # K of six 16-column stages, N not a power of two
+    (300, 48, 144),           # K of three stages, N past one 128-column half
     (44446, 256, 256),        # encoder tokens x d_model: many tiles per CTA
 ])
 def test_linear_f32_matches_fp64(B, rows, k, n):
@@ -152,5 +153,5 @@ def test_linear_f32_without_bias_batched_and_checks(B):
         B.msda_linear_f32(x, w, workspace=ws[:-16])           # workspace one chunk short
     assert e.value.status == 5
     with pytest.raises(B.MsdaError) as e:
-        B.msda_linear_f32(torch.zeros(8, 48, device="cuda"), torch.zeros(16, 48, device="cuda"))
-    assert e.value.status == 3                                 # in_features not a multiple of 32
+        B.msda_linear_f32(torch.zeros(8, 40, device="cuda"), torch.zeros(16, 40, device="cuda"))
+    assert e.value.status == 3                                 # in_features not a multiple of 16

@@ -303,8 +303,8 @@ def run_layer(args, wl):
                               "gradients; weight gradients with torch, cuBLAS bf16)"
                               if wl.dtype == "bf16" else
                               "(msda_linear_f32, three TF32 products on the tensor cores, "
-                              "forward and for the input gradients; weight gradients with "
-                              "torch, cuBLAS fp32)")
+                              "forward and for the input gradients; weight and bias "
+                              "gradients with msda_linear_wgrad_f32)")
                            + " around msda_forward_fused / msda_backward_fused, autograd")
     cfg["launch"] = ("eager through autograd (Python and autograd inside the events)"
                      if not use_graph else
@@ -325,8 +325,9 @@ def run_layer(args, wl):
         # the library's kernels per step: fused forward; grad_value (or fp32 workspace)
         # zero-fill + fused backward (+ the bf16 finalize); four projections forward
         # and four input gradients, one launch each in bf16 and two (the split of w
-        # and the GEMM) in fp32
-        "gpu_launches": (3 + 8 * 2 if wl.dtype == "f32" else 4 + 8) * args.steps,
+        # and the GEMM) in fp32; in fp32 also four weight gradients (two zero-fills
+        # and the kernel each)
+        "gpu_launches": (3 + 8 * 2 + 4 * 3 if wl.dtype == "f32" else 4 + 8) * args.steps,
     }
     print(json.dumps(line), flush=True)
     if dist:
@@ -337,7 +338,8 @@ def run_layer(args, wl):
 def _projection_gemm(linear, rows, dev, flush, reps=20):
     """One d_model x d_model projection of `rows` tokens in the layer's dtype:
     msda_linear / msda_linear_f32 (tcgen05) against torch's F.linear (cuBLAS),
-    CUDA events, L2 flushed before each call."""
+    and in fp32 the parameter gradients (msda_linear_wgrad_f32 against torch);
+    CUDA events around graph replays, L2 flushed before each call."""
     import torch
     import torch.nn.functional as F
     from scale_deformable_attention_05_b300 import binding as B
@@ -351,9 +353,16 @@ def _projection_gemm(linear, rows, dev, flush, reps=20):
                      dtype=torch.uint8, device=dev)
 
     def timed(fn):
-        # every rep enqueued before the one synchronisation, so that the host's
-        # marshalling runs ahead of the device and stays outside the events
-        for _ in range(3):
+        # each call captured as a CUDA graph and replayed, so that the host's
+        # marshalling (15-20 us a call, more on a loaded host) stays outside the events
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
             fn()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(reps)]
@@ -361,7 +370,7 @@ def _projection_gemm(linear, rows, dev, flush, reps=20):
         for e0, e1 in evs:
             flush.zero_()
             e0.record()
-            fn()
+            graph.replay()
             e1.record()
         torch.cuda.synchronize()
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
@@ -373,10 +382,20 @@ def _projection_gemm(linear, rows, dev, flush, reps=20):
     cb = timed(lambda: F.linear(xg, w, b))
     flops = 2.0 * rows * linear.in_features * linear.out_features
     nbytes = float(xg.element_size()) * rows * (linear.in_features + linear.out_features)
-    return {"rows": rows, "in_features": linear.in_features,
-            "out_features": linear.out_features,
-            "tcgen05_us": tc * 1e3, "cublas_us": cb * 1e3,
-            "tcgen05_tflops": flops / tc / 1e9, "tcgen05_gbs": nbytes / tc / 1e6}
+    res = {"rows": rows, "in_features": linear.in_features,
+           "out_features": linear.out_features,
+           "tcgen05_us": tc * 1e3, "cublas_us": cb * 1e3,
+           "tcgen05_tflops": flops / tc / 1e9, "tcgen05_gbs": nbytes / tc / 1e6}
+    if dt == torch.float32:
+        # the parameter gradients of the same projection: msda_linear_wgrad_f32
+        # against torch's grad_y^T x and column sum (cuBLAS fp32 and a reduction)
+        gy = torch.randn(rows, linear.out_features, generator=g, device=dev)
+        gw = torch.empty_like(w)
+        gb = torch.empty_like(b)
+        wg = timed(lambda: B.msda_linear_wgrad_f32(gy, xg, grad_w=gw, grad_b=gb))
+        wg_torch = timed(lambda: (gy.t() @ xg, gy.sum(0)))
+        res.update(wgrad_tcgen05_us=wg * 1e3, wgrad_torch_us=wg_torch * 1e3)
+    return res
 
 
 def touched_roofline(wl, inp, passes, hbm_gbs):

@@ -325,6 +325,29 @@ MSDA_API int msda_linear_f32(const float* x, const float* w, const float* bias, 
                              void* workspace, size_t workspace_bytes, int rows, int in_features,
                              int out_features, void* stream);
 
+/*
+ * Parameter gradients of that fp32 projection on the tensor cores, with the
+ * same three-TF32-product split:
+ *   grad_w[n, k] (+)= sum_r grad_y[r, n] x[r, k]      (grad_y^T x)
+ *   grad_b[n]    (+)= sum_r grad_y[r, n]              (skipped when grad_b is NULL)
+ *   grad_y [rows, out_features], x [rows, in_features]: fp32, row-major,
+ *          device pointers (the layer's output gradient and input)
+ *   grad_w [out_features, in_features], grad_b [out_features]: fp32, device
+ * flags: 0 overwrites grad_w and grad_b, MSDA_GRAD_VALUE_ACCUMULATE adds to
+ * them.  in_features and out_features must be multiples of 16, both at most
+ * MSDA_LINEAR_MAX_FEATURES (else MSDA_ERR_UNSUPPORTED); every pointer 16-byte
+ * aligned (MSDA_ERR_ALIGN).  Launches on `stream`: zero-fills unless
+ * accumulating, then one kernel of one CTA per SM, each summing a contiguous
+ * range of rows for 128 columns of grad_y in tensor memory and adding its
+ * partial sums with fp32 reductions (so the order of the additions, and the
+ * last bits of the result, vary between runs).  A device-side wait that runs
+ * out of its iteration limit stops the kernel and raises the error word
+ * msda_last_device_error() reads.
+ */
+MSDA_API int msda_linear_wgrad_f32(const float* grad_y, const float* x, float* grad_w,
+                                   float* grad_b, int rows, int in_features, int out_features,
+                                   unsigned flags, void* stream);
+
 /* MSDA_VERSION of the built library. */
 MSDA_API int msda_version(void);
 

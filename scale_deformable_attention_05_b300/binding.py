@@ -21,7 +21,7 @@ __all__ = [
     "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
     "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused", "msda_linear",
-    "msda_linear_f32", "msda_linear_workspace_bytes",
+    "msda_linear_f32", "msda_linear_workspace_bytes", "msda_linear_wgrad_f32",
     "MSDeformAttnFunction", "MSDeformAttnFusedFunction", "ms_deform_attn", "ms_deform_attn_fused",
     "EXPORTED_SYMBOLS", "load_library",
 ]
@@ -40,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "msda_forward", "msda_backward", "msda_backward_workspace_bytes", "msda_zero_fill",
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
     "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused", "msda_linear",
-    "msda_linear_f32", "msda_linear_workspace_bytes",
+    "msda_linear_f32", "msda_linear_workspace_bytes", "msda_linear_wgrad_f32",
 )
 
 _vp = ctypes.c_void_p
@@ -84,6 +84,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msda_linear_workspace_bytes.restype = ctypes.c_size_t
     lib.msda_linear_f32.argtypes = [_vp] * 5 + [ctypes.c_size_t] + [_int] * 3 + [_vp]
     lib.msda_linear_f32.restype = _int
+    lib.msda_linear_wgrad_f32.argtypes = [_vp] * 4 + [_int] * 3 + [ctypes.c_uint, _vp]
+    lib.msda_linear_wgrad_f32.restype = _int
     lib.msda_forward_fused.argtypes = [_vp] * 8 + _DIMS + [_int, _int, _vp]
     lib.msda_forward_fused.restype = _int
     lib.msda_backward_fused.argtypes = ([_vp] * 13 + [ctypes.c_size_t] + _DIMS +
@@ -328,6 +330,46 @@ def msda_linear_f32(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.
         _ptr(x2), _ptr(weight), _ptr(bias) if bias is not None else None, _ptr(out),
         _ptr(workspace), ws_bytes, rows, n_in, n_out, _stream(stream)))
     return out
+
+
+def msda_linear_wgrad_f32(grad_y: torch.Tensor, x: torch.Tensor, bias: bool = True,
+                          grad_w: Optional[torch.Tensor] = None,
+                          grad_b: Optional[torch.Tensor] = None, accumulate: bool = False,
+                          stream=None):
+    """(grad_w, grad_b) of y = x @ w.T + b in fp32 on the tensor cores (see
+    msda_linear_wgrad_f32 in include/msda.h): grad_y [..., out] and x [..., in]
+    fp32 CUDA tensors; grad_w = grad_y^T x [out, in], grad_b = sum of grad_y
+    [out] (None unless `bias`).  With `accumulate` the sums are added to the
+    given grad_w / grad_b."""
+    if grad_y.dtype != torch.float32 or x.dtype != torch.float32:
+        raise TypeError("msda_linear_wgrad_f32 takes fp32 grad_y and x")
+    if not (grad_y.is_cuda and x.is_cuda) or grad_y.device != x.device:
+        raise ValueError("grad_y and x must be CUDA tensors on one device")
+    g2 = grad_y.reshape(-1, grad_y.shape[-1])
+    x2 = x.reshape(-1, x.shape[-1])
+    if g2.shape[0] != x2.shape[0] or not (g2.is_contiguous() and x2.is_contiguous()):
+        raise ValueError("grad_y and x must be contiguous with the same leading dimensions")
+    rows, n_out, n_in = int(g2.shape[0]), int(g2.shape[1]), int(x2.shape[1])
+    dev = x.device
+    if grad_w is None:
+        if accumulate:
+            raise ValueError("accumulate needs grad_w")
+        grad_w = torch.empty(n_out, n_in, dtype=torch.float32, device=dev)
+    elif grad_w.shape != (n_out, n_in) or grad_w.dtype != torch.float32 or not grad_w.is_contiguous():
+        raise ValueError("grad_w must be a contiguous fp32 [out_features, in_features] tensor")
+    if bias:
+        if grad_b is None:
+            if accumulate:
+                raise ValueError("accumulate needs grad_b")
+            grad_b = torch.empty(n_out, dtype=torch.float32, device=dev)
+        elif grad_b.shape != (n_out,) or grad_b.dtype != torch.float32:
+            raise ValueError("grad_b must be an fp32 [out_features] tensor")
+    else:
+        grad_b = None
+    _check("msda_linear_wgrad_f32", _LIB.msda_linear_wgrad_f32(
+        _ptr(g2), _ptr(x2), _ptr(grad_w), _ptr(grad_b) if grad_b is not None else None,
+        rows, n_in, n_out, MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0, _stream(stream)))
+    return grad_w, grad_b
 
 
 def _fused_dims(value, spatial_shapes, reference_points, sampling_offsets, attn_logits):

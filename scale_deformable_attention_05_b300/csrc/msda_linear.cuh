@@ -651,6 +651,238 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                      : "memory");
 }
 
+// ------------------------------------------------ fp32 weight gradient (3 x TF32)
+// The projections' parameter gradients, gw = gy^T x ([n, k], a sum over all
+// rows) and gb = sum over rows of gy ([n]), in fp32 on the tensor cores with the
+// same three-TF32-product split.  As an MMA, D[m, j] = sum_r A[m, r] B[j, r]
+// with A = gy^T and B = x^T, whose rows are strided in memory; the kernel
+// loads row-major blocks of gy and x and transposes them while it splits them:
+//   * each CTA owns one 128-column tile of gy (m0 = 128 * tile) and one
+//     contiguous range of rows, so its whole contribution accumulates in one
+//     [128, k] fp32 accumulator in tensor memory;
+//   * warp 0 loads 16-row blocks of gy (128 columns) and x (k columns) with
+//     TMA into a ring of raw stages;
+//   * warps 2..5 (thread t owns column m0 + t of gy and columns t, t + 128 of
+//     x) read 4 rows at a time, add gy's values to a running bias sum, split
+//     them into TF32 head and remainder, and write both as K-major rows of 16
+//     elements with the 64-byte swizzle (16-byte chunk c of row i at
+//     c ^ ((i >> 1) & 3) within its 512-byte group) into a ring of split stages;
+//   * warp 1 issues the three kind::tf32 MMAs per 8 rows;
+//   * at the end warps 2..5 read the accumulator and add it to gw with
+//     red.global.add.v4.f32, and their bias sums to gb with atomicAdd.
+// Rows past the matrices read as zero (TMA fill), so ragged ranges need no
+// special case.  gw and gb must hold zeros (or the sums to add to) on entry.
+constexpr int kWgRows = 16;              // rows (the MMA's K) per stage
+constexpr int kWgRaw = 3, kWgSplit = 3;  // raw and split ring depths
+constexpr int kWgConvWarps = 4;
+constexpr int kWgThreads = 32 * (2 + kWgConvWarps);
+
+struct SmemWg {
+    uint32_t raw_bytes, split_bytes, raw, split, bars, tmem_slot, total;
+};
+__host__ __device__ inline SmemWg smem_layout_wg() {
+    SmemWg s;
+    s.raw_bytes = kWgRows * (kBM + MSDA_LINEAR_MAX_FEATURES) * 4;          // gy block, x block
+    s.split_bytes = 2u * kBM * kWgRows * 4 + 2u * MSDA_LINEAR_MAX_FEATURES * kWgRows * 4;
+    s.split = 0;                                                         // A_hi, A_lo, B_hi, B_lo
+    s.raw = s.split + kWgSplit * s.split_bytes;
+    s.bars = s.raw + kWgRaw * s.raw_bytes;
+    s.tmem_slot = s.bars + (2 * kWgRaw + 2 * kWgSplit + 1) * 8;
+    s.total = s.tmem_slot + 8;
+    return s;
+}
+
+// Byte offset of element (row i, column r) of a K-major operand with 16-element
+// rows and the 64-byte swizzle, r a multiple of 4 (one 16-byte chunk).
+__device__ __forceinline__ uint32_t sw64_offset(int i, int r) {
+    return (uint32_t)(i >> 3) * 512u + (uint32_t)(i & 7) * 64u +
+           ((uint32_t)((r >> 2) ^ ((i >> 1) & 3)) << 4);
+}
+
+__device__ __forceinline__ void split4(const float (&v)[4], float4& hi, float4& lo) {
+    float h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        uint32_t r;
+        asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v[e]));
+        h[e] = __uint_as_float(r);
+    }
+    hi = make_float4(h[0], h[1], h[2], h[3]);
+    lo = make_float4(v[0] - h[0], v[1] - h[1], v[2] - h[2], v[3] - h[3]);
+}
+
+__global__ void __launch_bounds__(kWgThreads, 1)
+    linear_wgrad_f32_kernel(const __grid_constant__ CUtensorMap gy_map,
+                            const __grid_constant__ CUtensorMap x_map, float* __restrict__ gw,
+                            float* __restrict__ gb, int rows, int n, int k, int tiles_m,
+                            int rows_per_cta) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const SmemWg L = smem_layout_wg();
+    const uint32_t bars = smem_u32(base + L.bars);
+    auto raw_full = [&](int s) { return bars + 8u * s; };
+    auto raw_empty = [&](int s) { return bars + 8u * (kWgRaw + s); };
+    auto split_full = [&](int s) { return bars + 8u * (2 * kWgRaw + s); };
+    auto split_empty = [&](int s) { return bars + 8u * (2 * kWgRaw + kWgSplit + s); };
+    const uint32_t acc_full = bars + 8u * (2 * kWgRaw + 2 * kWgSplit);
+    auto raw_gy = [&](int s) { return base + L.raw + (size_t)s * L.raw_bytes; };
+    auto raw_x = [&](int s) { return raw_gy(s) + (size_t)kWgRows * kBM * 4; };
+    auto a_hi = [&](int s) { return base + L.split + (size_t)s * L.split_bytes; };
+    auto a_lo = [&](int s) { return a_hi(s) + (size_t)kBM * kWgRows * 4; };
+    auto b_hi = [&](int s) { return a_hi(s) + (size_t)2 * kBM * kWgRows * 4; };
+    auto b_lo = [&](int s) {
+        return b_hi(s) + (size_t)MSDA_LINEAR_MAX_FEATURES * kWgRows * 4;
+    };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.tmem_slot);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x % tiles_m;
+    const int m0 = tile * kBM;
+    const int r_begin = (blockIdx.x / tiles_m) * rows_per_cta;
+    const int r_end = min(rows, r_begin + rows_per_cta);
+    const int stages = r_end > r_begin ? (r_end - r_begin + kWgRows - 1) / kWgRows : 0;
+
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(MSDA_LINEAR_MAX_FEATURES)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWgRaw; ++s) {
+            mbar_init(raw_full(s), 1);
+            mbar_init(raw_empty(s), kWgConvWarps);
+        }
+        for (int s = 0; s < kWgSplit; ++s) {
+            mbar_init(split_full(s), kWgConvWarps);
+            mbar_init(split_empty(s), 1);
+        }
+        mbar_init(acc_full, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---- producer: 16-row blocks of gy (columns m0 .. m0+127) and of x
+        if (lane == 0) {
+            const uint32_t bytes = (uint32_t)kWgRows * (kBM + k) * 4;
+            bool ok = true;
+            for (int it = 0; it < stages && ok; ++it) {
+                const int s = it % kWgRaw;
+                ok = mbar_wait(raw_empty(s), ((it / kWgRaw) & 1) ^ 1);
+                if (!ok) break;
+                mbar_expect_tx(raw_full(s), bytes);
+                const int r0 = r_begin + it * kWgRows;
+                tma_load_2d(smem_u32(raw_gy(s)), &gy_map, m0, r0, raw_full(s));
+                tma_load_2d(smem_u32(raw_x(s)), &x_map, 0, r0, raw_full(s));
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer: D[m, j] += three TF32 products over 8 rows at a time
+        if (lane == 0 && stages > 0) {
+            const uint32_t idesc = tf32_idesc(k);
+            bool ok = true;
+            for (int it = 0; it < stages && ok; ++it) {
+                const int s = it % kWgSplit;
+                ok = mbar_wait(split_full(s), (it / kWgSplit) & 1);
+                if (!ok) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+                for (int ks = 0; ks < kWgRows / 8; ++ks) {
+                    const uint32_t koff = (uint32_t)ks * 32;   // 8 rows (fp32) per MMA
+                    const uint64_t ah = kmajor_sw64_desc(smem_u32(a_hi(s)) + koff);
+                    const uint64_t al = kmajor_sw64_desc(smem_u32(a_lo(s)) + koff);
+                    const uint64_t bh = kmajor_sw64_desc(smem_u32(b_hi(s)) + koff);
+                    const uint64_t bl = kmajor_sw64_desc(smem_u32(b_lo(s)) + koff);
+                    umma_tf32(tmem, ah, bh, idesc, it > 0 || ks > 0);
+                    umma_tf32(tmem, ah, bl, idesc, true);
+                    umma_tf32(tmem, al, bh, idesc, true);
+                }
+                umma_commit(split_empty(s));
+            }
+            if (ok) umma_commit(acc_full);
+        }
+    } else {
+        // ---- converters (warps 2..5), then the epilogue
+        const int t = (warp - 2) * 32 + lane;          // gy column m0 + t; x columns t, t + 128
+        float bias_sum = 0.f;
+        bool ok = true;
+        for (int it = 0; it < stages && ok; ++it) {
+            const int sr = it % kWgRaw, ss = it % kWgSplit;
+            ok = mbar_wait(raw_full(sr), (it / kWgRaw) & 1) &&
+                 mbar_wait(split_empty(ss), ((it / kWgSplit) & 1) ^ 1);
+            if (!ok) break;
+            const float* gys = reinterpret_cast<const float*>(raw_gy(sr));
+            const float* xs = reinterpret_cast<const float*>(raw_x(sr));
+#pragma unroll
+            for (int q = 0; q < kWgRows / 4; ++q) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = gys[(4 * q + e) * kBM + t];
+                bias_sum += (v[0] + v[1]) + (v[2] + v[3]);
+                float4 hi, lo;
+                split4(v, hi, lo);
+                const uint32_t off = sw64_offset(t, 4 * q);
+                *reinterpret_cast<float4*>(a_hi(ss) + off) = hi;
+                *reinterpret_cast<float4*>(a_lo(ss) + off) = lo;
+#pragma unroll
+                for (int hcol = 0; hcol < 2; ++hcol) {
+                    const int j = t + hcol * kBM;
+                    if (j < k) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) v[e] = xs[(4 * q + e) * k + j];
+                        split4(v, hi, lo);
+                        const uint32_t offb = sw64_offset(j, 4 * q);
+                        *reinterpret_cast<float4*>(b_hi(ss) + offb) = hi;
+                        *reinterpret_cast<float4*>(b_lo(ss) + offb) = lo;
+                    }
+                }
+            }
+            // the tensor cores read the split stage through the async proxy
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(split_full(ss));
+                mbar_arrive(raw_empty(sr));
+            }
+        }
+        if (ok && stages > 0) {
+            if (gb != nullptr && m0 + t < n) atomicAdd(gb + m0 + t, bias_sum);
+            ok = mbar_wait(acc_full, 0);
+            if (ok) {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const int quarter = warp & 3;   // the tensor-memory lanes this warp may read
+                const int m = m0 + quarter * 32 + lane;
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+                for (int c0 = 0; c0 < k; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + (uint32_t)c0, v);
+                    if (m < n) {
+                        float* dst = gw + (size_t)m * k + c0;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (c0 + 4 * j < k)
+                                msda::red_add_v4(dst + 4 * j, v[4 * j], v[4 * j + 1],
+                                                 v[4 * j + 2], v[4 * j + 3]);
+                    }
+                }
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(MSDA_LINEAR_MAX_FEATURES)
+                     : "memory");
+}
+
 // ------------------------------------------------------------------- host
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -790,5 +1022,52 @@ extern "C" int msda_linear_f32(const float* x, const float* w, const float* bias
     linear_f32x3_kernel<<<grid, kThreadsF, (size_t)L.total + 1024, st>>>(xm, wh, wl, ym, bias,
                                                                           rows, out_features,
                                                                           in_features);
+    return cudaGetLastError() == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA;
+}
+
+extern "C" int msda_linear_wgrad_f32(const float* grad_y, const float* x, float* grad_w,
+                                     float* grad_b, int rows, int in_features, int out_features,
+                                     unsigned flags, void* stream) {
+    using namespace msda::linear;
+    if (rows < 0 || in_features < 0 || out_features < 0) return MSDA_ERR_DIM;
+    if (flags & ~MSDA_GRAD_VALUE_ACCUMULATE) return MSDA_ERR_UNSUPPORTED;
+    if (in_features % 16 != 0 || in_features < 16 || in_features > MSDA_LINEAR_MAX_FEATURES ||
+        out_features % 16 != 0 || out_features < 16 ||
+        out_features > MSDA_LINEAR_MAX_FEATURES)
+        return MSDA_ERR_UNSUPPORTED;
+    if (grad_w == nullptr) return MSDA_ERR_NULL;
+    const auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (misaligned(grad_w) || (grad_b && misaligned(grad_b))) return MSDA_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!(flags & MSDA_GRAD_VALUE_ACCUMULATE)) {
+        if (msda::launch_zero_fill(grad_w, (size_t)out_features * in_features * 4, st) !=
+                cudaSuccess ||
+            (grad_b && msda::launch_zero_fill(grad_b, (size_t)out_features * 4, st) != cudaSuccess))
+            return MSDA_ERR_CUDA;
+    }
+    if (rows == 0) return MSDA_OK;
+    if (grad_y == nullptr || x == nullptr) return MSDA_ERR_NULL;
+    if (misaligned(grad_y) || misaligned(x)) return MSDA_ERR_ALIGN;
+    CUtensorMap gym, xm;
+    if (!make_map(&gym, grad_y, out_features, rows, kBM, kWgRows, 0, true) ||
+        !make_map(&xm, x, in_features, rows, in_features, kWgRows, 0, true))
+        return MSDA_ERR_CUDA;
+    static std::once_flag attr_once;
+    std::call_once(attr_once, [] {
+        cudaFuncSetAttribute(linear_wgrad_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(smem_layout_wg().total + 1024));
+    });
+    // one CTA per SM: tiles_m column tiles of gy, each with sms / tiles_m row ranges
+    const int tiles_m = (out_features + kBM - 1) / kBM;
+    const int sms = sm_count();
+    const int blocks16 = (rows + kWgRows - 1) / kWgRows;
+    int ranges = sms / tiles_m;
+    if (ranges < 1) ranges = 1;
+    if (ranges > blocks16) ranges = blocks16;
+    const int rows_per_cta = (blocks16 + ranges - 1) / ranges * kWgRows;
+    ranges = (rows + rows_per_cta - 1) / rows_per_cta;
+    linear_wgrad_f32_kernel<<<ranges * tiles_m, kWgThreads, (size_t)smem_layout_wg().total + 1024,
+                              st>>>(gym, xm, grad_w, grad_b, rows, out_features, in_features,
+                                    tiles_m, rows_per_cta);
     return cudaGetLastError() == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA;
 }

@@ -14,8 +14,9 @@ The four projections are dense GEMMs.  They run on the library's tensor-core
 kernels (tcgen05.mma with the accumulator in tensor memory) for the forward and
 for the input gradient (x-gradient = grad_y times the weight, i.e. the same
 kernel with the transposed weight): ``msda_linear`` in bf16, ``msda_linear_f32``
-(three TF32 products per step, fp32 accuracy) in fp32.  The weight gradient (a
-reduction over all tokens) uses torch (cuBLAS).  Everything between the projections -- masking,
+(three TF32 products per step, fp32 accuracy) in fp32.  The weight and bias
+gradients (reductions over all tokens) use ``msda_linear_wgrad_f32`` in fp32
+and torch (cuBLAS) in bf16.  Everything between the projections -- masking,
 softmax, locations from 2-d or 4-d reference points, bilinear sampling and
 their backward -- is one launch of the fused entry points of ``libmsda.so``
 each way.  The tensors the GEMMs produce are already in the operator's
@@ -51,8 +52,9 @@ def _tc_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tenso
 class TensorCoreLinear(torch.autograd.Function):
     """y = x w^T + b with x and w both bf16 or both fp32 on the tensor cores
     (msda_linear / msda_linear_f32); the input gradient through the same kernel
-    with w^T when its shape allows (else a cuBLAS matmul), the weight and bias
-    gradients with torch."""
+    with w^T when its shape allows (else a cuBLAS matmul); the weight and bias
+    gradients on the tensor cores in fp32 (msda_linear_wgrad_f32), with torch
+    (cuBLAS) in bf16."""
 
     @staticmethod
     def forward(ctx, x, weight, bias):
@@ -70,6 +72,10 @@ class TensorCoreLinear(torch.autograd.Function):
         else:
             gx = gy @ weight
         g2 = gy.reshape(-1, n_out)
+        if weight.dtype == torch.float32:
+            gw, gb = B.msda_linear_wgrad_f32(g2, x.reshape(-1, n_in).contiguous(),
+                                             bias=ctx.has_bias)
+            return gx, gw, gb
         gw = g2.t() @ x.reshape(-1, n_in)
         gb = torch.sum(g2, 0, dtype=torch.float32).to(weight.dtype) if ctx.has_bias else None
         return gx, gw, gb

@@ -155,3 +155,70 @@ def test_linear_f32_without_bias_batched_and_checks(B):
     with pytest.raises(B.MsdaError) as e:
         B.msda_linear_f32(torch.zeros(8, 40, device="cuda"), torch.zeros(16, 40, device="cuda"))
     assert e.value.status == 3                                 # in_features not a multiple of 16
+
+
+# ------------------------------------------------------ fp32 weight gradient (3 x TF32)
+# msda_linear_wgrad_f32 against grad_w = gy^T x and grad_b = sum gy in fp64.  The
+# split contributes <= 2^-19.4 |gy||x| per term, as above; the partial sums of up
+# to 148 CTAs (each over a contiguous range of rows) are added with fp32
+# reductions, each rounding by <= 2^-24 of the running sum: allowed 2^-16 of
+# S = |gy|^T |x| for grad_w, and 2^-16 of sum |gy| for grad_b (a thread's
+# sequential sum over its rows, then the same reductions).
+
+def _check_wgrad(B, rows, k, n, seed, accumulate=False):
+    g = torch.Generator().manual_seed(seed)
+    gy = torch.randn(rows, n, generator=g)
+    x = torch.randn(rows, k, generator=g)
+    w0 = torch.randn(n, k, generator=g) if accumulate else None
+    b0 = torch.randn(n, generator=g) if accumulate else None
+    if accumulate:
+        gw, gb = B.msda_linear_wgrad_f32(gy.cuda(), x.cuda(), grad_w=w0.cuda(), grad_b=b0.cuda(),
+                                         accumulate=True)
+    else:
+        gw, gb = B.msda_linear_wgrad_f32(gy.cuda(), x.cuda())
+    torch.cuda.synchronize()
+    assert B.msda_last_device_error() == 0
+    gyd, xd = gy.double().numpy(), x.double().numpy()
+    ref_w = gyd.T @ xd + (w0.double().numpy() if accumulate else 0.0)
+    ref_b = gyd.sum(0) + (b0.double().numpy() if accumulate else 0.0)
+    s = np.abs(gyd).T @ np.abs(xd) + (np.abs(w0.double().numpy()) if accumulate else 0.0)
+    sb = np.abs(gyd).sum(0) + (np.abs(b0.double().numpy()) if accumulate else 0.0)
+    err_w = np.abs(gw.cpu().double().numpy() - ref_w)
+    err_b = np.abs(gb.cpu().double().numpy() - ref_b)
+    assert (err_w <= 2.0 ** -16 * s).all(), f"grad_w max err {err_w.max():.3e}"
+    assert (err_b <= 2.0 ** -16 * sb).all(), f"grad_b max err {err_b.max():.3e}"
+    return err_w, s
+
+
+@pytest.mark.parametrize("rows,k,n", [
+    (16, 16, 16),             # one block of rows, smallest widths
+    (300, 256, 256),          # two column tiles of grad_y, ragged last block
+    (1000, 256, 128),         # one column tile (attention-weight projection width)
+    (517, 96, 80),            # widths that are not powers of two
+    (44446, 256, 256),        # encoder tokens: every CTA sums ~600 rows
+])
+def test_linear_wgrad_f32_matches_fp64(B, rows, k, n):
+    _check_wgrad(B, rows, k, n, seed=rows + 3 * k + n)
+
+
+def test_linear_wgrad_f32_accumulates_and_beats_one_tf32_product(B):
+    _check_wgrad(B, 777, 128, 144, seed=21, accumulate=True)
+    err, s = _check_wgrad(B, 64, 256, 256, seed=22)
+    g = torch.Generator().manual_seed(22)
+    gy, x = torch.randn(64, 256, generator=g), torch.randn(64, 256, generator=g)
+    tf32 = lambda a: (a.view(torch.int32) + 0x1000 & ~0x1FFF).view(torch.float32)
+    err1 = (tf32(gy).double().T @ tf32(x).double() - gy.double().T @ x.double()).abs().numpy()
+    assert err.max() * 16 < err1.max()
+
+
+def test_linear_wgrad_f32_without_bias_and_checks(B):
+    gy = torch.randn(40, 32, device="cuda")
+    x = torch.randn(40, 48, device="cuda")
+    gw, gb = B.msda_linear_wgrad_f32(gy, x, bias=False)
+    torch.cuda.synchronize()
+    assert gb is None
+    ref = gy.double().T @ x.double()
+    assert (gw.double() - ref).abs().max().item() <= 2.0 ** -16 * (gy.abs().double().T @ x.abs().double()).max().item()
+    with pytest.raises(B.MsdaError) as e:
+        B.msda_linear_wgrad_f32(torch.zeros(8, 24, device="cuda"), torch.zeros(8, 32, device="cuda"))
+    assert e.value.status == 3                                 # out_features not a multiple of 16

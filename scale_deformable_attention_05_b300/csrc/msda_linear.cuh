@@ -662,19 +662,21 @@ __global__ void __launch_bounds__(kThreadsF, 1)
 //     [128, k] fp32 accumulator in tensor memory;
 //   * warp 0 loads 16-row blocks of gy (128 columns) and x (k columns) with
 //     TMA into a ring of raw stages;
-//   * warps 2..5 (thread t owns column m0 + t of gy and columns t, t + 128 of
-//     x) read 4 rows at a time, add gy's values to a running bias sum, split
-//     them into TF32 head and remainder, and write both as K-major rows of 16
-//     elements with the 64-byte swizzle (16-byte chunk c of row i at
-//     c ^ ((i >> 1) & 3) within its 512-byte group) into a ring of split stages;
+//   * warps 2..9 (thread t owns column t of x, and column m0 + t % 128 of gy
+//     for rows 8 * (t / 128) .. + 7 of each block) read 4 rows at a time, add
+//     gy's values to a running bias sum, split them into TF32 head and
+//     remainder, and write both as K-major rows of 16 elements with the
+//     64-byte swizzle (16-byte chunk c of row i at c ^ ((i >> 1) & 3) within
+//     its 512-byte group) into a ring of split stages;
 //   * warp 1 issues the three kind::tf32 MMAs per 8 rows;
-//   * at the end warps 2..5 read the accumulator and add it to gw with
-//     red.global.add.v4.f32, and their bias sums to gb with atomicAdd.
+//   * at the end warps 2..9 read the accumulator (two warps per lane quarter,
+//     alternate 32-column pieces) and add it to gw with red.global.add.v4.f32,
+//     and their bias sums to gb with atomicAdd.
 // Rows past the matrices read as zero (TMA fill), so ragged ranges need no
 // special case.  gw and gb must hold zeros (or the sums to add to) on entry.
 constexpr int kWgRows = 16;              // rows (the MMA's K) per stage
-constexpr int kWgRaw = 3, kWgSplit = 3;  // raw and split ring depths
-constexpr int kWgConvWarps = 4;
+constexpr int kWgRaw = 5, kWgSplit = 2;  // raw ring deep enough to cover HBM latency
+constexpr int kWgConvWarps = 8;
 constexpr int kWgThreads = 32 * (2 + kWgConvWarps);
 
 struct SmemWg {
@@ -808,8 +810,9 @@ __global__ void __launch_bounds__(kWgThreads, 1)
             if (ok) umma_commit(acc_full);
         }
     } else {
-        // ---- converters (warps 2..5), then the epilogue
-        const int t = (warp - 2) * 32 + lane;          // gy column m0 + t; x columns t, t + 128
+        // ---- converters (warps 2..9), then the epilogue
+        const int t = (warp - 2) * 32 + lane;          // x column t; gy column m0 + (t & 127)
+        const int tg = t & (kBM - 1), q0 = (t >> 7) * 2;   // gy rows 4*q0 .. 4*q0 + 7
         float bias_sum = 0.f;
         bool ok = true;
         for (int it = 0; it < stages && ok; ++it) {
@@ -819,28 +822,28 @@ __global__ void __launch_bounds__(kWgThreads, 1)
             if (!ok) break;
             const float* gys = reinterpret_cast<const float*>(raw_gy(sr));
             const float* xs = reinterpret_cast<const float*>(raw_x(sr));
+            float v[4];
+            float4 hi, lo;
 #pragma unroll
-            for (int q = 0; q < kWgRows / 4; ++q) {
-                float v[4];
+            for (int qq = 0; qq < 2; ++qq) {
+                const int q = q0 + qq;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] = gys[(4 * q + e) * kBM + t];
+                for (int e = 0; e < 4; ++e) v[e] = gys[(4 * q + e) * kBM + tg];
                 bias_sum += (v[0] + v[1]) + (v[2] + v[3]);
-                float4 hi, lo;
                 split4(v, hi, lo);
-                const uint32_t off = sw64_offset(t, 4 * q);
+                const uint32_t off = sw64_offset(tg, 4 * q);
                 *reinterpret_cast<float4*>(a_hi(ss) + off) = hi;
                 *reinterpret_cast<float4*>(a_lo(ss) + off) = lo;
+            }
+            if (t < k) {
 #pragma unroll
-                for (int hcol = 0; hcol < 2; ++hcol) {
-                    const int j = t + hcol * kBM;
-                    if (j < k) {
+                for (int q = 0; q < kWgRows / 4; ++q) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) v[e] = xs[(4 * q + e) * k + j];
-                        split4(v, hi, lo);
-                        const uint32_t offb = sw64_offset(j, 4 * q);
-                        *reinterpret_cast<float4*>(b_hi(ss) + offb) = hi;
-                        *reinterpret_cast<float4*>(b_lo(ss) + offb) = lo;
-                    }
+                    for (int e = 0; e < 4; ++e) v[e] = xs[(4 * q + e) * k + t];
+                    split4(v, hi, lo);
+                    const uint32_t off = sw64_offset(t, 4 * q);
+                    *reinterpret_cast<float4*>(b_hi(ss) + off) = hi;
+                    *reinterpret_cast<float4*>(b_lo(ss) + off) = lo;
                 }
             }
             // the tensor cores read the split stage through the async proxy
@@ -852,23 +855,24 @@ __global__ void __launch_bounds__(kWgThreads, 1)
             }
         }
         if (ok && stages > 0) {
-            if (gb != nullptr && m0 + t < n) atomicAdd(gb + m0 + t, bias_sum);
+            if (gb != nullptr && m0 + tg < n) atomicAdd(gb + m0 + tg, bias_sum);
             ok = mbar_wait(acc_full, 0);
             if (ok) {
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const int quarter = warp & 3;   // the tensor-memory lanes this warp may read
+                const int half = (warp - 2) >> 2;
                 const int m = m0 + quarter * 32 + lane;
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-                for (int c0 = 0; c0 < k; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(taddr + (uint32_t)c0, v);
+                for (int c0 = half * 32; c0 < k; c0 += 64) {
+                    float v32[32];
+                    tmem_ld32(taddr + (uint32_t)c0, v32);
                     if (m < n) {
                         float* dst = gw + (size_t)m * k + c0;
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             if (c0 + 4 * j < k)
-                                msda::red_add_v4(dst + 4 * j, v[4 * j], v[4 * j + 1],
-                                                 v[4 * j + 2], v[4 * j + 3]);
+                                msda::red_add_v4(dst + 4 * j, v32[4 * j], v32[4 * j + 1],
+                                                 v32[4 * j + 2], v32[4 * j + 3]);
                     }
                 }
             }

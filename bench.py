@@ -280,17 +280,20 @@ def run_layer(args, wl):
     # the same layer with torch.nn.Linear (cuBLAS) projections first, for
     # comparison; it warms up twice as long as asked (first-use costs of the
     # allocator and of each kernel module)
-    cb_eager, cb_graph, _ = measure(False, 2 * args.warmup)
-    compare = {"cublas_projections_ms": statistics.median(cb_graph or cb_eager),
-               "cublas_projections_eager_ms": statistics.median(cb_eager),
-               "gemm": None}
+    compare = None
+    if not args.no_projection_compare:
+        cb_eager, cb_graph, _ = measure(False, 2 * args.warmup)
+        compare = {"cublas_projections_ms": statistics.median(cb_graph or cb_eager),
+                   "cublas_projections_eager_ms": statistics.median(cb_eager),
+                   "gemm": None}
     if dist:
         dist.barrier()
     sampler = ClockSampler(local)
     tc_eager, tc_graph, clocks = measure(True, args.warmup, sampler)
     if dist:
         dist.barrier()
-    compare["gemm"] = _projection_gemm(layer.output_proj, wl.bs * wl.num_keys, dev, flush)
+    if compare is not None:
+        compare["gemm"] = _projection_gemm(layer.output_proj, wl.bs * wl.num_keys, dev, flush)
     ms = tc_graph or tc_eager
     ms_step = max_over_ranks(sum(ms) / len(ms), dist, dev)
     if rank != 0:
@@ -339,7 +342,8 @@ def _projection_gemm(linear, rows, dev, flush, reps=20):
     """One d_model x d_model projection of `rows` tokens in the layer's dtype:
     msda_linear / msda_linear_f32 (tcgen05) against torch's F.linear (cuBLAS),
     and in fp32 the parameter gradients (msda_linear_wgrad_f32 against torch);
-    CUDA events around graph replays, L2 flushed before each call."""
+    CUDA events around each call, enqueued while the device sleeps, L2 flushed
+    before each call."""
     import torch
     import torch.nn.functional as F
     from scale_deformable_attention_05_b300 import binding as B
@@ -353,24 +357,18 @@ def _projection_gemm(linear, rows, dev, flush, reps=20):
                      dtype=torch.uint8, device=dev)
 
     def timed(fn):
-        # each call captured as a CUDA graph and replayed, so that the host's
+        # the device sleeps while the host enqueues every rep, so that the host's
         # marshalling (15-20 us a call, more on a loaded host) stays outside the events
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            for _ in range(3):
-                fn()
-        torch.cuda.current_stream().wait_stream(side)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
+        for _ in range(3):
             fn()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(reps)]
         torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)           # ~10 ms at the B300's clocks
         for e0, e1 in evs:
             flush.zero_()
             e0.record()
-            graph.replay()
+            fn()
             e1.record()
         torch.cuda.synchronize()
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
@@ -879,6 +877,9 @@ def main():
                     help="with --path fused: pass a key padding mask (padded image batch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-projection-compare", action="store_true",
+                    help="--path layer: skip the cuBLAS-projection layer and the GEMM comparisons "
+                         "(for launch lists of the library's own step)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every pass through the Python binding instead of replaying "
                          "its captured CUDA graph")

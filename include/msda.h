@@ -348,6 +348,23 @@ MSDA_API int msda_linear_wgrad_f32(const float* grad_y, const float* x, float* g
                                    float* grad_b, int rows, int in_features, int out_features,
                                    unsigned flags, void* stream);
 
+/*
+ * Bias gradient of a projection: grad_b[c] (+)= sum_r grad_y[r, c], summed in
+ * fp32 (the bf16 and fp16 layers' bias gradients; the fp32 layers get theirs
+ * from msda_linear_wgrad_f32).
+ *   grad_y [rows, features]  dtype MSDA_F32, MSDA_BF16 or MSDA_F16, row-major,
+ *                            device pointer
+ *   grad_b [features]        fp32, device pointer; overwritten unless flags
+ *                            has MSDA_GRAD_VALUE_ACCUMULATE
+ * features must be a multiple of the 16-byte vector (4 fp32 or 8 half
+ * elements) and at most 256 vectors (else MSDA_ERR_UNSUPPORTED); pointers
+ * 16-byte aligned (MSDA_ERR_ALIGN).  Launches on `stream` (a zero-fill unless
+ * accumulating, then one kernel whose CTAs add their partial sums with
+ * atomicAdd, so the last bits vary between runs).
+ */
+MSDA_API int msda_linear_bias_grad(const void* grad_y, float* grad_b, int rows, int features,
+                                   int dtype, unsigned flags, void* stream);
+
 /* MSDA_VERSION of the built library. */
 MSDA_API int msda_version(void);
 

@@ -22,7 +22,7 @@ __all__ = [
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
     "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused", "msda_linear",
     "msda_linear_f32", "msda_linear_workspace_bytes", "msda_linear_wgrad_f32",
-    "MSDeformAttnFunction", "MSDeformAttnFusedFunction", "ms_deform_attn", "ms_deform_attn_fused",
+    "msda_linear_bias_grad", "MSDeformAttnFunction", "MSDeformAttnFusedFunction", "ms_deform_attn", "ms_deform_attn_fused",
     "EXPORTED_SYMBOLS", "load_library",
 ]
 
@@ -41,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "msda_check_shapes", "msda_last_device_error", "msda_status_string", "msda_version",
     "msda_backward_noalloc", "msda_forward_fused", "msda_backward_fused", "msda_linear",
     "msda_linear_f32", "msda_linear_workspace_bytes", "msda_linear_wgrad_f32",
+    "msda_linear_bias_grad",
 )
 
 _vp = ctypes.c_void_p
@@ -86,6 +87,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.msda_linear_f32.restype = _int
     lib.msda_linear_wgrad_f32.argtypes = [_vp] * 4 + [_int] * 3 + [ctypes.c_uint, _vp]
     lib.msda_linear_wgrad_f32.restype = _int
+    lib.msda_linear_bias_grad.argtypes = [_vp, _vp, _int, _int, _int, ctypes.c_uint, _vp]
+    lib.msda_linear_bias_grad.restype = _int
     lib.msda_forward_fused.argtypes = [_vp] * 8 + _DIMS + [_int, _int, _vp]
     lib.msda_forward_fused.restype = _int
     lib.msda_backward_fused.argtypes = ([_vp] * 13 + [ctypes.c_size_t] + _DIMS +
@@ -370,6 +373,26 @@ def msda_linear_wgrad_f32(grad_y: torch.Tensor, x: torch.Tensor, bias: bool = Tr
         _ptr(g2), _ptr(x2), _ptr(grad_w), _ptr(grad_b) if grad_b is not None else None,
         rows, n_in, n_out, MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0, _stream(stream)))
     return grad_w, grad_b
+
+
+def msda_linear_bias_grad(grad_y: torch.Tensor, grad_b: Optional[torch.Tensor] = None,
+                          accumulate: bool = False, stream=None) -> torch.Tensor:
+    """fp32 column sums of grad_y [..., features] (fp32, bf16 or fp16 CUDA tensor):
+    the bias gradient of a projection (see msda_linear_bias_grad in include/msda.h)."""
+    g2 = grad_y.reshape(-1, grad_y.shape[-1])
+    if not (g2.is_cuda and g2.is_contiguous()):
+        raise ValueError("grad_y must be a contiguous CUDA tensor")
+    n = int(g2.shape[1])
+    if grad_b is None:
+        if accumulate:
+            raise ValueError("accumulate needs grad_b")
+        grad_b = torch.empty(n, dtype=torch.float32, device=g2.device)
+    elif grad_b.shape != (n,) or grad_b.dtype != torch.float32 or grad_b.device != g2.device:
+        raise ValueError("grad_b must be an fp32 [features] tensor on grad_y's device")
+    _check("msda_linear_bias_grad", _LIB.msda_linear_bias_grad(
+        _ptr(g2), _ptr(grad_b), int(g2.shape[0]), n, _dtype_code(g2),
+        MSDA_GRAD_VALUE_ACCUMULATE if accumulate else 0, _stream(stream)))
+    return grad_b
 
 
 def _fused_dims(value, spatial_shapes, reference_points, sampling_offsets, attn_logits):

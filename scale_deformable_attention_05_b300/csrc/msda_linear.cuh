@@ -887,6 +887,58 @@ __global__ void __launch_bounds__(kWgThreads, 1)
                      : "memory");
 }
 
+// ------------------------------------------------------------ bias gradient
+// Column sums of a projection's output gradient, grad_b[c] = sum_r grad_y[r, c],
+// for the bf16 and fp16 layers (whose weight gradients run on the library GEMM):
+// a streaming read of grad_y at HBM speed, fp32 sums.  Each CTA takes a
+// contiguous range of rows; its threads hold one 16-byte vector of columns each
+// for a set of rows, the CTA adds its rows up in shared memory and adds its
+// column sums to grad_b with atomicAdd.
+constexpr int kColThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kColThreads)
+    column_sum_kernel(const T* __restrict__ gy, float* __restrict__ out, int rows, int n,
+                      int rows_per_cta) {
+    constexpr int V = IO<T>::kVec;
+    __shared__ float s_part[kColThreads * V];
+    const int vpr = n / V;                          // vectors per row (<= kColThreads)
+    const int rpp = kColThreads / vpr;              // rows in parallel
+    const int cv = threadIdx.x % vpr, rsub = threadIdx.x / vpr;
+    const int r0 = blockIdx.x * rows_per_cta;
+    const int r1 = min(rows, r0 + rows_per_cta);
+    float acc[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) acc[j] = 0.f;
+    if (rsub < rpp) {
+        const T* base = gy + (size_t)cv * V;
+        int r = r0 + rsub;
+        for (; r + 3 * rpp < r1; r += 4 * rpp) {   // four independent rows in flight
+            float v[4][V];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) IO<T>::load_vec_stream(base + (size_t)(r + u * rpp) * n, v[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int j = 0; j < V; ++j) acc[j] += v[u][j];
+        }
+        for (; r < r1; r += rpp) {
+            float v[V];
+            IO<T>::load_vec_stream(base + (size_t)r * n, v);
+#pragma unroll
+            for (int j = 0; j < V; ++j) acc[j] += v[j];
+        }
+#pragma unroll
+        for (int j = 0; j < V; ++j) s_part[rsub * n + cv * V + j] = acc[j];
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < n; c += kColThreads) {
+        float t = 0.f;
+        for (int i = 0; i < rpp; ++i) t += s_part[i * n + c];
+        atomicAdd(out + c, t);
+    }
+}
+
 // ------------------------------------------------------------------- host
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1073,5 +1125,41 @@ extern "C" int msda_linear_wgrad_f32(const float* grad_y, const float* x, float*
     linear_wgrad_f32_kernel<<<ranges * tiles_m, kWgThreads, (size_t)smem_layout_wg().total + 1024,
                               st>>>(gym, xm, grad_w, grad_b, rows, out_features, in_features,
                                     tiles_m, rows_per_cta);
+    return cudaGetLastError() == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA;
+}
+
+extern "C" int msda_linear_bias_grad(const void* grad_y, float* grad_b, int rows, int features,
+                                     int dtype, unsigned flags, void* stream) {
+    using namespace msda;
+    if (rows < 0 || features < 0) return MSDA_ERR_DIM;
+    if (flags & ~MSDA_GRAD_VALUE_ACCUMULATE) return MSDA_ERR_UNSUPPORTED;
+    if (dtype != MSDA_F32 && dtype != MSDA_BF16 && dtype != MSDA_F16) return MSDA_ERR_UNSUPPORTED;
+    const int vec = dtype == MSDA_F32 ? 4 : 8;
+    if (features == 0 || features % vec != 0 || features / vec > linear::kColThreads)
+        return MSDA_ERR_UNSUPPORTED;
+    if (grad_b == nullptr) return MSDA_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(grad_b) & 15u) != 0) return MSDA_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!(flags & MSDA_GRAD_VALUE_ACCUMULATE) &&
+        launch_zero_fill(grad_b, (size_t)features * 4, st) != cudaSuccess)
+        return MSDA_ERR_CUDA;
+    if (rows == 0) return MSDA_OK;
+    if (grad_y == nullptr) return MSDA_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(grad_y) & 15u) != 0) return MSDA_ERR_ALIGN;
+    // a few CTAs per SM, each over a contiguous range of at least 32 rows
+    int grid = linear::sm_count() * 4;
+    const int max_grid = (rows + 31) / 32;
+    if (grid > max_grid) grid = max_grid;
+    const int rows_per_cta = (rows + grid - 1) / grid;
+    grid = (rows + rows_per_cta - 1) / rows_per_cta;
+    if (dtype == MSDA_F32)
+        linear::column_sum_kernel<float><<<grid, linear::kColThreads, 0, st>>>(
+            static_cast<const float*>(grad_y), grad_b, rows, features, rows_per_cta);
+    else if (dtype == MSDA_BF16)
+        linear::column_sum_kernel<__nv_bfloat16><<<grid, linear::kColThreads, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(grad_y), grad_b, rows, features, rows_per_cta);
+    else
+        linear::column_sum_kernel<__half><<<grid, linear::kColThreads, 0, st>>>(
+            static_cast<const __half*>(grad_y), grad_b, rows, features, rows_per_cta);
     return cudaGetLastError() == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA;
 }

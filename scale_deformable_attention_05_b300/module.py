@@ -15,8 +15,9 @@ kernels (tcgen05.mma with the accumulator in tensor memory) for the forward and
 for the input gradient (x-gradient = grad_y times the weight, i.e. the same
 kernel with the transposed weight): ``msda_linear`` in bf16, ``msda_linear_f32``
 (three TF32 products per step, fp32 accuracy) in fp32.  The weight and bias
-gradients (reductions over all tokens) use ``msda_linear_wgrad_f32`` in fp32
-and torch (cuBLAS) in bf16.  Everything between the projections -- masking,
+gradients (reductions over all tokens) use ``msda_linear_wgrad_f32`` in fp32;
+in bf16 the weight gradient uses torch (cuBLAS) and the bias gradient
+``msda_linear_bias_grad``.  Everything between the projections -- masking,
 softmax, locations from 2-d or 4-d reference points, bilinear sampling and
 their backward -- is one launch of the fused entry points of ``libmsda.so``
 each way.  The tensors the GEMMs produce are already in the operator's
@@ -53,8 +54,9 @@ class TensorCoreLinear(torch.autograd.Function):
     """y = x w^T + b with x and w both bf16 or both fp32 on the tensor cores
     (msda_linear / msda_linear_f32); the input gradient through the same kernel
     with w^T when its shape allows (else a cuBLAS matmul); the weight and bias
-    gradients on the tensor cores in fp32 (msda_linear_wgrad_f32), with torch
-    (cuBLAS) in bf16."""
+    gradients on the tensor cores in fp32 (msda_linear_wgrad_f32); in bf16 the
+    weight gradient with torch (cuBLAS) and the bias gradient with
+    msda_linear_bias_grad."""
 
     @staticmethod
     def forward(ctx, x, weight, bias):
@@ -77,7 +79,7 @@ class TensorCoreLinear(torch.autograd.Function):
                                              bias=ctx.has_bias)
             return gx, gw, gb
         gw = g2.t() @ x.reshape(-1, n_in)
-        gb = torch.sum(g2, 0, dtype=torch.float32).to(weight.dtype) if ctx.has_bias else None
+        gb = B.msda_linear_bias_grad(g2).to(weight.dtype) if ctx.has_bias else None
         return gx, gw, gb
 
 

@@ -222,3 +222,34 @@ def test_linear_wgrad_f32_without_bias_and_checks(B):
     with pytest.raises(B.MsdaError) as e:
         B.msda_linear_wgrad_f32(torch.zeros(8, 24, device="cuda"), torch.zeros(8, 32, device="cuda"))
     assert e.value.status == 3                                 # out_features not a multiple of 16
+
+
+# ------------------------------------------------------------------ bias gradient
+# msda_linear_bias_grad: fp32 column sums of grad_y against fp64.  Each sum is a
+# thread's sequential sum over its rows, a sum over the CTA's row lanes and the
+# CTAs' atomic additions, each rounding by <= 2^-24 of its running sum; a few
+# hundred roundings at most: allowed 2^-14 of sum |grad_y|.
+
+@pytest.mark.parametrize("rows,n,dtype", [
+    (1, 16, torch.bfloat16), (88892, 256, torch.bfloat16), (44446, 256, torch.float32),
+    (1000, 128, torch.float16), (517, 40, torch.float32), (300, 2048, torch.bfloat16),
+])
+def test_linear_bias_grad_matches_fp64(B, rows, n, dtype):
+    g = torch.Generator().manual_seed(rows + n)
+    gy = torch.randn(rows, n, generator=g).to(dtype)
+    gb = B.msda_linear_bias_grad(gy.cuda())
+    torch.cuda.synchronize()
+    ref = gy.double().sum(0).numpy()
+    err = np.abs(gb.cpu().double().numpy() - ref)
+    assert (err <= 2.0 ** -14 * gy.double().abs().sum(0).numpy()).all(), err.max()
+
+
+def test_linear_bias_grad_accumulates_and_checks(B):
+    gy = torch.randn(70, 64, device="cuda")
+    acc = torch.ones(64, device="cuda")
+    B.msda_linear_bias_grad(gy, grad_b=acc, accumulate=True)
+    torch.cuda.synchronize()
+    assert torch.allclose(acc.double(), 1 + gy.double().sum(0), atol=1e-4)
+    with pytest.raises(B.MsdaError) as e:
+        B.msda_linear_bias_grad(torch.zeros(4, 12, dtype=torch.bfloat16, device="cuda"))
+    assert e.value.status == 3                        # 12 bf16 columns: not whole 16-byte vectors

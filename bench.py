@@ -198,11 +198,11 @@ def run_layer(args, wl):
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     from scale_deformable_attention_05_b300.module import MSDeformAttn
-    if wl.dtype not in ("f32", "bf16"):
-        raise SystemExit("--path layer runs fp32 or bf16 workloads")
+    if wl.dtype not in ("f32", "bf16", "f16"):
+        raise SystemExit("--path layer runs fp32, bf16 or fp16 workloads")
     torch.backends.cuda.matmul.allow_tf32 = False
     dev = torch.device("cuda", local)
-    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[wl.dtype]
     wl_r = rank_workload(wl, rank)
     C = wl.num_heads * wl.head_dim
     torch.manual_seed(wl_r.seed)
@@ -303,8 +303,9 @@ def run_layer(args, wl):
     cfg = _config(wl, args)
     cfg["entry_points"] = ("module.MSDeformAttn: value / offset / weight / output projections "
                            + ("(msda_linear on the tensor cores forward and for the input "
-                              "gradients; weight gradients with torch, cuBLAS bf16)"
-                              if wl.dtype == "bf16" else
+                              "gradients; weight gradients with torch (cuBLAS), bias gradients "
+                              "with msda_linear_bias_grad)"
+                              if wl.dtype != "f32" else
                               "(msda_linear_f32, three TF32 products on the tensor cores, "
                               "forward and for the input gradients; weight and bias "
                               "gradients with msda_linear_wgrad_f32)")
@@ -326,11 +327,12 @@ def run_layer(args, wl):
         "projections": compare,
         "roofline": None, "clocks": clocks, "e2e": None,
         # the library's kernels per step: fused forward; grad_value (or fp32 workspace)
-        # zero-fill + fused backward (+ the bf16 finalize); four projections forward
-        # and four input gradients, one launch each in bf16 and two (the split of w
-        # and the GEMM) in fp32; in fp32 also four weight gradients (two zero-fills
-        # and the kernel each)
-        "gpu_launches": (3 + 8 * 2 + 4 * 3 if wl.dtype == "f32" else 4 + 8) * args.steps,
+        # zero-fill + fused backward (+ the half-precision finalize); four projections
+        # forward and four input gradients, one launch each in bf16 / fp16 and two (the
+        # split of w and the GEMM) in fp32; four parameter gradients: in fp32 two
+        # zero-fills and the weight-gradient kernel each, in bf16 / fp16 a zero-fill
+        # and the bias column sum each
+        "gpu_launches": (3 + 8 * 2 + 4 * 3 if wl.dtype == "f32" else 4 + 8 + 4 * 2) * args.steps,
     }
     print(json.dumps(line), flush=True)
     if dist:
@@ -373,7 +375,7 @@ def _projection_gemm(linear, rows, dev, flush, reps=20):
         torch.cuda.synchronize()
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
 
-    if dt == torch.bfloat16:
+    if dt != torch.float32:
         tc = timed(lambda: B.msda_linear(xg, w, bf, out=out))
     else:
         tc = timed(lambda: B.msda_linear_f32(xg, w, b, out=out, workspace=ws))

@@ -276,13 +276,15 @@ MSDA_API int msda_backward_noalloc(const void* value, const void* spatial_shapes
  * Linear projection on the tensor cores: y = x * w^T + bias, the nn.Linear
  * layers around the operator in MSDeformAttn.forward (walk-through, "2.2.4
  * 源码分析": value_proj, sampling_offsets, attention_weights, output_proj).
- *   x    [rows, in_features]          bf16, row-major, device pointer
- *   w    [out_features, in_features]  bf16 (nn.Linear weight layout)
- *   bias [out_features]               fp32, or bf16 when dtype has
- *                                      MSDA_LINEAR_BIAS_BF16, or NULL
- *   y    [rows, out_features]         bf16, overwritten; fp32 accumulation,
- *                                      one rounding to bf16 after the bias
- * dtype must be MSDA_BF16 (optionally | MSDA_LINEAR_BIAS_BF16).  in_features
+ *   x    [rows, in_features]          bf16 (fp16 when dtype is MSDA_F16),
+ *                                      row-major, device pointer
+ *   w    [out_features, in_features]  the same type (nn.Linear weight layout)
+ *   bias [out_features]               fp32, or the operands' type when dtype
+ *                                      has MSDA_LINEAR_BIAS_HALF, or NULL
+ *   y    [rows, out_features]         the operands' type, overwritten; fp32
+ *                                      accumulation, one rounding after the bias
+ * dtype must be MSDA_BF16 or MSDA_F16 (optionally | MSDA_LINEAR_BIAS_HALF;
+ * MSDA_LINEAR_BIAS_BF16 is the same flag).  in_features
  * must be a multiple of 64 and
  * out_features a multiple of 16, both at most MSDA_LINEAR_MAX_FEATURES (else
  * MSDA_ERR_UNSUPPORTED); every pointer 16-byte aligned (MSDA_ERR_ALIGN).
@@ -291,7 +293,8 @@ MSDA_API int msda_backward_noalloc(const void* value, const void* spatial_shapes
  * stops the kernel and raises the error word msda_last_device_error() reads.
  */
 #define MSDA_LINEAR_MAX_FEATURES 256
-#define MSDA_LINEAR_BIAS_BF16 0x200
+#define MSDA_LINEAR_BIAS_HALF 0x200
+#define MSDA_LINEAR_BIAS_BF16 MSDA_LINEAR_BIAS_HALF
 MSDA_API int msda_linear(const void* x, const void* w, const void* bias, void* y, int rows,
                          int in_features, int out_features, int dtype, void* stream);
 

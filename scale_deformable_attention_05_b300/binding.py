@@ -33,7 +33,8 @@ MSDA_INDEX_INT32 = 0x100
 MSDA_GRAD_VALUE_ACCUMULATE = 1
 MSDA_MAX_FUSED_LEVEL_POINTS = 64
 MSDA_LINEAR_MAX_FEATURES = 256
-MSDA_LINEAR_BIAS_BF16 = 0x200
+MSDA_LINEAR_BIAS_HALF = 0x200
+MSDA_LINEAR_BIAS_BF16 = MSDA_LINEAR_BIAS_HALF
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsda.so")
 EXPORTED_SYMBOLS = (
@@ -263,10 +264,10 @@ def msda_backward_noalloc(value, spatial_shapes, level_start_index, sampling_loc
 def msda_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """y = x @ weight.T + bias on the tensor cores (see msda_linear in include/msda.h):
-    x [..., in] and weight [out, in] bf16 CUDA tensors, bias fp32 or bf16 [out] or
-    None; returns bf16 [..., out]."""
-    if x.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
-        raise TypeError("msda_linear takes bf16 x and weight")
+    x [..., in] and weight [out, in] bf16 (or both fp16) CUDA tensors, bias fp32 or
+    the operands' dtype [out] or None; returns [..., out] in the operands' dtype."""
+    if x.dtype not in (torch.bfloat16, torch.float16) or weight.dtype != x.dtype:
+        raise TypeError("msda_linear takes bf16 (or fp16) x and weight of one dtype")
     if not (x.is_cuda and weight.is_cuda) or x.device != weight.device:
         raise ValueError("x and weight must be CUDA tensors on one device")
     if weight.dim() != 2 or x.shape[-1] != weight.shape[1]:
@@ -276,18 +277,18 @@ def msda_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tens
         raise ValueError("x must be contiguous")
     weight = weight.contiguous()
     n_out = int(weight.shape[0])
-    code = MSDA_BF16
+    code = MSDA_BF16 if x.dtype == torch.bfloat16 else MSDA_F16
     if bias is not None:
-        if (bias.dtype not in (torch.float32, torch.bfloat16) or bias.shape != (n_out,)
+        if (bias.dtype not in (torch.float32, x.dtype) or bias.shape != (n_out,)
                 or bias.device != x.device):
-            raise ValueError("bias must be an fp32 or bf16 [out_features] tensor on x's device")
+            raise ValueError("bias must be an fp32 or x-dtype [out_features] tensor on x's device")
         bias = bias.contiguous()
-        if bias.dtype == torch.bfloat16:
-            code |= MSDA_LINEAR_BIAS_BF16
+        if bias.dtype == x.dtype:
+            code |= MSDA_LINEAR_BIAS_HALF
     if out is None:
-        out = torch.empty(*x.shape[:-1], n_out, dtype=torch.bfloat16, device=x.device)
-    elif out.dtype != torch.bfloat16 or out.shape != (*x.shape[:-1], n_out) or not out.is_contiguous():
-        raise ValueError("out must be a contiguous bf16 [..., out_features] tensor")
+        out = torch.empty(*x.shape[:-1], n_out, dtype=x.dtype, device=x.device)
+    elif out.dtype != x.dtype or out.shape != (*x.shape[:-1], n_out) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [..., out_features] tensor of x's dtype")
     _check("msda_linear", _LIB.msda_linear(
         _ptr(x2), _ptr(weight), _ptr(bias) if bias is not None else None, _ptr(out),
         int(x2.shape[0]), int(x2.shape[1]), n_out, code, _stream(stream)))

@@ -32,11 +32,13 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/msda.h"
 #include "msda_device.cuh"
@@ -125,12 +127,12 @@ __device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both K-major,
-// M = 128 and N = n.
-__host__ __device__ constexpr uint32_t bf16_idesc(int n) {
+// Instruction descriptor of kind::f16 with bf16 (or, with f16, fp16) A and B,
+// fp32 D, both K-major, M = 128 and N = n.
+__host__ __device__ constexpr uint32_t bf16_idesc(int n, bool f16 = false) {
     return (1u << 4)                         // D format: f32
-           | (1u << 7)                       // A format: bf16
-           | (1u << 10)                      // B format: bf16
+           | ((f16 ? 0u : 1u) << 7)          // A format: bf16 (1) or f16 (0)
+           | ((f16 ? 0u : 1u) << 10)         // B format: the same type as A
            | ((uint32_t)(n >> 3) << 17)      // N / 8
            | ((uint32_t)(kBM >> 4) << 24);   // M / 16
 }
@@ -185,11 +187,28 @@ __host__ __device__ inline Smem smem_layout(int n, int k) {
     return s;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    linear_bf16_kernel(const __grid_constant__ CUtensorMap x_map,
-                       const __grid_constant__ CUtensorMap w_map,
-                       const __grid_constant__ CUtensorMap y_map, const void* __restrict__ bias,
-                       int bias_bf16, int rows, int n, int k) {
+// Two fp32 values rounded to nearest even in T and packed low, high.
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// The 16-bit kernels' body; T is __nv_bfloat16 or __half (both operands, the
+// output, and the bias when bias_half).
+template <typename T>
+__device__ __forceinline__ void linear16_body(const CUtensorMap& x_map, const CUtensorMap& w_map,
+                                              const CUtensorMap& y_map,
+                                              const void* __restrict__ bias, int bias_half,
+                                              int rows, int n, int k) {
+    constexpr bool kF16 = std::is_same<T, __half>::value;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // TMA destinations with the 128-byte swizzle must sit on 1024-byte boundaries
     unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -254,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = bf16_idesc(n);
+            const uint32_t idesc = bf16_idesc(n, kF16);
             bool ok = mbar_wait(w_full, 0);
             uint32_t it = 0, acc_it = 0;
             for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++acc_it) {
@@ -293,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = ew * 32 + lane; c < MSDA_LINEAR_MAX_FEATURES; c += kEpiWarps * 32) {
             float bv = 0.f;
             if (bias != nullptr && c < n)
-                bv = bias_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(bias)[c])
+                bv = bias_half ? (float)static_cast<const T*>(bias)[c]
                                : static_cast<const float*>(bias)[c];
             s_bias[c] = bv;
         }
@@ -318,12 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float4 bb = bq[i];
-                    const __nv_bfloat162 h0 =
-                        __floats2bfloat162_rn(v[4 * i] + bb.x, v[4 * i + 1] + bb.y);
-                    const __nv_bfloat162 h1 =
-                        __floats2bfloat162_rn(v[4 * i + 2] + bb.z, v[4 * i + 3] + bb.w);
-                    o[2 * i] = *reinterpret_cast<const uint32_t*>(&h0);
-                    o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+                    o[2 * i] = pack2<T>(v[4 * i] + bb.x, v[4 * i + 1] + bb.y);
+                    o[2 * i + 1] = pack2<T>(v[4 * i + 2] + bb.z, v[4 * i + 3] + bb.w);
                 }
                 // the staging buffer of this piece must have been read by its previous store
                 const int buf = (int)(piece & 1u);
@@ -354,6 +369,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(2 * kAccCols)
                      : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_bf16_kernel(const __grid_constant__ CUtensorMap x_map,
+                       const __grid_constant__ CUtensorMap w_map,
+                       const __grid_constant__ CUtensorMap y_map, const void* __restrict__ bias,
+                       int bias_half, int rows, int n, int k) {
+    linear16_body<__nv_bfloat16>(x_map, w_map, y_map, bias, bias_half, rows, n, k);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_f16_kernel(const __grid_constant__ CUtensorMap x_map,
+                      const __grid_constant__ CUtensorMap w_map,
+                      const __grid_constant__ CUtensorMap y_map, const void* __restrict__ bias,
+                      int bias_half, int rows, int n, int k) {
+    linear16_body<__half>(x_map, w_map, y_map, bias, bias_half, rows, n, k);
 }
 
 // ---------------------------------------------------------- fp32 (3 x TF32)
@@ -958,18 +989,21 @@ EncodeTiled encode_tiled() {
     return fn;
 }
 
-// Row-major bf16 (or fp32) matrix [outer, inner] moved in boxes of [box_rows, box_cols]
+// Row-major bf16 (or fp32, or fp16) matrix [outer, inner] moved in boxes of [box_rows, box_cols]
 // (with the 128- or 64-byte swizzle, or none); elements past the matrix read as
 // zero and are not written.
 bool make_map(CUtensorMap* map, const void* ptr, int inner, int outer, int box_cols, int box_rows,
-              int swizzle_bytes, bool fp32 = false) {
+              int swizzle_bytes, bool fp32 = false, bool f16 = false) {
     const EncodeTiled enc = encode_tiled();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
     const cuuint64_t strides[1] = {(cuuint64_t)inner * (fp32 ? 4 : 2)};
     const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    const CUtensorMapDataType type = fp32  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return enc(map, type, 2,
                const_cast<void*>(ptr), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
@@ -992,8 +1026,10 @@ int sm_count() {
 extern "C" int msda_linear(const void* x, const void* w, const void* bias, void* y,
                                     int rows, int in_features, int out_features, int dtype,
                                     void* stream) {
-    if ((dtype & ~MSDA_LINEAR_BIAS_BF16) != MSDA_BF16) return MSDA_ERR_UNSUPPORTED;
-    const int bias_bf16 = (dtype & MSDA_LINEAR_BIAS_BF16) ? 1 : 0;
+    const int type = dtype & ~MSDA_LINEAR_BIAS_HALF;
+    if (type != MSDA_BF16 && type != MSDA_F16) return MSDA_ERR_UNSUPPORTED;
+    const bool f16 = type == MSDA_F16;
+    const int bias_half = (dtype & MSDA_LINEAR_BIAS_HALF) ? 1 : 0;
     if (rows < 0 || in_features < 0 || out_features < 0) return MSDA_ERR_DIM;
     using namespace msda::linear;
     if (in_features % kBK != 0 || in_features < kBK || in_features > MSDA_LINEAR_MAX_FEATURES ||
@@ -1006,23 +1042,27 @@ extern "C" int msda_linear(const void* x, const void* w, const void* bias, void*
         return MSDA_ERR_ALIGN;
     if ((int64_t)rows * in_features > 2147483647LL * 64) return MSDA_ERR_DIM;
     CUtensorMap xm, wm, ym;
-    if (!make_map(&xm, x, in_features, rows, kBK, kBM, 128) ||
-        !make_map(&wm, w, in_features, out_features, kBK, out_features, 128) ||
-        !make_map(&ym, y, out_features, rows, kChunk, kChunk, 0))
+    if (!make_map(&xm, x, in_features, rows, kBK, kBM, 128, false, f16) ||
+        !make_map(&wm, w, in_features, out_features, kBK, out_features, 128, false, f16) ||
+        !make_map(&ym, y, out_features, rows, kChunk, kChunk, 0, false, f16))
         return MSDA_ERR_CUDA;
     const Smem L = smem_layout(out_features, in_features);
     const size_t smem = (size_t)L.total + 1024;
     static std::once_flag attr_once;
     std::call_once(attr_once, [] {
-        cudaFuncSetAttribute(linear_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(smem_layout(MSDA_LINEAR_MAX_FEATURES, MSDA_LINEAR_MAX_FEATURES)
-                                       .total +
-                                   1024));
+        const int most =
+            (int)(smem_layout(MSDA_LINEAR_MAX_FEATURES, MSDA_LINEAR_MAX_FEATURES).total + 1024);
+        cudaFuncSetAttribute(linear_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+        cudaFuncSetAttribute(linear_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     });
     const int tiles = (rows + kBM - 1) / kBM;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    linear_bf16_kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-        xm, wm, ym, bias, bias_bf16, rows, out_features, in_features);
+    if (f16)
+        linear_f16_kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+            xm, wm, ym, bias, bias_half, rows, out_features, in_features);
+    else
+        linear_bf16_kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+            xm, wm, ym, bias, bias_half, rows, out_features, in_features);
     return cudaGetLastError() == cudaSuccess ? MSDA_OK : MSDA_ERR_CUDA;
 }
 

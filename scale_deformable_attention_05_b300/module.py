@@ -13,10 +13,10 @@ them,
 The four projections are dense GEMMs.  They run on the library's tensor-core
 kernels (tcgen05.mma with the accumulator in tensor memory) for the forward and
 for the input gradient (x-gradient = grad_y times the weight, i.e. the same
-kernel with the transposed weight): ``msda_linear`` in bf16, ``msda_linear_f32``
-(three TF32 products per step, fp32 accuracy) in fp32.  The weight and bias
+kernel with the transposed weight): ``msda_linear`` in bf16 and fp16,
+``msda_linear_f32`` (three TF32 products per step, fp32 accuracy) in fp32.  The weight and bias
 gradients (reductions over all tokens) use ``msda_linear_wgrad_f32`` in fp32;
-in bf16 the weight gradient uses torch (cuBLAS) and the bias gradient
+in bf16 and fp16 the weight gradient uses torch (cuBLAS) and the bias gradient
 ``msda_linear_bias_grad``.  Everything between the projections -- masking,
 softmax, locations from 2-d or 4-d reference points, bilinear sampling and
 their backward -- is one launch of the fused entry points of ``libmsda.so``
@@ -34,28 +34,28 @@ from torch import nn
 from . import binding as B
 
 
-_TC_DTYPES = (torch.bfloat16, torch.float32)
+_TC_DTYPES = (torch.bfloat16, torch.float16, torch.float32)
 
 
 def _tensor_core_shape(in_features: int, out_features: int, dtype=torch.bfloat16) -> bool:
-    k_step = 64 if dtype == torch.bfloat16 else 16        # the kernels' K block
+    k_step = 16 if dtype == torch.float32 else 64         # the kernels' K block
     return (in_features % k_step == 0 and out_features % 16 == 0 and
             in_features <= B.MSDA_LINEAR_MAX_FEATURES and
             out_features <= B.MSDA_LINEAR_MAX_FEATURES)
 
 
 def _tc_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor]) -> torch.Tensor:
-    if x.dtype == torch.bfloat16:
-        return B.msda_linear(x, weight, bias)
-    return B.msda_linear_f32(x, weight, bias)
+    if x.dtype == torch.float32:
+        return B.msda_linear_f32(x, weight, bias)
+    return B.msda_linear(x, weight, bias)
 
 
 class TensorCoreLinear(torch.autograd.Function):
-    """y = x w^T + b with x and w both bf16 or both fp32 on the tensor cores
-    (msda_linear / msda_linear_f32); the input gradient through the same kernel
-    with w^T when its shape allows (else a cuBLAS matmul); the weight and bias
-    gradients on the tensor cores in fp32 (msda_linear_wgrad_f32); in bf16 the
-    weight gradient with torch (cuBLAS) and the bias gradient with
+    """y = x w^T + b with x and w of one dtype (bf16, fp16 or fp32) on the tensor
+    cores (msda_linear / msda_linear_f32); the input gradient through the same
+    kernel with w^T when its shape allows (else a cuBLAS matmul); the weight and
+    bias gradients on the tensor cores in fp32 (msda_linear_wgrad_f32); in bf16
+    and fp16 the weight gradient with torch (cuBLAS) and the bias gradient with
     msda_linear_bias_grad."""
 
     @staticmethod
@@ -84,7 +84,7 @@ class TensorCoreLinear(torch.autograd.Function):
 
 
 def project(linear: nn.Linear, x: torch.Tensor, tensor_cores: bool = True) -> torch.Tensor:
-    """linear(x), on the tensor-core kernels for bf16 or fp32 operands of supported widths."""
+    """linear(x), on the tensor-core kernels for bf16, fp16 or fp32 operands of supported widths."""
     if (tensor_cores and x.is_cuda and x.dtype in _TC_DTYPES and
             linear.weight.dtype == x.dtype and
             _tensor_core_shape(linear.in_features, linear.out_features, x.dtype)):
@@ -97,8 +97,8 @@ def project(linear: nn.Linear, x: torch.Tensor, tensor_cores: bool = True) -> to
 class MSDeformAttn(nn.Module):
     """Multi-scale deformable attention with d_model channels split into
     n_heads heads, sampling n_points points on each of n_levels levels.
-    tensor_core_projections: bf16 and fp32 projections on the library's
-    tensor-core kernels (True) or on torch.nn.Linear (False)."""
+    tensor_core_projections: projections on the library's tensor-core kernels
+    (True) or on torch.nn.Linear (False)."""
 
     tensor_core_projections = True
 

@@ -253,3 +253,19 @@ def test_linear_bias_grad_accumulates_and_checks(B):
     with pytest.raises(B.MsdaError) as e:
         B.msda_linear_bias_grad(torch.zeros(4, 12, dtype=torch.bfloat16, device="cuda"))
     assert e.value.status == 3                        # 12 bf16 columns: not whole 16-byte vectors
+
+
+def test_linear_fp16_operands(B):
+    """fp16 x and w (kind::f16 with f16 operands), fp32 and fp16 bias: the same
+    bound with fp16's unit roundoff (one rounding of the result, 2^-11 relative)."""
+    for rows, k, n, seed in ((300, 256, 256, 31), (1000, 64, 80, 32)):
+        g = torch.Generator().manual_seed(seed)
+        x = torch.randn(rows, k, generator=g).to(torch.float16)
+        w = (torch.randn(n, k, generator=g) / np.sqrt(k)).to(torch.float16)
+        for b in (torch.randn(n, generator=g), torch.randn(n, generator=g).to(torch.float16)):
+            y = B.msda_linear(x.cuda(), w.cuda(), b.cuda())
+            torch.cuda.synchronize()
+            assert y.dtype == torch.float16
+            ref = x.double().numpy() @ w.double().numpy().T + b.double().numpy()
+            err = np.abs(y.double().cpu().numpy() - ref)
+            assert (err <= 2.0 ** -10 * np.abs(ref) + 1e-4 * np.abs(ref).max()).all(), err.max()

@@ -101,27 +101,39 @@ def test_module_matches_fp64_composition(ref_dim, masked):
         assert not host(tx.grad)[mask].any()
 
 
-def _bf16(a):
-    """Round to bf16 (round to nearest even) and widen back to fp64, on the CPU."""
-    return torch.from_numpy(np.asarray(a, np.float64)).to(torch.bfloat16).double().numpy()
+def _round(a, dtype):
+    """Round to bf16 or fp16 (round to nearest even) and widen back to fp64, on the CPU."""
+    return torch.from_numpy(np.asarray(a, np.float64)).to(dtype).double().numpy()
 
 
-def test_bf16_module_on_tensor_cores_matches_fp64_composition():
-    """The layer in bf16: its four projections run on the tensor-core kernel
-    (msda_linear) forward, and for the input gradients backward.  Reference:
-    the fp64 composition, with the layer's stored intermediates (value,
-    offsets, logits, the operator's output) rounded to bf16 where the layer
-    stores them.  Tolerance: the bf16 gradient rule, max|err| <= 1e-2 max|ref|,
-    for the output and every gradient."""
+def _assert_close(got, ref, tol, what):
+    scale = float(np.abs(ref).max())
+    err = float(np.abs(got - ref).max())
+    assert err <= tol * scale, f"{what}: max|err| {err:.3e} > {tol} * max|ref| ({scale:.3e})"
+
+
+@pytest.mark.parametrize("dtype,tol", [
+    (torch.bfloat16, 1e-2),     # the bf16 gradient rule
+    (torch.float16, 4e-3),      # eight fp16 unit roundoffs: the layer stores value, offsets,
+                                # logits, the operator's output and every gradient in fp16
+])
+def test_half_module_on_tensor_cores_matches_fp64_composition(dtype, tol):
+    """The layer in bf16 / fp16: its four projections run on the tensor-core
+    kernel (msda_linear) forward, and for the input gradients backward; bias
+    gradients on msda_linear_bias_grad.  Reference: the fp64 composition, with
+    the layer's stored intermediates (value, offsets, logits, the operator's
+    output) rounded to the layer's dtype where the layer stores them."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from scale_deformable_attention_05_b300.module import MSDeformAttn
+    r = lambda a: _round(a, dtype)
     shapes = ((10, 12), (5, 6))
     C, M, L, P, N, Q = 128, 4, len(shapes), 4, 2, 9      # offsets 64 and logits 32 wide
-    wl = gen.random_workload(91, N, shapes, M, C // M, P, Q, dtype="bf16")
+    wl = gen.random_workload(91, N, shapes, M, C // M, P, Q,
+                             dtype="bf16" if dtype == torch.bfloat16 else "f16")
     K = wl.num_keys
     rng = np.random.default_rng(wl.seed)
-    layer = MSDeformAttn(C, L, M, P).cuda().to(torch.bfloat16)
+    layer = MSDeformAttn(C, L, M, P).cuda().to(dtype)
     params = {}
     with torch.no_grad():
         for name, p in layer.named_parameters():
@@ -131,31 +143,31 @@ def test_bf16_module_on_tensor_cores_matches_fp64_composition():
                 a = rng.normal(0.0, 2.0, tuple(p.shape))
             else:
                 a = rng.normal(0.0, 1.0 / np.sqrt(C), tuple(p.shape))
-            a = _bf16(a)
+            a = r(a)
             p.copy_(torch.from_numpy(a))
             params[name] = a
-    q, x = _bf16(rng.standard_normal((N, Q, C))), _bf16(rng.standard_normal((N, K, C)))
-    ref = _bf16(rng.uniform(0.1, 0.9, (N, Q, L, 2)))
-    g = _bf16(rng.standard_normal((N, Q, C)))
+    q, x = r(rng.standard_normal((N, Q, C))), r(rng.standard_normal((N, K, C)))
+    ref = r(rng.uniform(0.1, 0.9, (N, Q, L, 2)))
+    g = r(rng.standard_normal((N, Q, C)))
     sh = torch.tensor(shapes, dtype=torch.int64, device="cuda")
     lsi = torch.from_numpy(gen.level_start_index(shapes)).cuda()
-    tq, tx, tref = (torch.tensor(a, device="cuda", dtype=torch.bfloat16, requires_grad=True)
+    tq, tx, tref = (torch.tensor(a, device="cuda", dtype=dtype, requires_grad=True)
                     for a in (q, x, ref))
     out = layer(tq, tref, tx, sh, lsi)
-    out.backward(torch.from_numpy(g).to(device="cuda", dtype=torch.bfloat16))
+    out.backward(torch.from_numpy(g).to(device="cuda", dtype=dtype))
     torch.cuda.synchronize()
 
     Wv, bv, Wo, bo, Wa, ba, Wout, bout = (params[k] for k in (
         "value_proj.weight", "value_proj.bias", "sampling_offsets.weight", "sampling_offsets.bias",
         "attention_weights.weight", "attention_weights.bias", "output_proj.weight",
         "output_proj.bias"))
-    value = _bf16(x @ Wv.T + bv).reshape(N, K, M, C // M)
-    off = _bf16(q @ Wo.T + bo).reshape(N, Q, M, L, P, 2)
-    logits = _bf16(q @ Wa.T + ba).reshape(N, Q, M, L * P)
+    value = r(x @ Wv.T + bv).reshape(N, K, M, C // M)
+    off = r(q @ Wo.T + bo).reshape(N, Q, M, L, P, 2)
+    logits = r(q @ Wa.T + ba).reshape(N, Q, M, L * P)
     shp, lsin = np.array(shapes), gen.level_start_index(shapes)
-    y = _bf16(ofused.forward(value, shp, lsin, ref, off.astype(np.float32), logits))
+    y = r(ofused.forward(value, shp, lsin, ref, off.astype(np.float32), logits))
     want = y @ Wout.T + bout
-    assert_grad_close(host(out), want, "bf16", "output")
+    _assert_close(host(out), want, tol, "output")
     gy = g @ Wout
     gv, goff, glog, gref = ofused.backward(value, shp, lsin, ref, off.astype(np.float32), logits,
                                            gy)
@@ -173,7 +185,7 @@ def test_bf16_module_on_tensor_cores_matches_fp64_composition():
     got = {n: p.grad for n, p in layer.named_parameters()}
     got.update(query=tq.grad, input_flatten=tx.grad, reference_points=tref.grad)
     for name, ref_grad in grads.items():
-        assert_grad_close(host(got[name]), ref_grad, "bf16", name)
+        _assert_close(host(got[name]), ref_grad, tol, name)
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])

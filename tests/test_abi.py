@@ -237,3 +237,48 @@ def test_module_initial_state():
         MSDeformAttn(60, n_heads=8)                 # d_model not a multiple of n_heads
     with pytest.raises(ValueError):
         MSDeformAttn(64, n_levels=5, n_heads=8, n_points=16)   # L*P above the fused limit
+
+
+def test_projection_entry_points_reject_on_host():
+    """msda_linear, msda_linear_f32, msda_linear_wgrad_f32 and msda_linear_bias_grad
+    refuse unsupported widths, types, flags, missing or misaligned pointers and
+    short workspaces before their first CUDA call."""
+    lin = lambda x=A, w=A, b=None, y=A, rows=8, k=64, n=16, dtype=1: L.msda_linear(
+        x, w, b, y, rows, k, n, dtype, None)
+    assert lin(dtype=0) == 3                     # fp32 operands go to msda_linear_f32
+    assert lin(dtype=1 | 0x100) == 3             # no index flag here
+    assert lin(k=32) == 3 and lin(k=320) == 3    # K a multiple of 64, at most 256
+    assert lin(n=24) == 3 and lin(n=272) == 3    # N a multiple of 16, at most 256
+    assert lin(rows=-1) == 2
+    assert lin(rows=0, x=None) == 0              # nothing to do
+    assert lin(x=None) == 1 and lin(y=None) == 1
+    assert lin(x=A + 2) == 4 and lin(b=A + 8) == 4
+    f32 = lambda x=A, w=A, y=A, ws=A, wsb=1 << 20, rows=8, k=32, n=16: L.msda_linear_f32(
+        x, w, None, y, ws, wsb, rows, k, n, None)
+    assert f32(k=24) == 3 and f32(n=8) == 3
+    assert f32(ws=None) == 5
+    assert f32(wsb=B.msda_linear_workspace_bytes(8, 32, 16) - 16) == 5
+    assert f32(ws=A + 4) == 4 and f32(w=A + 4) == 4
+    assert B.msda_linear_workspace_bytes(8, 32, 16) == 8 * 32 * 16
+    assert B.msda_linear_workspace_bytes(8, 32, 16, B.MSDA_BF16) == 0
+    wg = lambda gy=A, x=A, gw=A, gb=A, rows=8, k=32, n=16, flags=1: L.msda_linear_wgrad_f32(
+        gy, x, gw, gb, rows, k, n, flags, None)
+    assert wg(flags=2) == 3 and wg(k=8) == 3 and wg(n=24) == 3
+    assert wg(gw=None) == 1 and wg(gy=None) == 1
+    assert wg(gw=A + 4) == 4 and wg(gb=A + 4) == 4
+    assert wg(rows=0) == 0                       # accumulating nothing: no launch
+    bg = lambda gy=A, gb=A, rows=8, n=16, dtype=1, flags=1: L.msda_linear_bias_grad(
+        gy, gb, rows, n, dtype, flags, None)
+    assert bg(dtype=3) == 3 and bg(n=12) == 3 and bg(n=8 * 257) == 3
+    assert bg(dtype=0, n=6) == 3                 # 4 fp32 columns per 16-byte vector
+    assert bg(gb=None) == 1 and bg(gy=None) == 1 and bg(gb=A + 4) == 4
+    assert bg(rows=0) == 0
+
+
+def test_projection_constants_match_header():
+    text = open(HEADER).read()
+    for name in ("MSDA_LINEAR_MAX_FEATURES", "MSDA_LINEAR_BIAS_HALF"):
+        m = re.search(r"#define\s+" + name + r"\s+(0x[0-9a-fA-F]+|\d+)", text)
+        assert m, name
+        assert int(m.group(1), 0) == getattr(B, name), name
+    assert B.MSDA_LINEAR_BIAS_BF16 == B.MSDA_LINEAR_BIAS_HALF

@@ -462,8 +462,9 @@ def _config(wl, args):
             "num_heads": wl.num_heads, "head_dim": wl.head_dim, "num_levels": wl.num_levels,
             "num_points": wl.num_points, "io_dtype": wl.dtype,
             "passes": "forward+backward",
-            "entry_points": ("msda_forward_fused / msda_backward_fused (2-d reference points, "
-                             "offsets, logits)" if getattr(args, "path", "plain") == "fused"
+            "entry_points": (f"msda_forward_fused / msda_backward_fused "
+                             f"({getattr(args, 'ref_dim', 2)}-d reference points, offsets, logits)"
+                             if getattr(args, "path", "plain") == "fused"
                              else "msda_forward / msda_backward"),
             "padding_mask": ("per-image top-left valid region, U[0.6, 1] of each side, image 0 "
                              "unpadded" if getattr(args, "padding_mask", False) else None),
@@ -656,7 +657,7 @@ def run_native(args, wl):
     dev = torch.device("cuda", local)
     fused = args.path == "fused"
     wl_r = rank_workload(wl, rank)
-    inp = gen.make_fused_inputs(wl_r, 2) if fused else gen.make_inputs(wl_r)
+    inp = gen.make_fused_inputs(wl_r, args.ref_dim) if fused else gen.make_inputs(wl_r)
     names = (("value", "reference_points", "sampling_offsets", "attention_logits",
               "grad_output") if fused else
              ("value", "sampling_locations", "attention_weights", "grad_output"))
@@ -776,9 +777,9 @@ def run_native(args, wl):
 
     hbm_gbs, peak_src = _peaks()
     if fused:
-        # reference points [bs, Q, L, 2] replace nothing; offsets and logits have the
-        # sizes of locations and weights
-        ref_bytes = wl.bs * wl.num_queries * wl.num_levels * 2 * wl.elem_bytes
+        # reference points [bs, Q, L, 2 or 4] replace nothing; offsets and logits have
+        # the sizes of locations and weights
+        ref_bytes = wl.bs * wl.num_queries * wl.num_levels * args.ref_dim * wl.elem_bytes
         if mask is not None:
             ref_bytes += wl.bs * wl.num_keys        # one mask byte per key
         fb = wl.compulsory_bytes(backward=False) + ref_bytes
@@ -808,7 +809,8 @@ def run_native(args, wl):
                 "peak": hbm_gbs, "unit": "GB/s", "frac": passes[dom]["gbs"] / hbm_gbs,
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": passes[dom]["compulsory_bytes"],
-                "traffic": (None if mask is not None else   # the committed captures run unmasked
+                # the committed captures run unmasked, with 2-d reference points
+                "traffic": (None if mask is not None or (fused and args.ref_dim != 2) else
                             _profiled_traffic(wl.name, kname + ("_fused" if fused else "")))}
 
     line = {
@@ -879,6 +881,8 @@ def main():
                     help="with --path fused: pass a key padding mask (padded image batch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-dim", type=int, default=2, choices=[2, 4],
+                    help="--path fused: 2-d reference points or 4-d reference boxes")
     ap.add_argument("--no-projection-compare", action="store_true",
                     help="--path layer: skip the cuBLAS-projection layer and the GEMM comparisons "
                          "(for launch lists of the library's own step)")

@@ -1013,6 +1013,26 @@ bool make_map(CUtensorMap* map, const void* ptr, int inner, int outer, int box_c
            CUDA_SUCCESS;
 }
 
+// A host action taken once per device (kernel attributes belong to the device's
+// context): run() calls f the first time it is called with a given device current.
+struct PerDevice {
+    std::mutex m;
+    bool done[64] = {};
+    template <typename F>
+    void run(F&& f) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+            f();
+            return;
+        }
+        std::lock_guard<std::mutex> lock(m);
+        if (!done[dev]) {
+            f();
+            done[dev] = true;
+        }
+    }
+};
+
 int sm_count() {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess)
@@ -1048,8 +1068,8 @@ extern "C" int msda_linear(const void* x, const void* w, const void* bias, void*
         return MSDA_ERR_CUDA;
     const Smem L = smem_layout(out_features, in_features);
     const size_t smem = (size_t)L.total + 1024;
-    static std::once_flag attr_once;
-    std::call_once(attr_once, [] {
+    static PerDevice attr_once;
+    attr_once.run([] {
         const int most =
             (int)(smem_layout(MSDA_LINEAR_MAX_FEATURES, MSDA_LINEAR_MAX_FEATURES).total + 1024);
         cudaFuncSetAttribute(linear_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
@@ -1107,8 +1127,8 @@ extern "C" int msda_linear_f32(const float* x, const float* w, const float* bias
         !make_map(&ym, y, out_features, rows, kChunk, kChunk, 128, true))
         return MSDA_ERR_CUDA;
     const SmemF L = smem_layout_f();
-    static std::once_flag attr_once;
-    std::call_once(attr_once, [] {
+    static PerDevice attr_once;
+    attr_once.run([] {
         cudaFuncSetAttribute(linear_f32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(smem_layout_f().total + 1024));
     });
@@ -1148,8 +1168,8 @@ extern "C" int msda_linear_wgrad_f32(const float* grad_y, const float* x, float*
     if (!make_map(&gym, grad_y, out_features, rows, kBM, kWgRows, 0, true) ||
         !make_map(&xm, x, in_features, rows, in_features, kWgRows, 0, true))
         return MSDA_ERR_CUDA;
-    static std::once_flag attr_once;
-    std::call_once(attr_once, [] {
+    static PerDevice attr_once;
+    attr_once.run([] {
         cudaFuncSetAttribute(linear_wgrad_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(smem_layout_wg().total + 1024));
     });

@@ -91,6 +91,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return false;
 }
 
+// Before a CTA leaves, its producer waits (bounded) for the TMA loads it issued
+// into the last `depth` stages of a ring (issues it - depth .. it - 1; stage s's
+// full barrier at full0 + 8 s), so that no copy lands in shared memory after the
+// CTA has gone, also when another role gave up on a wait.  After a normal run
+// every such phase has completed and each wait returns at once.
+__device__ __forceinline__ void drain_loads(uint32_t full0, uint32_t it, int depth) {
+    for (uint32_t j = it > (uint32_t)depth ? it - (uint32_t)depth : 0u; j < it; ++j)
+        mbar_wait(full0 + 8u * (j % (uint32_t)depth), (j / (uint32_t)depth) & 1u);
+}
+
+// The MMA issuer's last step: a commit tracking every tcgen05.mma it issued,
+// waited on (bounded), so that tensor memory is freed only after they finish.
+__device__ __forceinline__ void drain_mmas(uint32_t bar);
+
 // 2-d TMA tile load into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             uint32_t bar) {
@@ -151,6 +165,11 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
         : "memory");
 }
 
+__device__ __forceinline__ void drain_mmas(uint32_t bar) {
+    umma_commit(bar);
+    mbar_wait(bar, 0);
+}
+
 // 32 consecutive fp32 columns of this thread's tensor-memory lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
@@ -182,7 +201,7 @@ __host__ __device__ inline Smem smem_layout(int n, int k) {
     s.stage_out = s.x + (uint32_t)kStages * kBM * 128;       // 2 x 32 x 32 bf16 per epilogue warp
     s.bias = s.stage_out + (uint32_t)kEpiWarps * 2 * kChunk * kChunk * 2;   // 256 fp32
     s.bars = s.bias + MSDA_LINEAR_MAX_FEATURES * 4;
-    s.tmem_slot = s.bars + (1 + 2 * kStages + 4) * 8;
+    s.tmem_slot = s.bars + (1 + 2 * kStages + 4 + 1) * 8;
     s.total = s.tmem_slot + 8;
     return s;
 }
@@ -221,6 +240,7 @@ __device__ __forceinline__ void linear16_body(const CUtensorMap& x_map, const CU
     auto x_empty = [&](int s) { return bars + 8u * (1 + kStages + s); };
     auto acc_full = [&](int a) { return bars + 8u * (1 + 2 * kStages + a); };
     auto acc_empty = [&](int a) { return bars + 8u * (3 + 2 * kStages + a); };
+    const uint32_t mma_done = bars + 8u * (5 + 2 * kStages);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.tmem_slot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kblocks = k / kBK;
@@ -235,6 +255,7 @@ __device__ __forceinline__ void linear16_body(const CUtensorMap& x_map, const CU
     }
     if (threadIdx.x == 0) {
         mbar_init(w_full, 1);
+        mbar_init(mma_done, 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(x_full(s), 1);
             mbar_init(x_empty(s), 1);
@@ -269,6 +290,8 @@ __device__ __forceinline__ void linear16_body(const CUtensorMap& x_map, const CU
                     tma_load_2d(s_x + (uint32_t)s * kBM * 128, &x_map, kb * kBK, t * kBM,
                                 x_full(s));
                 }
+            mbar_wait(w_full, 0);
+            drain_loads(x_full(0), it, kStages);
         }
     } else if (warp == 1) {
         // ---- MMA issuer
@@ -300,6 +323,7 @@ __device__ __forceinline__ void linear16_body(const CUtensorMap& x_map, const CU
                 }
                 if (ok) umma_commit(acc_full(a));
             }
+            drain_mmas(mma_done);
         }
     } else {
         // ---- epilogue: warp w (2..9) reads lanes 32 * (w % 4) .. + 31 of the
@@ -472,7 +496,7 @@ __host__ __device__ inline SmemF smem_layout_f() {
     s.stage_out = s.stages + kStagesF * s.stage_bytes;         // 32 x 32 fp32 per epilogue warp
     s.bias = s.stage_out + (uint32_t)kEpiWarps * kChunk * kChunk * 4;
     s.bars = s.bias + MSDA_LINEAR_MAX_FEATURES * 4;
-    s.tmem_slot = s.bars + (3 * kStagesF + 4) * 8;
+    s.tmem_slot = s.bars + (3 * kStagesF + 4 + 1) * 8;
     s.total = s.tmem_slot + 8;
     return s;
 }
@@ -498,6 +522,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     auto x_empty = [&](int s) { return bars + 8u * (2 * kStagesF + s); }; // MMAs done with it
     auto acc_full = [&](int a) { return bars + 8u * (3 * kStagesF + a); };
     auto acc_empty = [&](int a) { return bars + 8u * (3 * kStagesF + 2 + a); };
+    const uint32_t mma_done = bars + 8u * (3 * kStagesF + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.tmem_slot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kblocks = k / kBKF;
@@ -512,6 +537,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (threadIdx.x == 0) {
+        mbar_init(mma_done, 1);
         for (int s = 0; s < kStagesF; ++s) {
             mbar_init(x_full(s), 1);
             mbar_init(x_split(s), kConvWarps);
@@ -549,6 +575,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                     tma_load_2d(wlo(s), &wlo_map, kb * kBKF, part * kPartF, x_full(s));
                 }
             }
+            drain_loads(x_full(0), it, kStagesF);
         }
     } else if (warp == 1) {
         // ---- MMA issuer: three TF32 products per K step of 8
@@ -585,6 +612,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 }
                 if (ok) umma_commit(acc_full(a));
             }
+            drain_mmas(mma_done);
         }
     } else if (warp >= 2 + kEpiWarps) {
         // ---- x split: converter warp c takes rows 32c .. 32c+31 of the block (2 KB),
@@ -720,7 +748,7 @@ __host__ __device__ inline SmemWg smem_layout_wg() {
     s.split = 0;                                                         // A_hi, A_lo, B_hi, B_lo
     s.raw = s.split + kWgSplit * s.split_bytes;
     s.bars = s.raw + kWgRaw * s.raw_bytes;
-    s.tmem_slot = s.bars + (2 * kWgRaw + 2 * kWgSplit + 1) * 8;
+    s.tmem_slot = s.bars + (2 * kWgRaw + 2 * kWgSplit + 2) * 8;
     s.total = s.tmem_slot + 8;
     return s;
 }
@@ -759,6 +787,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
     auto split_full = [&](int s) { return bars + 8u * (2 * kWgRaw + s); };
     auto split_empty = [&](int s) { return bars + 8u * (2 * kWgRaw + kWgSplit + s); };
     const uint32_t acc_full = bars + 8u * (2 * kWgRaw + 2 * kWgSplit);
+    const uint32_t mma_done = acc_full + 8u;
     auto raw_gy = [&](int s) { return base + L.raw + (size_t)s * L.raw_bytes; };
     auto raw_x = [&](int s) { return raw_gy(s) + (size_t)kWgRows * kBM * 4; };
     auto a_hi = [&](int s) { return base + L.split + (size_t)s * L.split_bytes; };
@@ -792,6 +821,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
             mbar_init(split_empty(s), 1);
         }
         mbar_init(acc_full, 1);
+        mbar_init(mma_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -804,6 +834,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
         // ---- producer: 16-row blocks of gy (columns m0 .. m0+127) and of x
         if (lane == 0) {
             const uint32_t bytes = (uint32_t)kWgRows * (kBM + k) * 4;
+            uint32_t issued = 0;
             bool ok = true;
             for (int it = 0; it < stages && ok; ++it) {
                 const int s = it % kWgRaw;
@@ -813,7 +844,9 @@ __global__ void __launch_bounds__(kWgThreads, 1)
                 const int r0 = r_begin + it * kWgRows;
                 tma_load_2d(smem_u32(raw_gy(s)), &gy_map, m0, r0, raw_full(s));
                 tma_load_2d(smem_u32(raw_x(s)), &x_map, 0, r0, raw_full(s));
+                issued = (uint32_t)it + 1;
             }
+            drain_loads(raw_full(0), issued, kWgRaw);
         }
     } else if (warp == 1) {
         // ---- MMA issuer: D[m, j] += three TF32 products over 8 rows at a time
@@ -839,6 +872,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
                 umma_commit(split_empty(s));
             }
             if (ok) umma_commit(acc_full);
+            drain_mmas(mma_done);
         }
     } else {
         // ---- converters (warps 2..9), then the epilogue

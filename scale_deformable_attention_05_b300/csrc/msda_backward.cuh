@@ -23,9 +23,54 @@
 // gradients, so the group writes eight consecutive samples' gradients at once.
 #pragma once
 
+#include <type_traits>
+
 #include "msda_device.cuh"
 
 namespace msda {
+
+// Corner dot products of 16-bit rows with sm_100's mixed-precision FMA (16-bit
+// multiplicands, fp32 addend and result): the value row stays packed instead of
+// being widened channel by channel.  A product of two bf16 (or fp16) values is
+// exact in fp32 and each fma rounds once, so the sums equal fmaf on the widened
+// values bit for bit, in the same order (low half, then high half).
+#ifndef MSDA_BWD_MIXED_DOT
+#define MSDA_BWD_MIXED_DOT 1
+#endif
+template <typename T>
+__device__ __forceinline__ float dot2_16(uint32_t a, uint32_t b, float d);
+template <>
+__device__ __forceinline__ float dot2_16<__nv_bfloat16>(uint32_t a, uint32_t b, float d) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+        : "+f"(d)
+        : "r"(a), "r"(b));
+    return d;
+}
+template <>
+__device__ __forceinline__ float dot2_16<__half>(uint32_t a, uint32_t b, float d) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+        : "+f"(d)
+        : "r"(a), "r"(b));
+    return d;
+}
+// Two fp32 values that are exact in T (a widened grad_output row), packed back.
+template <typename T>
+__device__ __forceinline__ uint32_t repack16x2(float lo, float hi) {
+    if constexpr (std::is_same<T, __half>::value) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        return pack_bf16x2(lo, hi);
+    }
+}
 
 // Bilinear weight of corner c and its derivatives along x_im and y_im.
 __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w, float& dwx,
@@ -309,6 +354,14 @@ __global__ void __launch_bounds__(BwdShape<kLanes, kVPL, kRef>::kWarps * 32,
         const int64_t head0 = ((int64_t)cur.b * num_keys * num_heads + cur.m) * head_dim;
         const char* vbase = reinterpret_cast<const char*>(value + head0);
         char* gvbase = reinterpret_cast<char*>(grad_value_f32 + head0);
+        constexpr bool kMixedDot = MSDA_BWD_MIXED_DOT != 0 && sizeof(T) == 2 && kVB == 8;
+        uint2 grp[kVPL];                  // the grad_output row packed (16-bit rows)
+        if constexpr (kMixedDot) {
+#pragma unroll
+            for (int k = 0; k < kVPL; ++k)
+                grp[k] = make_uint2(repack16x2<T>(gr[k][0], gr[k][1]),
+                                    repack16x2<T>(gr[k][2], gr[k][3]));
+        }
         const int q = cur.q0 + g;
         const int64_t row = ((int64_t)cur.b * num_queries + q) * num_heads + cur.m;
         const int nj = min(kSPG, LP - r0);
@@ -327,21 +380,33 @@ __global__ void __launch_bounds__(BwdShape<kLanes, kVPL, kRef>::kWarps * 32,
                 const float awc[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    float v[kVPL][V];
                     const char* p = row_ptr(vbase, keys[c], row_bytes);
-#pragma unroll
-                    for (int k = 0; k < kVPL; ++k) {
-                        const int vi = li + k * kLanes;
-#pragma unroll
-                        for (int e = 0; e < V; ++e) v[k][e] = 0.f;
-                        if (keys[c] >= 0 && vi < nvec && row_in_range(keys[c], num_keys))
-                            VIO::load(p + vi * kVB, v[k]);
-                    }
                     float d = 0.f;
+                    if constexpr (kMixedDot) {
 #pragma unroll
-                    for (int k = 0; k < kVPL; ++k)
+                        for (int k = 0; k < kVPL; ++k) {
+                            const int vi = li + k * kLanes;
+                            uint2 raw = make_uint2(0u, 0u);
+                            if (keys[c] >= 0 && vi < nvec && row_in_range(keys[c], num_keys))
+                                raw = __ldg(reinterpret_cast<const uint2*>(p + vi * kVB));
+                            d = dot2_16<T>(grp[k].x, raw.x, d);
+                            d = dot2_16<T>(grp[k].y, raw.y, d);
+                        }
+                    } else {
+                        float v[kVPL][V];
 #pragma unroll
-                        for (int e = 0; e < V; ++e) d = fmaf(gr[k][e], v[k][e], d);
+                        for (int k = 0; k < kVPL; ++k) {
+                            const int vi = li + k * kLanes;
+#pragma unroll
+                            for (int e = 0; e < V; ++e) v[k][e] = 0.f;
+                            if (keys[c] >= 0 && vi < nvec && row_in_range(keys[c], num_keys))
+                                VIO::load(p + vi * kVB, v[k]);
+                        }
+#pragma unroll
+                        for (int k = 0; k < kVPL; ++k)
+#pragma unroll
+                            for (int e = 0; e < V; ++e) d = fmaf(gr[k][e], v[k][e], d);
+                    }
                     dots[s8 * 4 + c] = d;
                     // merged duplicates carry red weight 0 and send nothing
                     if (keys[c] >= 0 && awc[c] != 0.f && row_in_range(keys[c], num_keys)) {

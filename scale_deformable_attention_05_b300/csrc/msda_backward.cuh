@@ -34,6 +34,12 @@ namespace msda {
 // being widened channel by channel.  A product of two bf16 (or fp16) values is
 // exact in fp32 and each fma rounds once, so the sums equal fmaf on the widened
 // values bit for bit, in the same order (low half, then high half).
+// Packed fp32 multiply (two channels per instruction) for the red payload of
+// 16-bit rows (with the mixed-precision dot products below: bf16 encoder
+// backward 906 -> 872 us); fp32 rows measured slower with it (430 -> 434 us).
+#ifndef MSDA_BWD_PACKED
+#define MSDA_BWD_PACKED 1
+#endif
 #ifndef MSDA_BWD_MIXED_DOT
 #define MSDA_BWD_MIXED_DOT 1
 #endif
@@ -355,6 +361,7 @@ __global__ void __launch_bounds__(BwdShape<kLanes, kVPL, kRef>::kWarps * 32,
         const char* vbase = reinterpret_cast<const char*>(value + head0);
         char* gvbase = reinterpret_cast<char*>(grad_value_f32 + head0);
         constexpr bool kMixedDot = MSDA_BWD_MIXED_DOT != 0 && sizeof(T) == 2 && kVB == 8;
+        constexpr bool kPackedMul = MSDA_BWD_PACKED != 0 && sizeof(T) == 2;
         uint2 grp[kVPL];                  // the grad_output row packed (16-bit rows)
         if constexpr (kMixedDot) {
 #pragma unroll
@@ -417,10 +424,22 @@ __global__ void __launch_bounds__(BwdShape<kLanes, kVPL, kRef>::kWarps * 32,
                             const int vi = li + k * kLanes;
                             if (vi < nvec) {
 #pragma unroll
-                                for (int e = 0; e < V; e += 4)
-                                    red_add_v4(gp + vi * V + e, awc[c] * gr[k][e],
-                                               awc[c] * gr[k][e + 1], awc[c] * gr[k][e + 2],
-                                               awc[c] * gr[k][e + 3]);
+                                for (int e = 0; e < V; e += 4) {
+                                    if constexpr (kPackedMul) {
+                                        // the payload two channels per instruction (sm_100
+                                        // packed fp32 multiply; each half is the scalar product)
+                                        const float2 a2 = make_float2(awc[c], awc[c]);
+                                        const float2 p01 = __fmul2_rn(
+                                            a2, make_float2(gr[k][e], gr[k][e + 1]));
+                                        const float2 p23 = __fmul2_rn(
+                                            a2, make_float2(gr[k][e + 2], gr[k][e + 3]));
+                                        red_add_v4(gp + vi * V + e, p01.x, p01.y, p23.x, p23.y);
+                                    } else {
+                                        red_add_v4(gp + vi * V + e, awc[c] * gr[k][e],
+                                                   awc[c] * gr[k][e + 1], awc[c] * gr[k][e + 2],
+                                                   awc[c] * gr[k][e + 3]);
+                                    }
+                                }
                             }
                         }
                     }

@@ -841,6 +841,8 @@ CEILING_PROBES = [
     ("red_shared_f32_conflict_free", 3, 0, 2), ("red_shared_f32_4way", 3, 1, 2),
     ("red_shared_f32_stride33", 3, 2, 2), ("rmw_shared_f32_conflict_free", 5, 0, 2),
     ("red_global_v4_l2", 4, 64 << 20, 2), ("red_global_v4_l2", 4, 64 << 20, 4),
+    ("gather_tma4_l2", 6, 64 << 20, 1), ("gather_tma4_l2", 6, 64 << 20, 2),
+    ("gather_tma4_hbm", 6, 512 << 20, 2),
 ]
 
 

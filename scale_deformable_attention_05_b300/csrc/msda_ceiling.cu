@@ -14,6 +14,11 @@
 //   kRedGlobalV4  red.global.add.v4.f32, 8 lanes per row (the global scatter)
 //   kRmwShared    plain load + add + store in shared memory (no atomicity),
 //                 for comparison with kRedShared
+//   kGatherTma4   TMA tile::gather4 (four random rows per copy, one row-high
+//                 box) into shared-memory rings, each slot then read once
+//                 with 128-bit shared loads: 8 producer / consumer warp pairs
+//                 per CTA, 8 slots of 512 bytes each (the copy engine as a
+//                 gather path that bypasses the L1 tags)
 // `param` selects the region: for the global probes its size in bytes (a
 // region that fits L1 measures L1 hits, one of tens of MB measures L2 hits);
 // for kRedShared / kRmwShared the bank pattern of the four rows an
@@ -23,6 +28,7 @@
 //
 // Not part of the operator's ABI: a measurement tool, allocating its own
 // buffers.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -36,6 +42,7 @@ enum Probe {
     kRedShared = 3,
     kRedGlobalV4 = 4,
     kRmwShared = 5,
+    kGatherTma4 = 6,
 };
 
 constexpr int kThreads = 512;            // 16 warps per CTA
@@ -199,6 +206,122 @@ __global__ void __launch_bounds__(kThreads) scatter_red_global(float* __restrict
     if (threadIdx.x == 0) stamps[blockIdx.x] = Stamp{c0, clock64(), t0, global_ns()};
 }
 
+// kGatherTma4: warps 0..7 produce (lane 0 issues the copies of its ring), warps
+// 8..15 consume.  Every wait is bounded; a wait that runs out sets `err`.
+constexpr int kTmaPairs = 8, kTmaSlots = 8;
+__device__ unsigned g_tma_err;
+
+__device__ __forceinline__ bool tma_wait(uint32_t bar, uint32_t parity) {
+    for (int i = 0; i < (1 << 22); ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.b32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    atomicOr(&g_tma_err, 1u);
+    return false;
+}
+
+__global__ void __launch_bounds__(kThreads) gather_tma4(const __grid_constant__ CUtensorMap map,
+                                                        uint32_t row_mask, int iters,
+                                                        float* __restrict__ sink,
+                                                        Stamp* __restrict__ stamps) {
+    __shared__ __align__(1024) float ring[kTmaPairs][kTmaSlots][128];
+    __shared__ __align__(8) unsigned long long full[kTmaPairs][kTmaSlots];
+    __shared__ __align__(8) unsigned long long empty[kTmaPairs][kTmaSlots];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pair = warp % kTmaPairs;
+    if (threadIdx.x == 0) {
+        for (int p = 0; p < kTmaPairs; ++p)
+            for (int s = 0; s < kTmaSlots; ++s) {
+                asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[p][s])));
+                asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&empty[p][s])));
+            }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    long long c0 = clock64();
+    unsigned long long t0 = global_ns();
+    float acc = 0.f;
+    if (warp < kTmaPairs) {
+        if (lane == 0) {
+            uint32_t x = lcg(blockIdx.x * 977u + (uint32_t)pair * 131u + 1u);
+            int it = 0;
+            for (; it < iters; ++it) {
+                const int s = it % kTmaSlots;
+                if (!tma_wait(smem_addr(&empty[pair][s]), ((it / kTmaSlots) & 1) ^ 1)) break;
+                const uint32_t fb = smem_addr(&full[pair][s]);
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                             "r"(512)
+                             : "memory");
+                int r[4];
+                for (int k = 0; k < 4; ++k) {
+                    x = lcg(x);
+                    r[k] = (int)((x >> 7) & row_mask);
+                }
+                asm volatile(
+                    "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::"
+                    "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(
+                        smem_addr(ring[pair][s])),
+                    "l"(reinterpret_cast<uint64_t>(&map)), "r"(0), "r"(r[0]), "r"(r[1]), "r"(r[2]),
+                    "r"(r[3]), "r"(fb)
+                    : "memory");
+            }
+            // wait for the copies still in flight before the CTA may leave
+            for (int j = it > kTmaSlots ? it - kTmaSlots : 0; j < it; ++j)
+                tma_wait(smem_addr(&full[pair][j % kTmaSlots]), (j / kTmaSlots) & 1);
+        }
+    } else {
+        for (int it = 0; it < iters; ++it) {
+            const int s = it % kTmaSlots;
+            if (!tma_wait(smem_addr(&full[pair][s]), (it / kTmaSlots) & 1)) break;
+            const float4 v = reinterpret_cast<const float4*>(ring[pair][s])[lane];
+            acc += v.x + v.y + v.z + v.w;
+            __syncwarp();
+            if (lane == 0)
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(
+                                 smem_addr(&empty[pair][s]))
+                             : "memory");
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        stamps[0].clk0 = c0;
+        stamps[0].clk1 = clock64();
+        stamps[0].ns0 = t0;
+        stamps[0].ns1 = global_ns();
+    }
+    sink[blockIdx.x * kThreads + threadIdx.x] = acc;
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// A [rows, 32] fp32 map with a one-row box (the gather4 form).
+bool row_map(CUtensorMap* map, float* region, size_t rows) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+    const cuuint64_t dims[2] = {32, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {32, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    return reinterpret_cast<EncodeTiled>(fn)(
+               map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, region, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 __global__ void fill_kernel(float* p, size_t n) {
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (size_t)gridDim.x * blockDim.x)
@@ -224,13 +347,11 @@ extern "C" __attribute__((visibility("default"))) int msda_ceiling_run(int probe
     float* sink = nullptr;
     Stamp* stamps = nullptr;
     float* region = nullptr;
-    size_t region_bytes = (probe == kGatherLdg16 || probe == kGatherLdg32 || probe == kRedGlobalV4)
-                              ? (size_t)param
-                              : 0;
+    const bool global_probe = probe == kGatherLdg16 || probe == kGatherLdg32 ||
+                              probe == kRedGlobalV4 || probe == kGatherTma4;
+    size_t region_bytes = global_probe ? (size_t)param : 0;
     if (region_bytes < 128 || (region_bytes & (region_bytes - 1)) != 0) region_bytes = 0;
-    const bool global_probe =
-        probe == kGatherLdg16 || probe == kGatherLdg32 || probe == kRedGlobalV4;
-    if (probe < kGatherLdg16 || probe > kRmwShared || iters < 1 || ctas_per_sm < 1 ||
+    if (probe < kGatherLdg16 || probe > kGatherTma4 || iters < 1 || ctas_per_sm < 1 ||
         (global_probe && region_bytes == 0))
         return (int)cudaErrorInvalidValue;
     if ((e = cudaMalloc(&sink, (size_t)grid * kThreads * sizeof(float))) != cudaSuccess) return e;
@@ -240,6 +361,12 @@ extern "C" __attribute__((visibility("default"))) int msda_ceiling_run(int probe
         fill_kernel<<<sms * 4, 256>>>(region, region_bytes / 4);
     }
     const uint32_t row_mask = region_bytes ? (uint32_t)(region_bytes / 128 - 1) : 0;
+    CUtensorMap map;
+    if (probe == kGatherTma4) {
+        if (!row_map(&map, region, region_bytes / 128)) return (int)cudaErrorInvalidValue;
+        const unsigned zero = 0;
+        if ((e = cudaMemcpyToSymbol(g_tma_err, &zero, sizeof(zero))) != cudaSuccess) return e;
+    }
     const size_t lds_bytes = (size_t)kSharedRows * 128;
     const size_t win_bytes = (size_t)4 * (kSubRows * 32 + 4) * sizeof(float);
     auto launch = [&]() {
@@ -261,6 +388,9 @@ extern "C" __attribute__((visibility("default"))) int msda_ceiling_run(int probe
                 break;
             case kRedGlobalV4:
                 scatter_red_global<<<grid, kThreads>>>(region, row_mask, iters, stamps);
+                break;
+            case kGatherTma4:
+                gather_tma4<<<grid, kThreads>>>(map, row_mask, iters, sink, stamps);
                 break;
             default: break;
         }
@@ -288,7 +418,14 @@ extern "C" __attribute__((visibility("default"))) int msda_ceiling_run(int probe
     Stamp s0{};
     if (e == cudaSuccess) e = cudaMemcpy(&s0, stamps, sizeof(Stamp), cudaMemcpyDeviceToHost);
     const int lanes_per_row = probe == kGatherLdg32 ? 4 : 8;
-    const double rows = (double)grid * kThreads / lanes_per_row * 4.0 * iters;
+    const double rows = probe == kGatherTma4
+                            ? (double)grid * kTmaPairs * 4.0 * iters
+                            : (double)grid * kThreads / lanes_per_row * 4.0 * iters;
+    if (e == cudaSuccess && probe == kGatherTma4) {
+        unsigned err = 0;
+        e = cudaMemcpyFromSymbol(&err, g_tma_err, sizeof(err));
+        if (e == cudaSuccess && err != 0) e = cudaErrorLaunchTimeout;   // a bounded wait ran out
+    }
     const double mhz = s0.ns1 > s0.ns0 ? (double)(s0.clk1 - s0.clk0) / (double)(s0.ns1 - s0.ns0) * 1e3
                                        : 0.0;
     out[0] = (ms > 0 && mhz > 0) ? rows / ((double)ms * 1e-3 * mhz * 1e6 * sms) : 0.0;

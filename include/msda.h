@@ -289,8 +289,13 @@ MSDA_API int msda_backward_noalloc(const void* value, const void* spatial_shapes
  * out_features a multiple of 16, both at most MSDA_LINEAR_MAX_FEATURES (else
  * MSDA_ERR_UNSUPPORTED); every pointer 16-byte aligned (MSDA_ERR_ALIGN).
  * One kernel launch (one persistent CTA per SM: TMA loads, tcgen05.mma into
- * two alternating accumulators in tensor memory, TMA stores).  A device-side wait that runs out of its iteration limit
- * stops the kernel and raises the error word msda_last_device_error() reads.
+ * two alternating accumulators in tensor memory, TMA stores).  A device-side
+ * wait that runs out of its iteration limit stops the kernel and raises the
+ * error word msda_last_device_error() reads.  The first call of each
+ * projection entry point on a device raises its kernel's shared-memory limit
+ * (cudaFuncSetAttribute): make it before capturing a CUDA graph of later calls.
+ * The entry points allocate nothing and never synchronise, so later calls can
+ * be captured.
  */
 #define MSDA_LINEAR_MAX_FEATURES 256
 #define MSDA_LINEAR_BIAS_HALF 0x200

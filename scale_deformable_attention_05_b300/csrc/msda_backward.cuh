@@ -89,22 +89,33 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
 }
 
 // CTA shape of backward_kernel.  The plain path with lane groups of at most 8
-// lanes and one vector per lane (head_dim <= 32) runs 3 resident CTAs of 8
-// warps per SM (80 registers per thread; measured against one CTA of 16 warps
-// with 128 registers: encoder fp32 452 -> 440 us, bf16 1073 -> 925 us, fp16
-// 1034 -> 918 us); wider rows and the fused entry points, whose state does not
-// fit 80 registers, keep one CTA of 16 warps.
+// lanes and one vector per lane (head_dim <= 32) runs resident CTAs of 8 warps,
+// 3 per SM for fp32 rows (80 registers per thread) and 4 for 16-bit rows (64
+// registers), and loads each round's inputs at the start of that round rather
+// than one round ahead, which frees the registers the prefetch held.  Measured
+// (kernel-only events, against the previous 3 CTAs with the prefetch): encoder
+// fp32 440 -> 417 us, bf16 877 -> 825 us, fp16 879 -> 827 us, decoder 38.9 ->
+// 34.8 us; one CTA of 16 warps with 128 registers had been slower still (fp32
+// 452 us, bf16 1073 us).  Wider rows and the fused entry points, whose state
+// does not fit these budgets, keep one CTA of 16 warps and the prefetch.
 #ifndef MSDA_BWD_NARROW_WARPS
 #define MSDA_BWD_NARROW_WARPS 8
 #endif
 #ifndef MSDA_BWD_NARROW_BLOCKS
 #define MSDA_BWD_NARROW_BLOCKS 3
 #endif
-template <int kLanes, int kVPL, int kRef>
+#ifndef MSDA_BWD_NARROW_BLOCKS16
+#define MSDA_BWD_NARROW_BLOCKS16 4
+#endif
+#ifndef MSDA_BWD_NARROW_PREFETCH
+#define MSDA_BWD_NARROW_PREFETCH 0
+#endif
+template <typename T, int kLanes, int kVPL, int kRef>
 struct BwdShape {
     static constexpr bool kNarrow = kLanes <= 8 && kVPL == 1 && kRef == 0;
     static constexpr int kWarps = kNarrow ? MSDA_BWD_NARROW_WARPS : MSDA_BWD_WARPS;
-    static constexpr int kMinBlocks = kNarrow ? MSDA_BWD_NARROW_BLOCKS : 1;
+    static constexpr int kMinBlocks =
+        !kNarrow ? 1 : sizeof(T) == 4 ? MSDA_BWD_NARROW_BLOCKS : MSDA_BWD_NARROW_BLOCKS16;
 };
 // backward_merge_kernel: one CTA of MSDA_MERGE_WARPS warps per SM (its 1 KB
 // rows measured 10% slower with 24 warps of 80 registers).
@@ -113,7 +124,8 @@ struct BwdShape {
 #endif
 
 // Locations, weights and grad_output rows of the next round loaded during this
-// round's gathers (1), or at the start of their round (0, fewer live registers).
+// round's gathers (1), or at the start of their round (0, fewer live registers);
+// the narrow shapes above use MSDA_BWD_NARROW_PREFETCH instead.
 #ifndef MSDA_BWD_PREFETCH
 #define MSDA_BWD_PREFETCH 1
 #endif
@@ -240,8 +252,8 @@ __device__ __forceinline__ void load_grad_row(float (&gr)[kVPL][VecIO<T, kVB>::k
 // each covering half of every 32-byte sector of the row; the bf16 encoder
 // backward measured 1298 us that way against 1207 us with 8-byte vectors.)
 template <typename T, int kLanes, int kVPL, int kRef, int kVB>
-__global__ void __launch_bounds__(BwdShape<kLanes, kVPL, kRef>::kWarps * 32,
-                                  BwdShape<kLanes, kVPL, kRef>::kMinBlocks)
+__global__ void __launch_bounds__(BwdShape<T, kLanes, kVPL, kRef>::kWarps * 32,
+                                  BwdShape<T, kLanes, kVPL, kRef>::kMinBlocks)
     backward_kernel(const T* __restrict__ value, const void* __restrict__ spatial_shapes,
                     const void* __restrict__ level_start_index, int idx32, const T* __restrict__ loc,
                     const T* __restrict__ attn, const T* __restrict__ grad_out,
@@ -251,7 +263,7 @@ __global__ void __launch_bounds__(BwdShape<kLanes, kVPL, kRef>::kWarps * 32,
                     int num_tiles, int tiles_per_cta, const T* __restrict__ ref,
                     const unsigned char* __restrict__ mask, float* __restrict__ grad_ref) {
     constexpr bool kPrep = kRef != 0;
-    constexpr int kWarps = BwdShape<kLanes, kVPL, kRef>::kWarps;
+    constexpr int kWarps = BwdShape<T, kLanes, kVPL, kRef>::kWarps;
     using Geom = TileGeom<kLanes>;
     using VIO = VecIO<T, kVB>;
     constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
@@ -306,7 +318,10 @@ __global__ void __launch_bounds__(BwdShape<kLanes, kVPL, kRef>::kWarps * 32,
     it.stride = kWarps;
     if (!it.valid()) return;
 
-    constexpr bool kPrefetch = MSDA_BWD_PREFETCH != 0 || kPrep;
+    constexpr bool kPrefetch =
+        (BwdShape<T, kLanes, kVPL, kRef>::kNarrow ? MSDA_BWD_NARROW_PREFETCH != 0
+                                                   : MSDA_BWD_PREFETCH != 0) ||
+        kPrep;
     SampleFetch f;
     PrepFetch pf;
     TileCoord tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);

@@ -180,7 +180,7 @@ cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv
                               void* grad_loc, void* grad_attn, cudaStream_t st,
                               float* grad_ref = nullptr) {
     auto kernel = backward_kernel<T, kLanes, kVPL, kRef, kVB>;
-    constexpr int kWarps = BwdShape<kLanes, kVPL, kRef>::kWarps;
+    constexpr int kWarps = BwdShape<T, kLanes, kVPL, kRef>::kWarps;
     constexpr int kThreads = kWarps * 32;
     const TileGrid tg =
         tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), kWarps,

@@ -88,16 +88,18 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
     dwy = cy ? wx : -wx;
 }
 
-// CTA shape of backward_kernel.  The plain path with lane groups of at most 8
-// lanes and one vector per lane (head_dim <= 32) runs resident CTAs of 8 warps,
-// 3 per SM for fp32 rows (80 registers per thread) and 4 for 16-bit rows (64
-// registers), and loads each round's inputs at the start of that round rather
-// than one round ahead, which frees the registers the prefetch held.  Measured
-// (kernel-only events, against the previous 3 CTAs with the prefetch): encoder
-// fp32 440 -> 417 us, bf16 877 -> 825 us, fp16 879 -> 827 us, decoder 38.9 ->
-// 34.8 us; one CTA of 16 warps with 128 registers had been slower still (fp32
-// 452 us, bf16 1073 us).  Wider rows and the fused entry points, whose state
-// does not fit these budgets, keep one CTA of 16 warps and the prefetch.
+// CTA shape of backward_kernel.  Lane groups of at most 8 lanes with one vector
+// per lane (head_dim <= 32) run resident CTAs of 8 warps, 3 per SM for fp32
+// rows (80 registers per thread) and 4 for 16-bit rows (64 registers), and load
+// each round's inputs at the start of that round rather than one round ahead,
+// which frees the registers the prefetch held.  Measured (kernel-only events,
+// against 3 CTAs with the prefetch on the plain path and one CTA of 16 warps
+// with it on the fused one): plain encoder fp32 440 -> 417 us, bf16 877 -> 825
+// us, fp16 879 -> 827 us, decoder 38.9 -> 34.8 us; fused encoder 2-d 563 -> 528
+// us, 4-d 576 -> 534 us, bf16 1300 -> 1090 us (the fused decoder 36 -> 39 us);
+// one CTA of 16 warps with 128 registers had been slower still on the plain
+// path (fp32 452 us, bf16 1073 us).  Wider rows keep one CTA of 16 warps and
+// the prefetch.
 #ifndef MSDA_BWD_NARROW_WARPS
 #define MSDA_BWD_NARROW_WARPS 8
 #endif
@@ -112,7 +114,7 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
 #endif
 template <typename T, int kLanes, int kVPL, int kRef>
 struct BwdShape {
-    static constexpr bool kNarrow = kLanes <= 8 && kVPL == 1 && kRef == 0;
+    static constexpr bool kNarrow = kLanes <= 8 && kVPL == 1;
     static constexpr int kWarps = kNarrow ? MSDA_BWD_NARROW_WARPS : MSDA_BWD_WARPS;
     static constexpr int kMinBlocks =
         !kNarrow ? 1 : sizeof(T) == 4 ? MSDA_BWD_NARROW_BLOCKS : MSDA_BWD_NARROW_BLOCKS16;
@@ -318,10 +320,9 @@ __global__ void __launch_bounds__(BwdShape<T, kLanes, kVPL, kRef>::kWarps * 32,
     it.stride = kWarps;
     if (!it.valid()) return;
 
-    constexpr bool kPrefetch =
-        (BwdShape<T, kLanes, kVPL, kRef>::kNarrow ? MSDA_BWD_NARROW_PREFETCH != 0
-                                                   : MSDA_BWD_PREFETCH != 0) ||
-        kPrep;
+    constexpr bool kPrefetch = BwdShape<T, kLanes, kVPL, kRef>::kNarrow
+                                   ? MSDA_BWD_NARROW_PREFETCH != 0
+                                   : MSDA_BWD_PREFETCH != 0 || kPrep;
     SampleFetch f;
     PrepFetch pf;
     TileCoord tc = tile_coord(it.t, num_heads, num_qtiles, kGroups);

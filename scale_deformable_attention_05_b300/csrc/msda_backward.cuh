@@ -89,10 +89,12 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
 }
 
 // CTA shape of backward_kernel.  Lane groups of at most 8 lanes with one vector
-// per lane (head_dim <= 32) run resident CTAs of 8 warps, 3 per SM for fp32
-// rows (80 registers per thread) and 4 for 16-bit rows (64 registers), and load
+// per lane (head_dim <= 32) run resident CTAs of 4 warps, 6 per SM for fp32
+// rows (80 registers per thread) and 8 for 16-bit rows (64 registers), and load
 // each round's inputs at the start of that round rather than one round ahead,
-// which frees the registers the prefetch held.  Measured (kernel-only events,
+// which frees the registers the prefetch held.  (CTAs of 4 warps instead of 8
+// at the same warps per SM: fp32 encoder 416 -> 413 us, decoder 34.8 -> 32.7
+// us, bf16 unchanged.)  Measured (kernel-only events,
 // against 3 CTAs with the prefetch on the plain path and one CTA of 16 warps
 // with it on the fused one): plain encoder fp32 440 -> 417 us, bf16 877 -> 825
 // us, fp16 879 -> 827 us, decoder 38.9 -> 34.8 us; fused encoder 2-d 563 -> 528
@@ -101,13 +103,13 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
 // path (fp32 452 us, bf16 1073 us).  Wider rows keep one CTA of 16 warps and
 // the prefetch.
 #ifndef MSDA_BWD_NARROW_WARPS
-#define MSDA_BWD_NARROW_WARPS 8
+#define MSDA_BWD_NARROW_WARPS 4
 #endif
 #ifndef MSDA_BWD_NARROW_BLOCKS
-#define MSDA_BWD_NARROW_BLOCKS 3
+#define MSDA_BWD_NARROW_BLOCKS 6
 #endif
 #ifndef MSDA_BWD_NARROW_BLOCKS16
-#define MSDA_BWD_NARROW_BLOCKS16 4
+#define MSDA_BWD_NARROW_BLOCKS16 8
 #endif
 #ifndef MSDA_BWD_NARROW_PREFETCH
 #define MSDA_BWD_NARROW_PREFETCH 0

@@ -29,9 +29,12 @@
 
 namespace msda {
 
-// Warps per CTA of the forward and backward kernels.
+// Warps per CTA of the forward and backward kernels.  The forward runs CTAs of
+// 4 warps (the same resident warps per SM as 8-warp CTAs: encoder fp32 forward
+// 163.8 -> 161.8 us, bf16 286.7 -> 284.7 us, kernel-only; 16-warp CTAs were
+// slower, 167.9 / 340.0 us).
 #ifndef MSDA_FWD_WARPS
-#define MSDA_FWD_WARPS 8
+#define MSDA_FWD_WARPS 4
 #endif
 #ifndef MSDA_BWD_WARPS
 #define MSDA_BWD_WARPS 16

@@ -121,10 +121,12 @@ struct BwdShape {
     static constexpr int kMinBlocks =
         !kNarrow ? 1 : sizeof(T) == 4 ? MSDA_BWD_NARROW_BLOCKS : MSDA_BWD_NARROW_BLOCKS16;
 };
-// backward_merge_kernel: one CTA of MSDA_MERGE_WARPS warps per SM (its 1 KB
-// rows measured 10% slower with 24 warps of 80 registers).
+// backward_merge_kernel: CTAs of MSDA_MERGE_WARPS warps (its 1 KB rows
+// measured 10% slower with 24 warps of 80 registers; CTAs of 8 warps instead of
+// one of 16, the same warps per SM: envelope backward 2481 -> 2417 us,
+// kernel-only).
 #ifndef MSDA_MERGE_WARPS
-#define MSDA_MERGE_WARPS 16
+#define MSDA_MERGE_WARPS 8
 #endif
 
 // Locations, weights and grad_output rows of the next round loaded during this

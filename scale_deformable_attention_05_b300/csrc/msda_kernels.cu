@@ -104,19 +104,23 @@ int64_t l2_bytes() {
 }
 
 // Waves per launch from the working set: value (and, in the backward, its fp32
-// gradient) over a target share of L2, rounded up to a power of two.  The CTAs
-// resident at a time then cover that share of the (b, m)-ordered tiles, whose
-// value and grad_value slices stay in L2 against the streamed inputs and
-// outputs.  Targets from a sweep of 1..32 waves (CUDA events): the backward
-// wants ~0.6 L2 of slices live (fp32 encoder 1-2 waves, bf16 encoder 2-4,
-// D = 256 envelope 8-16: -27%), the forward ~L2 / 8 (fp32 encoder flat, bf16
-// encoder 4-16: -6%, envelope 32: -30%).
+// gradient) over a target share of L2, rounded up to a power of two and capped.
+// The CTAs resident at a time then cover that share of the (b, m)-ordered
+// tiles, whose value and grad_value slices stay in L2 against the streamed
+// inputs and outputs, and the shorter tile ranges of more waves even out the
+// CTAs' finishing times.  Targets from sweeps of 1..64 waves (kernel-only CUDA
+// events) with the current CTA shapes (4-warp CTAs): the backward wants ~L2 / 13
+// of slices live, at most 16 waves (fp32 encoder 2 -> 16 waves: 412 -> 395 us,
+// bf16 822 -> 766, fp16 825 -> 767; 32 and 64 slower; D = 256 envelope best at
+// 8-16), the forward ~L2 / 32, at most 32 waves (fp32 encoder 4 -> 16: 162 ->
+// 158 us, bf16 285 -> 274; envelope best at 32).
 int persistent_waves(const Problem& pb, int elem_bytes, bool backward) {
     if (MSDA_PERSISTENT_WAVES > 0) return MSDA_PERSISTENT_WAVES;
     const double ws = (double)pb.bs * pb.K * pb.M * pb.D * (elem_bytes + (backward ? 4 : 0));
-    const double target = (double)l2_bytes() * (backward ? 0.6 : 0.125);
+    const double target = (double)l2_bytes() * (backward ? 0.075 : 1.0 / 32.0);
+    const int cap = backward ? 16 : 32;
     int w = 1;
-    while (w < 64 && w * target < ws) w <<= 1;
+    while (w < cap && w * target < ws) w <<= 1;
     return w;
 }
 

@@ -40,6 +40,12 @@ namespace msda {
 #ifndef MSDA_BWD_PACKED
 #define MSDA_BWD_PACKED 1
 #endif
+// 16-bit rows send each corner's reds as predicated instructions instead of
+// branching around them (bf16 encoder backward 768 -> 747 us, fp16 768 -> 750
+// us); fp32 rows keep the branch (393 -> 397 us predicated).
+#ifndef MSDA_BWD_PRED_RED
+#define MSDA_BWD_PRED_RED 1
+#endif
 #ifndef MSDA_BWD_MIXED_DOT
 #define MSDA_BWD_MIXED_DOT 1
 #endif
@@ -111,6 +117,12 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
 #ifndef MSDA_BWD_NARROW_BLOCKS16
 #define MSDA_BWD_NARROW_BLOCKS16 8
 #endif
+// The fused entry points' 16-bit backward holds the softmax-Jacobian and offset
+// state as well: at 8 CTAs (64 registers) it spilled 176 bytes per thread; 7 CTAs
+// (72 registers) measured best (bf16 encoder 953 -> 898 us; 6 CTAs 939 us).
+#ifndef MSDA_BWD_FUSED16_BLOCKS
+#define MSDA_BWD_FUSED16_BLOCKS 7
+#endif
 #ifndef MSDA_BWD_NARROW_PREFETCH
 #define MSDA_BWD_NARROW_PREFETCH 0
 #endif
@@ -118,8 +130,10 @@ template <typename T, int kLanes, int kVPL, int kRef>
 struct BwdShape {
     static constexpr bool kNarrow = kLanes <= 8 && kVPL == 1;
     static constexpr int kWarps = kNarrow ? MSDA_BWD_NARROW_WARPS : MSDA_BWD_WARPS;
-    static constexpr int kMinBlocks =
-        !kNarrow ? 1 : sizeof(T) == 4 ? MSDA_BWD_NARROW_BLOCKS : MSDA_BWD_NARROW_BLOCKS16;
+    static constexpr int kMinBlocks = !kNarrow           ? 1
+                                      : sizeof(T) == 4   ? MSDA_BWD_NARROW_BLOCKS
+                                      : kRef != 0        ? MSDA_BWD_FUSED16_BLOCKS
+                                                         : MSDA_BWD_NARROW_BLOCKS16;
 };
 // backward_merge_kernel: CTAs of MSDA_MERGE_WARPS warps (its 1 KB rows
 // measured 10% slower with 24 warps of 80 registers; CTAs of 8 warps instead of
@@ -206,12 +220,16 @@ __device__ __forceinline__ void backward_records(int4* wk, float4* waw, float4* 
             const int k = cc.key[t];
             float A = cc.w[t];
             bool lead = k >= 0;
-            for (int i = 1; i < dedup; ++i) {
-                const int kp = __shfl_xor_sync(0xffffffffu, k, i);
-                const float wp = __shfl_xor_sync(0xffffffffu, cc.w[t], i);
-                if (kp == k) {
-                    if ((lane ^ i) < lane) lead = false;
-                    else A += wp;
+            // peers at xor distance 1..3 within the segment (dedup is warp-uniform);
+            // selects instead of a branch on each match
+#pragma unroll
+            for (int i = 1; i < 4; ++i) {
+                if (i < dedup) {
+                    const int kp = __shfl_xor_sync(0xffffffffu, k, i);
+                    const float wp = __shfl_xor_sync(0xffffffffu, cc.w[t], i);
+                    const bool same = kp == k, lower = (lane ^ i) < lane;
+                    lead = lead && !(same && lower);
+                    A += (same && !lower) ? wp : 0.f;
                 }
             }
             // class t sits at corner ((t>>1)^py, (t&1)^px)
@@ -382,6 +400,7 @@ __global__ void __launch_bounds__(BwdShape<T, kLanes, kVPL, kRef>::kWarps * 32,
         char* gvbase = reinterpret_cast<char*>(grad_value_f32 + head0);
         constexpr bool kMixedDot = MSDA_BWD_MIXED_DOT != 0 && sizeof(T) == 2 && kVB == 8;
         constexpr bool kPackedMul = MSDA_BWD_PACKED != 0 && sizeof(T) == 2;
+        constexpr bool kPredRed = MSDA_BWD_PRED_RED != 0 && sizeof(T) == 2;
         uint2 grp[kVPL];                  // the grad_output row packed (16-bit rows)
         if constexpr (kMixedDot) {
 #pragma unroll
@@ -435,8 +454,36 @@ __global__ void __launch_bounds__(BwdShape<T, kLanes, kVPL, kRef>::kWarps * 32,
                             for (int e = 0; e < V; ++e) d = fmaf(gr[k][e], v[k][e], d);
                     }
                     dots[s8 * 4 + c] = d;
-                    // merged duplicates carry red weight 0 and send nothing
-                    if (keys[c] >= 0 && awc[c] != 0.f && row_in_range(keys[c], num_keys)) {
+                    // merged duplicates and corners off the map carry red weight 0
+                    // (the records zero both), so the weight alone decides the red
+                    // (one test fewer per corner: fp32 encoder 397 -> 393 us)
+                    if constexpr (kPredRed) {
+                        // the address of a corner that sends nothing is formed, never used
+                        const bool send = awc[c] != 0.f && row_in_range(keys[c], num_keys);
+                        float* gp = reinterpret_cast<float*>(
+                            gvbase + (size_t)(unsigned)keys[c] * row_bytes32);
+#pragma unroll
+                        for (int k = 0; k < kVPL; ++k) {
+                            const int vi = li + k * kLanes;
+                            const bool ok = send && vi < nvec;
+#pragma unroll
+                            for (int e = 0; e < V; e += 4) {
+                                if constexpr (kPackedMul) {
+                                    const float2 a2 = make_float2(awc[c], awc[c]);
+                                    const float2 p01 =
+                                        __fmul2_rn(a2, make_float2(gr[k][e], gr[k][e + 1]));
+                                    const float2 p23 =
+                                        __fmul2_rn(a2, make_float2(gr[k][e + 2], gr[k][e + 3]));
+                                    red_add_v4_if(ok, gp + vi * V + e, p01.x, p01.y, p23.x,
+                                                  p23.y);
+                                } else {
+                                    red_add_v4_if(ok, gp + vi * V + e, awc[c] * gr[k][e],
+                                                  awc[c] * gr[k][e + 1], awc[c] * gr[k][e + 2],
+                                                  awc[c] * gr[k][e + 3]);
+                                }
+                            }
+                        }
+                    } else if (awc[c] != 0.f && row_in_range(keys[c], num_keys)) {
                         float* gp = reinterpret_cast<float*>(
                             gvbase + (size_t)(unsigned)keys[c] * row_bytes32);
 #pragma unroll

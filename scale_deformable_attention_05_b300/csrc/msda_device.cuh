@@ -22,6 +22,8 @@
 // served by one cache line in the same load instruction.
 #pragma once
 
+#include <type_traits>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -317,6 +319,14 @@ struct VecIO<T, 8> {
     __device__ __forceinline__ static void load_stream(const T* p, float (&v)[kVec]) {
         unpack(__ldcs(reinterpret_cast<const uint2*>(p)), v);
     }
+    // round to nearest even, as the 16-byte stores
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+        if constexpr (std::is_same<T, __half>::value) return pack_half2(lo, hi);
+        else return pack_bf16x2(lo, hi);
+    }
+    __device__ __forceinline__ static void store(T* p, const float (&v)[kVec]) {
+        __stcs(reinterpret_cast<uint2*>(p), make_uint2(pack(v[0], v[1]), pack(v[2], v[3])));
+    }
 };
 
 template <typename T>
@@ -476,6 +486,14 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b),
                  "f"(c), "f"(d));
 #endif
+}
+
+// red_add_v4 under a predicate, one instruction (no branch around it).
+__device__ __forceinline__ void red_add_v4_if(bool pred, float* p, float a, float b, float c,
+                                              float d) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+                 "@q red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n\t}" ::"l"(p),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"((int)pred));
 }
 
 // Geometry of a warp tile for lane groups of kLanes lanes.

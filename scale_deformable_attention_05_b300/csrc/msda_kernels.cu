@@ -246,11 +246,12 @@ cudaError_t dispatch_forward_fused_ref(const Problem& pb, void* out, cudaStream_
     const Layout ly = fused_layout(pb, pb.D / IO<T>::kVec, 4);
     if constexpr (sizeof(T) == 2) {
         // The group is widened so one round holds the whole row of L*P samples;
-        // where 16-byte vectors of a 16-bit row would leave lanes of it idle,
-        // lanes read 8-byte vectors (four channels) instead.
-        if (ly.vpl == 1 && ly.lanes > pb.D / IO<T>::kVec && pb.D / 4 <= 32) {
-            const Layout l8 = fused_layout(pb, pb.D / 4, 4);
-            switch (l8.lanes) {
+        // where 16-byte vectors of a 16-bit row would leave lanes of it idle and
+        // 8-byte vectors (four channels a lane) fit the same group, lanes read
+        // those instead (more lanes busy at the same queries per warp).
+        if (ly.vpl == 1 && ly.lanes > pb.D / IO<T>::kVec && pb.D / 4 <= 32 &&
+            fused_layout(pb, pb.D / 4, 4).lanes == ly.lanes) {
+            switch (ly.lanes) {
                 case 4: return launch_forward_t<T, 4, 1, 8, kRef>(pb, out, st);
                 case 8: return launch_forward_t<T, 8, 1, 8, kRef>(pb, out, st);
                 case 16: return launch_forward_t<T, 16, 1, 8, kRef>(pb, out, st);

@@ -74,6 +74,9 @@ CASES = [
     ("bf16", 66, 2, ((9, 7), (5, 4)), 2, 32, 8, 11, "bf16", 2),
     ("f16-boxes", 67, 2, ((9, 7), (5, 4)), 2, 64, 4, 11, "f16", 4),
     ("odd-points", 68, 1, ((7, 5), (4, 3), (2, 2)), 2, 16, 3, 13, "f32", 2),
+    # 16-bit rows of 32 bytes in 4-lane groups of 8-byte vectors
+    ("bf16-narrow", 69, 2, ((9, 7), (5, 4)), 3, 16, 4, 13, "bf16", 2),
+    ("f16-narrow-boxes", 70, 1, ((8, 8), (4, 5)), 2, 16, 2, 9, "f16", 4),
 ]
 
 

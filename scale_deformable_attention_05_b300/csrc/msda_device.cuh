@@ -52,6 +52,10 @@ constexpr int kSamplesPerWarp = 64;
 // device code is compiled as the one translation unit msda_kernels.cu (no
 // relocatable device code).
 __device__ unsigned int g_error_word = 0;
+
+// 128 zero bytes: the row that dead corners and idle lanes of the narrow lane
+// groups (at most 8 lanes of at most 16 bytes) read instead of a predicated load.
+__device__ __align__(128) uint4 g_zero_row[8] = {};
 constexpr unsigned int kErrLevelOutOfRange = 1u;
 constexpr unsigned int kErrRowOutOfRange = 2u;
 

@@ -39,6 +39,15 @@ namespace msda {
 // Packed fp32 FMA (two channels per instruction) in the gather's accumulation of
 // 16-bit rows: bf16 encoder forward 303 -> 287 us; fp32 rows measured slower
 // (164.6 -> 166.3 us, the 64-register build spilled), so they keep scalar FMAs.
+// Plain 16-bit rows in groups of at most 8 lanes: dead corners and idle lanes
+// load the zero row (g_zero_row) instead of a predicated load into zero-filled
+// registers, which the ALU-bound widening of those rows felt (encoder forward
+// bf16 274 -> 262 us, fp16 283 -> 274 us).  Measured slower elsewhere: fp32 rows
+// (158 -> 162 us), the fused 16-bit forward (345 -> 367 us) and the backward
+// (fp32 393 -> 397 us, bf16 741 -> 805 us with 180 bytes of spills).
+#ifndef MSDA_FWD_ZERO_ROW
+#define MSDA_FWD_ZERO_ROW 1
+#endif
 #ifndef MSDA_FWD_PACKED
 #define MSDA_FWD_PACKED 1
 #endif
@@ -124,6 +133,8 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
                                 ? MSDA_FWD_UNROLL_F32_128
                                 : MSDA_FWD_UNROLL;
     constexpr bool kPackedFma = MSDA_FWD_PACKED != 0 && sizeof(T) == 2;
+    constexpr bool kZeroRow = MSDA_FWD_ZERO_ROW != 0 && sizeof(T) == 2 && kRef == 0 &&
+                              kVPL == 1 && kLanes <= 8 && kLanes * kVB <= 128;
     __shared__ LevelInfo s_levels[kMaxLevels];
     __shared__ unsigned char s_level_of[kMaxLevelPoints];
     constexpr int kWarps = MSDA_FWD_WARPS;
@@ -199,13 +210,21 @@ __global__ void __launch_bounds__(MSDA_FWD_WARPS * 32,
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const char* p = row_ptr(vbase, keys[c], row_bytes);
+                if constexpr (kZeroRow) {
+                    // dead corners and idle lanes read the zero row
+                    const bool live =
+                        keys[c] >= 0 && li < nvec && row_in_range(keys[c], num_keys);
+                    VIO::load((live ? p : reinterpret_cast<const char*>(g_zero_row)) + li * kVB,
+                              v[c][0]);
+                } else {
 #pragma unroll
-                for (int k = 0; k < kVPL; ++k) {
-                    const int vi = li + k * kLanes;
+                    for (int k = 0; k < kVPL; ++k) {
+                        const int vi = li + k * kLanes;
 #pragma unroll
-                    for (int e = 0; e < V; ++e) v[c][k][e] = 0.f;
-                    if (keys[c] >= 0 && vi < nvec && row_in_range(keys[c], num_keys))
-                        VIO::load(p + vi * kVB, v[c][k]);
+                        for (int e = 0; e < V; ++e) v[c][k][e] = 0.f;
+                        if (keys[c] >= 0 && vi < nvec && row_in_range(keys[c], num_keys))
+                            VIO::load(p + vi * kVB, v[c][k]);
+                    }
                 }
             }
 #pragma unroll

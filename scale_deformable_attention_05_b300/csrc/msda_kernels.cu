@@ -128,16 +128,17 @@ int persistent_waves(const Problem& pb, int elem_bytes, bool backward) {
 #define MSDA_SMEM_CARVEOUT -1
 #endif
 
-// CTAs of `kernel` that fit on one SM at once (looked up once per kernel).
-template <typename K>
-int resident_ctas(K kernel, int threads, size_t dynamic_smem = 0) {
-    static const int n = [&] {
+// CTAs of `Kernel` that fit on one SM at once, looked up once per kernel.  The
+// cache is keyed by the kernel itself: instantiations that differ only in their
+// template arguments share one function type but not their register counts.
+template <auto Kernel>
+int resident_ctas(int threads) {
+    static const int n = [threads] {
         if (MSDA_SMEM_CARVEOUT >= 0)
-            cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+            cudaFuncSetAttribute(Kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  MSDA_SMEM_CARVEOUT);
         int v = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, dynamic_smem) !=
-                cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, Kernel, threads, 0) != cudaSuccess ||
             v < 1)
             v = 1;
         return v;
@@ -169,9 +170,9 @@ template <typename T, int kLanes, int kVPL, int kVB, int kRef = 0>
 cudaError_t launch_forward_t(const Problem& pb, void* out, cudaStream_t st) {
     auto kernel = forward_kernel<T, kLanes, kVPL, kVB, kRef>;
     constexpr int kThreads = MSDA_FWD_WARPS * 32;
-    const TileGrid tg =
-        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_FWD_WARPS,
-                  persistent_waves(pb, (int)sizeof(T), false));
+    const int resident = resident_ctas<forward_kernel<T, kLanes, kVPL, kVB, kRef>>(kThreads);
+    const TileGrid tg = tile_grid(pb, 32 / kLanes, resident, MSDA_FWD_WARPS,
+                                  persistent_waves(pb, (int)sizeof(T), false));
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<T*>(out), pb.K, pb.M, pb.D, pb.L, pb.P, pb.Q,
@@ -186,9 +187,9 @@ cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv
     auto kernel = backward_kernel<T, kLanes, kVPL, kRef, kVB>;
     constexpr int kWarps = BwdShape<T, kLanes, kVPL, kRef>::kWarps;
     constexpr int kThreads = kWarps * 32;
-    const TileGrid tg =
-        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), kWarps,
-                  persistent_waves(pb, (int)sizeof(T), true));
+    const int resident = resident_ctas<backward_kernel<T, kLanes, kVPL, kRef, kVB>>(kThreads);
+    const TileGrid tg = tile_grid(pb, 32 / kLanes, resident, kWarps,
+                                  persistent_waves(pb, (int)sizeof(T), true));
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
@@ -293,9 +294,9 @@ cudaError_t launch_backward_merge_t(const Problem& pb, int log2_points, const vo
                                     cudaStream_t st) {
     auto kernel = backward_merge_kernel<T, kLanes, kVPL>;
     constexpr int kThreads = MSDA_MERGE_WARPS * 32;
-    const TileGrid tg =
-        tile_grid(pb, 32 / kLanes, resident_ctas(kernel, kThreads), MSDA_MERGE_WARPS,
-                  persistent_waves(pb, (int)sizeof(T), true));
+    const int resident = resident_ctas<backward_merge_kernel<T, kLanes, kVPL>>(kThreads);
+    const TileGrid tg = tile_grid(pb, 32 / kLanes, resident, MSDA_MERGE_WARPS,
+                                  persistent_waves(pb, (int)sizeof(T), true));
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,

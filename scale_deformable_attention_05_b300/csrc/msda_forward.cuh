@@ -39,6 +39,9 @@ namespace msda {
 // Packed fp32 FMA (two channels per instruction) in the gather's accumulation of
 // 16-bit rows: bf16 encoder forward 303 -> 287 us; fp32 rows measured slower
 // (164.6 -> 166.3 us, the 64-register build spilled), so they keep scalar FMAs.
+#ifndef MSDA_FWD_PACKED
+#define MSDA_FWD_PACKED 1
+#endif
 // Plain 16-bit rows in groups of at most 8 lanes: dead corners and idle lanes
 // load the zero row (g_zero_row) instead of a predicated load into zero-filled
 // registers, which the ALU-bound widening of those rows felt (encoder forward
@@ -47,9 +50,6 @@ namespace msda {
 // (fp32 393 -> 397 us, bf16 741 -> 805 us with 180 bytes of spills).
 #ifndef MSDA_FWD_ZERO_ROW
 #define MSDA_FWD_ZERO_ROW 1
-#endif
-#ifndef MSDA_FWD_PACKED
-#define MSDA_FWD_PACKED 1
 #endif
 #define MSDA_PRAGMA(x) _Pragma(#x)
 #define MSDA_UNROLL(n) MSDA_PRAGMA(unroll n)

@@ -126,12 +126,20 @@ __device__ __forceinline__ void corner_terms(int c, float fx, float fy, float& w
 #ifndef MSDA_BWD_NARROW_PREFETCH
 #define MSDA_BWD_NARROW_PREFETCH 0
 #endif
-template <typename T, int kLanes, int kVPL, int kRef>
+// fp32 rows also have a dense shape, 7 CTAs per SM at 72 registers, which the
+// launcher takes when the grid fills 7 CTAs on every SM: encoder backward 392 ->
+// 386 us; on grids of a few CTAs per SM (the decoder's 300) the 80-register
+// build is the faster one (32.7 against 36.9 us).
+#ifndef MSDA_BWD_NARROW_BLOCKS_DENSE
+#define MSDA_BWD_NARROW_BLOCKS_DENSE 7
+#endif
+template <typename T, int kLanes, int kVPL, int kRef, bool kDense = false>
 struct BwdShape {
     static constexpr bool kNarrow = kLanes <= 8 && kVPL == 1;
     static constexpr int kWarps = kNarrow ? MSDA_BWD_NARROW_WARPS : MSDA_BWD_WARPS;
     static constexpr int kMinBlocks = !kNarrow           ? 1
-                                      : sizeof(T) == 4   ? MSDA_BWD_NARROW_BLOCKS
+                                      : sizeof(T) == 4   ? (kDense ? MSDA_BWD_NARROW_BLOCKS_DENSE
+                                                                   : MSDA_BWD_NARROW_BLOCKS)
                                       : kRef != 0        ? MSDA_BWD_FUSED16_BLOCKS
                                                          : MSDA_BWD_NARROW_BLOCKS16;
 };
@@ -275,9 +283,9 @@ __device__ __forceinline__ void load_grad_row(float (&gr)[kVPL][VecIO<T, kVB>::k
 // 16-byte red.  (With eight 16-bit channels a lane sends two 16-byte reds,
 // each covering half of every 32-byte sector of the row; the bf16 encoder
 // backward measured 1298 us that way against 1207 us with 8-byte vectors.)
-template <typename T, int kLanes, int kVPL, int kRef, int kVB>
-__global__ void __launch_bounds__(BwdShape<T, kLanes, kVPL, kRef>::kWarps * 32,
-                                  BwdShape<T, kLanes, kVPL, kRef>::kMinBlocks)
+template <typename T, int kLanes, int kVPL, int kRef, int kVB, bool kDense = false>
+__global__ void __launch_bounds__(BwdShape<T, kLanes, kVPL, kRef, kDense>::kWarps * 32,
+                                  BwdShape<T, kLanes, kVPL, kRef, kDense>::kMinBlocks)
     backward_kernel(const T* __restrict__ value, const void* __restrict__ spatial_shapes,
                     const void* __restrict__ level_start_index, int idx32, const T* __restrict__ loc,
                     const T* __restrict__ attn, const T* __restrict__ grad_out,
@@ -287,7 +295,7 @@ __global__ void __launch_bounds__(BwdShape<T, kLanes, kVPL, kRef>::kWarps * 32,
                     int num_tiles, int tiles_per_cta, const T* __restrict__ ref,
                     const unsigned char* __restrict__ mask, float* __restrict__ grad_ref) {
     constexpr bool kPrep = kRef != 0;
-    constexpr int kWarps = BwdShape<T, kLanes, kVPL, kRef>::kWarps;
+    constexpr int kWarps = BwdShape<T, kLanes, kVPL, kRef, kDense>::kWarps;
     using Geom = TileGeom<kLanes>;
     using VIO = VecIO<T, kVB>;
     constexpr int kGroups = Geom::kGroups, kSPG = Geom::kSPG, kStride = Geom::kStride;
@@ -342,7 +350,7 @@ __global__ void __launch_bounds__(BwdShape<T, kLanes, kVPL, kRef>::kWarps * 32,
     it.stride = kWarps;
     if (!it.valid()) return;
 
-    constexpr bool kPrefetch = BwdShape<T, kLanes, kVPL, kRef>::kNarrow
+    constexpr bool kPrefetch = BwdShape<T, kLanes, kVPL, kRef, kDense>::kNarrow
                                    ? MSDA_BWD_NARROW_PREFETCH != 0
                                    : MSDA_BWD_PREFETCH != 0 || kPrep;
     SampleFetch f;

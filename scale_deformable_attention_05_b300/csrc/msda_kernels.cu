@@ -180,16 +180,12 @@ cudaError_t launch_forward_t(const Problem& pb, void* out, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <typename T, int kLanes, int kVPL, int kRef, int kVB>
-cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv32,
-                              void* grad_loc, void* grad_attn, cudaStream_t st,
-                              float* grad_ref = nullptr) {
-    auto kernel = backward_kernel<T, kLanes, kVPL, kRef, kVB>;
-    constexpr int kWarps = BwdShape<T, kLanes, kVPL, kRef>::kWarps;
-    constexpr int kThreads = kWarps * 32;
-    const int resident = resident_ctas<backward_kernel<T, kLanes, kVPL, kRef, kVB>>(kThreads);
-    const TileGrid tg = tile_grid(pb, 32 / kLanes, resident, kWarps,
-                                  persistent_waves(pb, (int)sizeof(T), true));
+template <typename T, int kLanes, int kVPL, int kRef, int kVB, bool kDense>
+cudaError_t launch_backward_shape(const Problem& pb, const TileGrid& tg, const void* grad_out,
+                                  float* gv32, void* grad_loc, void* grad_attn, cudaStream_t st,
+                                  float* grad_ref) {
+    auto kernel = backward_kernel<T, kLanes, kVPL, kRef, kVB, kDense>;
+    constexpr int kThreads = BwdShape<T, kLanes, kVPL, kRef, kDense>::kWarps * 32;
     kernel<<<tg.grid, kThreads, 0, st>>>(
         static_cast<const T*>(pb.value), pb.shapes, pb.lsi, pb.idx32, static_cast<const T*>(pb.loc),
         static_cast<const T*>(pb.attn), static_cast<const T*>(grad_out), gv32,
@@ -197,6 +193,30 @@ cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv
         pb.Q, tg.num_qtiles, tg.num_tiles, tg.tiles_per_cta, static_cast<const T*>(pb.ref),
         pb.mask, grad_ref);
     return cudaGetLastError();
+}
+
+template <typename T, int kLanes, int kVPL, int kRef, int kVB>
+cudaError_t launch_backward_t(const Problem& pb, const void* grad_out, float* gv32,
+                              void* grad_loc, void* grad_attn, cudaStream_t st,
+                              float* grad_ref = nullptr) {
+    constexpr int kWarps = BwdShape<T, kLanes, kVPL, kRef>::kWarps;
+    constexpr int kThreads = kWarps * 32;
+    const int waves = persistent_waves(pb, (int)sizeof(T), true);
+    if constexpr (sizeof(T) == 4 && BwdShape<T, kLanes, kVPL, kRef>::kNarrow) {
+        // the dense shape where its grid fills every SM's slots at least once
+        const int dense =
+            resident_ctas<backward_kernel<T, kLanes, kVPL, kRef, kVB, true>>(kThreads);
+        const TileGrid td = tile_grid(pb, 32 / kLanes, dense, kWarps, waves);
+        if ((int64_t)td.grid >= (int64_t)sm_count() * dense)
+            return launch_backward_shape<T, kLanes, kVPL, kRef, kVB, true>(pb, td, grad_out, gv32,
+                                                                           grad_loc, grad_attn, st,
+                                                                           grad_ref);
+    }
+    const int resident = resident_ctas<backward_kernel<T, kLanes, kVPL, kRef, kVB>>(kThreads);
+    const TileGrid tg = tile_grid(pb, 32 / kLanes, resident, kWarps, waves);
+    return launch_backward_shape<T, kLanes, kVPL, kRef, kVB, false>(pb, tg, grad_out, gv32,
+                                                                    grad_loc, grad_attn, st,
+                                                                    grad_ref);
 }
 
 #ifndef MSDA_FWD_VEC32

@@ -143,10 +143,12 @@ struct BwdShape {
                                       : kRef != 0        ? MSDA_BWD_FUSED16_BLOCKS
                                                          : MSDA_BWD_NARROW_BLOCKS16;
 };
-// backward_merge_kernel: CTAs of MSDA_MERGE_WARPS warps (its 1 KB rows
-// measured 10% slower with 24 warps of 80 registers; CTAs of 8 warps instead of
-// one of 16, the same warps per SM: envelope backward 2481 -> 2417 us,
-// kernel-only).
+// backward_merge_kernel: one CTA of MSDA_MERGE_WARPS warps per SM, whose
+// threads may then hold up to 255 registers.  Its 1 KB rows measured slower
+// with more warps of fewer registers (kernel-only, envelope backward): one CTA
+// of 16 warps at 128 registers 2481 us, one of 8 warps 2417 us, two of 8 warps
+// at 128 registers (62 bytes of spills) 2493 us, three 2734 us, 24 warps of 80
+// registers 10% slower.
 #ifndef MSDA_MERGE_WARPS
 #define MSDA_MERGE_WARPS 8
 #endif

@@ -31,6 +31,8 @@ CASES = [
     (203, 2, ((5, 6), (3, 3)), 2, 64, 2, 9, "bf16"),
     (204, 1, ((8, 8), (4, 4)), 1, 256, 16, 5, "f32"),      # merge kernel (one group per warp)
     (205, 2, ((6, 5), (3, 2)), 2, 16, 3, 11, "f16"),
+    # fp32 backward's dense shape: 4,400 tiles in a grid of 1,100 CTAs, 7 per SM on 148 SMs
+    (206, 2, ((60, 80), (30, 40)), 8, 32, 4, 1100, "f32"),
 ]
 
 
